@@ -1,0 +1,441 @@
+"""Benchmark of the Gated DeltaNet forward on GB300 (one JSON line on stdout).
+
+A step is one prefill layer pass of the hot path on the long-context workload
+(B=1, T=65536, H=16, HV=32, K=V=128, fp32 initial and final state):
+    gdn_gating (a, b -> g, beta)  then  gdn_chunk_fwd (q, k, v, g, beta, h0 -> o, h_T)
+with every input resident in HBM.  The inputs (1.6 GB) exceed the 129 MB L2,
+so no explicit flush is needed between steps.  Decode (256 requests against a
+[512, 32, 128, 128] fp32 pool, fused gating) and gating alone are timed
+separately and reported as sub-objects.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+For N > 1 (torchrun, one rank per GPU) every rank runs its own replica of the
+workload (no data-path collective: independent sequences) and the value is the
+tokens of all ranks divided by the slowest rank's time ("scaling": "weak").
+``--impl reference`` times the fp64 CPU oracle (the only reference this
+method has) on a bounded sample of the same workload, on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN chunk fwd tokens/s (1×GB300) and % of roofline; decode state GB/s"
+C = 64
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--e2e-steps", type=int, default=3)
+    p.add_argument("--cpu-tokens", type=int, default=16384,
+                   help="tokens of the workload (all heads) in the CPU oracle sample")
+    p.add_argument("--no-extras", action="store_true", help="skip e2e, CPU baseline, decode, gating")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ----------------------------------------------------------- algorithmic counts
+
+def prefill_bytes(B, T, H, HV, K, V, N, h0=True, ht=True):
+    tok = B * T
+    b = tok * (2 * H * K * 2 + HV * V * 2 + 2 * HV * 4 + HV * V * 2)
+    st = N * HV * K * V * 4
+    return b + (st if h0 else 0) + (st if ht else 0)
+
+
+def prefill_flops(tokens, H, HV, K, V):
+    G = HV // H
+    per = 6 * K * V + C * K + 2 * C * V + 2 * C * K / G + C * C / 3
+    return tokens * HV * per
+
+
+def gating_bytes(n_elem):
+    return n_elem * (2 + 2 + 4 + 4)
+
+
+# ------------------------------------------------------------------- clocks
+
+class Clocks:
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="gdn_clocks_", suffix=".csv")
+            os.close(fd)
+            q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- reference
+
+def cpu_oracle_sample(case, g, beta, tokens):
+    """Time the fp64 oracle (as it stands) on the first ``tokens`` tokens of the
+    workload, all heads, all host cores.  Returns (tokens/s, seconds, threads)."""
+    import numpy as np
+    import oracle
+    sl = slice(0, tokens)
+    f = lambda t: np.ascontiguousarray(t[:, sl].to("cpu").double().numpy())
+    q, k, v = f(case.q), f(case.k), f(case.v)
+    gg = np.ascontiguousarray(g[:, sl].double().cpu().numpy())
+    bb = np.ascontiguousarray(beta[:, sl].double().cpu().numpy())
+    h0 = case.initial_state.double().numpy()
+    threads = oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.recurrent(q, k, v, gg, bb, initial_state=h0, nthreads=threads)
+    dt = time.perf_counter() - t0
+    return tokens / dt, dt, threads
+
+
+def gates_for_cpu(case):
+    import numpy as np
+    import torch
+    import oracle
+    g, b = oracle.gating(case.A_log, case.a, case.b, case.dt_bias)
+    shp = (case.B, case.T, case.HV)
+    return (torch.from_numpy(g.astype(np.float32)).reshape(shp),
+            torch.from_numpy(b.astype(np.float32)).reshape(shp))
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from gated_deltanet_chunked_chunk_gb300 import workloads as W
+    case = W.config3()
+    tokens = min(args.cpu_tokens, case.T)
+    # the oracle's own gating (fp64, rounded to fp32) feeds its recurrence
+    g, beta = gates_for_cpu(case)
+    for _ in range(args.warmup):
+        cpu_oracle_sample(case, g, beta, tokens)
+    times = []
+    for _ in range(args.steps):
+        _, dt, threads = cpu_oracle_sample(case, g, beta, tokens)
+        times.append(dt)
+    tot = sum(times)
+    value = tokens * args.steps / tot
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(case, "reference: fp64 CPU oracle, per-token recurrence"),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"first {tokens} of {case.T} tokens, all {case.HV} value heads, per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(case, note=""):
+    return {"workload": f"long-context prefill B={case.B} T={case.T} H={case.H} HV={case.HV} "
+                        f"K={case.K} V={case.V}, fp32 initial+final state, l2norm on, chunk 64",
+            "global_batch": case.B, "seq_len": case.T, "parallelism": "replicas",
+            "l2_flush": "inputs larger than L2 (1.6 GB vs 129 MB)", "note": note}
+
+
+# ---------------------------------------------------------------------- ours
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import gated_deltanet_chunked_chunk_gb300 as gdn
+    from gated_deltanet_chunked_chunk_gb300 import build as gbuild
+    from gated_deltanet_chunked_chunk_gb300 import workloads as W
+
+    gbuild.build()
+    gdn.load_library()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    hbm, bf16_burst, bf16_sust, peak_src = peaks()
+
+    case = W.config3()
+    B, T, H, HV, K, V, N = case.B, case.T, case.H, case.HV, case.K, case.V, case.N
+    d = lambda t: t.to(dev).contiguous()
+    q, k, v = d(case.q), d(case.k), d(case.v)
+    A_log, dt_bias, a, b = d(case.A_log), d(case.dt_bias), d(case.a), d(case.b)
+    h0 = d(case.initial_state)
+    g = torch.empty(B * T, HV, device=dev)
+    beta = torch.empty(B * T, HV, device=dev)
+    o = torch.empty(B, T, HV, V, dtype=torch.bfloat16, device=dev)
+    ht = torch.empty(N, HV, K, V, device=dev)
+    ws_bytes = gdn.chunk_fwd_workspace_size(B, T, H, HV, K, V, N, False)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev) if ws_bytes else None
+
+    def step(ev=None):
+        gdn.gdn_gating(A_log, a, b, dt_bias, g=g, beta=beta)
+        if ev is not None:
+            ev[0].record(stream)
+        gdn.gdn_chunk_fwd(q, k, v, g.view(B, T, HV), beta.view(B, T, HV), initial_state=h0,
+                          o=o, final_state=ht, workspace=ws)
+        if ev is not None:
+            ev[1].record(stream)
+
+    launches_per_step = 2  # gating kernel + chunk kernel
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = Clocks(local_rank)
+    barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop()
+    ms = t_start.elapsed_time(t_end)
+    chunk_ms = [a_.elapsed_time(b_) for a_, b_ in evs]
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    tokens = B * T
+    value = tokens * world / (ms_per_step / 1e3)
+
+    chunk_avg_ms = sum(chunk_ms) / len(chunk_ms)
+    alg_b = prefill_bytes(B, T, H, HV, K, V, N)
+    alg_f = prefill_flops(tokens, H, HV, K, V)
+    achieved = alg_b / (chunk_avg_ms / 1e3) / 1e9
+    roof_ms = max(alg_b / (hbm * 1e9), alg_f / (bf16_sust * 1e12)) * 1e3
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "chunk_traffic.json")
+    if os.path.exists(tpath):
+        try:
+            tj = json.load(open(tpath))
+            if tj.get("kernel_source_sha") == kernel_source_sha():
+                traffic = tj.get("traffic_bytes_per_launch")
+        except Exception:
+            traffic = None
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(case, "step = gdn_gating + gdn_chunk_fwd; inputs resident in HBM"),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": traffic, "kernel": "gdn_chunk_fwd",
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else peak_src,
+                     "kernel_ms": chunk_avg_ms, "alg_bytes_per_launch": alg_b,
+                     "alg_flops_per_launch": alg_f,
+                     "tensor_frac_of_sustained": alg_f / (chunk_avg_ms / 1e3) / (bf16_sust * 1e12),
+                     "roofline_ms": roof_ms, "frac_of_roofline_time": roof_ms / chunk_avg_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+
+    if not args.no_extras:
+        line["decode"] = bench_decode(dev, stream, hbm, args)
+        line["gating"] = bench_gating(dev, stream, hbm, args)
+        line["e2e"] = bench_e2e(case, dev, stream, args, world)
+        if rank == 0 and world == 1:
+            gg, bb = gates_for_cpu(case)
+            cps, dt, threads = cpu_oracle_sample(case, gg, bb, min(args.cpu_tokens, T))
+            line["cpu_baseline"] = {"value": cps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                                    "sample": f"first {min(args.cpu_tokens, T)} of {T} tokens, all {HV} "
+                                              f"value heads ({dt:.1f} s)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def kernel_source_sha():
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gated_deltanet_chunked_chunk_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.startswith("gdn_chunk") and (f.endswith(".cu") or f.endswith(".cuh")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def bench_decode(dev, stream, hbm, args):
+    import torch
+    import gated_deltanet_chunked_chunk_gb300 as gdn
+    from gated_deltanet_chunked_chunk_gb300 import workloads as W
+    dc = W.config4()
+    d = lambda t: t.to(dev).contiguous()
+    q, k, v, idx = d(dc.q), d(dc.k), d(dc.v), d(dc.ssm_indices)
+    A_log, a, b, dt = d(dc.A_log), d(dc.a), d(dc.b), d(dc.dt_bias)
+    pool = d(dc.ssm_pool)
+    o = torch.empty(dc.R, 1, dc.HV, dc.V, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)  # 256 MB > L2
+
+    def call():
+        gdn.gdn_recurrent_decode(q, k, v, pool, idx, A_log=A_log, a=a, b=b, dt_bias=dt, o=o)
+    for _ in range(3):
+        call()
+    times = []
+    for _ in range(max(args.steps, 10)):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(e0.elapsed_time(e1))
+    ms = statistics.median(times)
+    valid = int((dc.ssm_indices >= 0).sum())
+    state_b = 2 * valid * dc.HV * dc.K * dc.V * 4
+    io_b = dc.R * (2 * dc.H * dc.K * 2 + dc.HV * dc.V * 2 * 2 + dc.HV * 2 * 2) + dc.R * 4
+    gbs = (state_b + io_b) / (ms / 1e3) / 1e9
+    return {"workload": "decode R=256 (valid %d) pool [512,32,128,128] fp32, fused gating" % valid,
+            "ms": ms, "state_GBps": state_b / (ms / 1e3) / 1e9, "achieved_GBps": gbs, "peak": hbm,
+            "frac": gbs / hbm, "requests_per_s": dc.R / (ms / 1e3), "l2_flush": "256 MB memset before each call"}
+
+
+def bench_gating(dev, stream, hbm, args):
+    import torch
+    import gated_deltanet_chunked_chunk_gb300 as gdn
+    n_tok, HV = 65536 * 8, 32
+    gen = torch.Generator().manual_seed(5)
+    a = torch.randn(n_tok, HV, generator=gen).to(torch.bfloat16).to(dev)
+    b = torch.randn(n_tok, HV, generator=gen).to(torch.bfloat16).to(dev)
+    A_log = torch.zeros(HV, device=dev)
+    dt = torch.zeros(HV, device=dev)
+    g = torch.empty(n_tok, HV, device=dev)
+    be = torch.empty(n_tok, HV, device=dev)
+    for _ in range(3):
+        gdn.gdn_gating(A_log, a, b, dt, g=g, beta=be)
+    times = []
+    for _ in range(max(args.steps, 10)):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        gdn.gdn_gating(A_log, a, b, dt, g=g, beta=be)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(e0.elapsed_time(e1))
+    ms = statistics.median(times)
+    gbs = gating_bytes(n_tok * HV) / (ms / 1e3) / 1e9
+    return {"workload": f"gating {n_tok}x{HV} (bf16 a,b -> fp32 g,beta; 200 MB in+out > L2)",
+            "ms": ms, "achieved_GBps": gbs, "peak": hbm, "frac": gbs / hbm}
+
+
+def bench_e2e(case, dev, stream, args, world):
+    """Same step through the public API, from pinned host buffers: H2D of every
+    input, gating + chunk forward, D2H of o and the final state, per step."""
+    import torch
+    import gated_deltanet_chunked_chunk_gb300 as gdn
+    B, T, H, HV, K, V, N = case.B, case.T, case.H, case.HV, case.K, case.V, case.N
+    host_in = [t.contiguous().pin_memory() for t in (case.q, case.k, case.v, case.a, case.b,
+                                                      case.A_log, case.dt_bias, case.initial_state)]
+    dev_in = [torch.empty_like(t, device=dev) for t in host_in]
+    o_h = torch.empty(B, T, HV, V, dtype=torch.bfloat16).pin_memory()
+    ht_h = torch.empty(N, HV, K, V).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = o_h.numel() * 2 + ht_h.numel() * 4
+
+    def step():
+        for hsrc, ddst in zip(host_in, dev_in):
+            ddst.copy_(hsrc, non_blocking=True)
+        q, k, v, a, b, A_log, dt, h0 = dev_in
+        g, beta = gdn.gdn_gating(A_log, a, b, dt)
+        o, ht = gdn.gdn_chunk_fwd(q, k, v, g.view(B, T, HV), beta.view(B, T, HV), initial_state=h0)
+        o_h.copy_(o, non_blocking=True)
+        ht_h.copy_(ht, non_blocking=True)
+    step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / args.e2e_steps
+    return {"value": B * T * world / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    run_ours(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,246 @@
+"""Gated DeltaNet forward on one GB300: Python binding of libgdn's C ABI.
+
+Three entry points, same names as the C ABI (``include/gdn.h``):
+
+* ``gdn_gating(A_log, a, b, dt_bias) -> (g, beta)``
+* ``gdn_chunk_fwd(q, k, v, g, beta, ...) -> (o, final_state)``
+* ``gdn_recurrent_decode(q, k, v, ..., ssm_pool, ssm_indices) -> o``
+
+This module only marshals arguments: it checks devices, dtypes and
+contiguity, allocates outputs with ``torch.empty`` and passes raw pointers and
+the current CUDA stream to the shared library.  Every step of the computation
+runs in libgdn's CUDA kernels; if the library is missing the calls raise, there
+is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+__all__ = ["gdn_gating", "gdn_chunk_fwd", "gdn_recurrent_decode", "chunk_fwd_workspace_size",
+           "GDNError", "lib_path", "load_library", "status_string", "DEV_BAD_CU_SEQLENS",
+           "DEV_BAD_SLOT", "DEV_WAIT_TIMEOUT", "EXPORTED_SYMBOLS"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "_build", "libgdn.so")
+_lib = None
+_lock = threading.Lock()
+
+GDN_OK, GDN_EINVAL, GDN_EUNSUPPORTED, GDN_ECUDA, GDN_EWORKSPACE = 0, 1, 2, 3, 4
+DEV_BAD_CU_SEQLENS, DEV_BAD_SLOT, DEV_WAIT_TIMEOUT = 1, 2, 4
+
+#: Every symbol include/gdn.h declares (checked by the tests).
+EXPORTED_SYMBOLS = ("gdn_status_string", "gdn_version", "gdn_gating", "gdn_chunk_fwd_workspace_size",
+                    "gdn_chunk_fwd", "gdn_recurrent_decode")
+
+
+class GDNError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn}: {status_string(code)} (status {code})")
+        self.code = code
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libgdn.so (built by ``build.py``); raise if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"libgdn.so not found at {_LIB_PATH}; build it first "
+                               "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, I, I64, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+        lib.gdn_status_string.argtypes = [I]
+        lib.gdn_status_string.restype = ctypes.c_char_p
+        lib.gdn_version.argtypes = []
+        lib.gdn_version.restype = I
+        lib.gdn_gating.argtypes = [P, P, P, P, I64, I, P, P, P]
+        lib.gdn_gating.restype = I
+        lib.gdn_chunk_fwd_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
+        lib.gdn_chunk_fwd_workspace_size.restype = SZ
+        lib.gdn_chunk_fwd.argtypes = [P, P, P, P, P, F, P, P, I, I, I, I, I, I, I, I, P, P, P, SZ, P, P]
+        lib.gdn_chunk_fwd.restype = I
+        lib.gdn_recurrent_decode.argtypes = [P, P, P, P, P, P, P, P, P, F, I, P, I, P, I, I, I, I, I,
+                                             P, P, P]
+        lib.gdn_recurrent_decode.restype = I
+        _lib = lib
+        return lib
+
+
+def status_string(code: int) -> str:
+    try:
+        return load_library().gdn_status_string(int(code)).decode()
+    except RuntimeError:
+        return f"status {code}"
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check(t, name, dtype, device, ndim=None):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (the library does not copy)")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+
+
+def _scale_arg(scale) -> float:
+    return -1.0 if scale is None else float(scale)
+
+
+def gdn_gating(A_log: torch.Tensor, a: torch.Tensor, b: torch.Tensor, dt_bias: torch.Tensor,
+               g: Optional[torch.Tensor] = None, beta: Optional[torch.Tensor] = None):
+    """g = -exp(A_log) * softplus(a + dt_bias), beta = sigmoid(b); fp32 [Ttok, HV].
+
+    A_log, dt_bias: fp32 [HV]; a, b: bf16 [Ttok, HV].  ``g``/``beta`` may be
+    passed to write into existing fp32 buffers."""
+    dev = a.device
+    HV = A_log.numel()
+    _check(A_log, "A_log", torch.float32, dev)
+    _check(dt_bias, "dt_bias", torch.float32, dev)
+    _check(a, "a", torch.bfloat16, dev)
+    _check(b, "b", torch.bfloat16, dev)
+    if a.shape != b.shape or a.numel() % max(HV, 1) != 0 or a.shape[-1] != HV or dt_bias.numel() != HV:
+        raise ValueError("gdn_gating: a, b must be [Ttok, HV] and A_log, dt_bias [HV]")
+    Ttok = a.numel() // HV
+    if g is None:
+        g = torch.empty(a.shape, dtype=torch.float32, device=dev)
+    if beta is None:
+        beta = torch.empty(a.shape, dtype=torch.float32, device=dev)
+    _check(g, "g", torch.float32, dev)
+    _check(beta, "beta", torch.float32, dev)
+    rc = load_library().gdn_gating(_ptr(A_log), _ptr(a), _ptr(b), _ptr(dt_bias), Ttok, HV,
+                                   _ptr(g), _ptr(beta), _stream(dev))
+    if rc != GDN_OK:
+        raise GDNError("gdn_gating", rc)
+    return g, beta
+
+
+def chunk_fwd_workspace_size(B, T, H, HV, K, V, N, varlen) -> int:
+    return int(load_library().gdn_chunk_fwd_workspace_size(B, T, H, HV, K, V, N, int(bool(varlen))))
+
+
+def gdn_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                  beta: torch.Tensor, scale: Optional[float] = None,
+                  initial_state: Optional[torch.Tensor] = None, output_final_state: bool = True,
+                  cu_seqlens: Optional[torch.Tensor] = None, use_qk_l2norm: bool = True,
+                  num_seqs: Optional[int] = None, dev_status: Optional[torch.Tensor] = None,
+                  o: Optional[torch.Tensor] = None, final_state: Optional[torch.Tensor] = None,
+                  workspace: Optional[torch.Tensor] = None
+                  ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Chunked prefill.  q, k bf16 [B,T,H,K]; v bf16 [B,T,HV,V]; g, beta fp32
+    [B,T,HV]; initial_state fp32 [N,HV,K,V] or None; cu_seqlens int32 [N+1]
+    (device) with B = 1, or None.  Returns (o bf16 [B,T,HV,V], final_state fp32
+    [N,HV,K,V] or None).  ``num_seqs`` gives N for varlen input without a
+    device-to-host read (default: cu_seqlens.numel() - 1, a host-side size)."""
+    dev = q.device
+    for t, n, dt in ((q, "q", torch.bfloat16), (k, "k", torch.bfloat16), (v, "v", torch.bfloat16),
+                     (g, "g", torch.float32), (beta, "beta", torch.float32)):
+        _check(t, n, dt, dev)
+    if q.dim() != 4 or k.shape != q.shape or v.dim() != 4 or v.shape[:2] != q.shape[:2]:
+        raise ValueError("gdn_chunk_fwd: q, k must be [B,T,H,K] and v [B,T,HV,V]")
+    B, T, H, K = q.shape
+    HV, V = v.shape[2], v.shape[3]
+    if tuple(g.shape) != (B, T, HV) or tuple(beta.shape) != (B, T, HV):
+        raise ValueError(f"gdn_chunk_fwd: g and beta must be [B,T,HV] = {(B, T, HV)}")
+    if cu_seqlens is not None:
+        _check(cu_seqlens, "cu_seqlens", torch.int32, dev, ndim=1)
+        N = int(num_seqs) if num_seqs is not None else cu_seqlens.numel() - 1
+    else:
+        N = B
+    if initial_state is not None:
+        _check(initial_state, "initial_state", torch.float32, dev)
+        if tuple(initial_state.shape) != (N, HV, K, V):
+            raise ValueError(f"initial_state must be [N,HV,K,V] = {(N, HV, K, V)}")
+    if o is None:
+        o = torch.empty((B, T, HV, V), dtype=torch.bfloat16, device=dev)
+    _check(o, "o", torch.bfloat16, dev)
+    if output_final_state and final_state is None:
+        final_state = torch.empty((N, HV, K, V), dtype=torch.float32, device=dev)
+    if final_state is not None:
+        _check(final_state, "final_state", torch.float32, dev)
+    if dev_status is not None:
+        _check(dev_status, "dev_status", torch.int32, dev)
+    ws_bytes = chunk_fwd_workspace_size(B, T, H, HV, K, V, N, cu_seqlens is not None)
+    if ws_bytes > 0 and workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    rc = load_library().gdn_chunk_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _scale_arg(scale), _ptr(initial_state),
+        _ptr(cu_seqlens), N, B, T, H, HV, K, V, int(bool(use_qk_l2norm)), _ptr(o),
+        _ptr(final_state), _ptr(workspace), 0 if workspace is None else workspace.numel(),
+        _ptr(dev_status), _stream(dev))
+    if rc != GDN_OK:
+        raise GDNError("gdn_chunk_fwd", rc)
+    return o, final_state
+
+
+def gdn_recurrent_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                         ssm_pool: torch.Tensor, ssm_indices: torch.Tensor,
+                         g: Optional[torch.Tensor] = None, beta: Optional[torch.Tensor] = None,
+                         A_log: Optional[torch.Tensor] = None, a: Optional[torch.Tensor] = None,
+                         b: Optional[torch.Tensor] = None, dt_bias: Optional[torch.Tensor] = None,
+                         scale: Optional[float] = None, use_qk_l2norm: bool = True,
+                         dev_status: Optional[torch.Tensor] = None,
+                         o: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """One-token decode against ``ssm_pool`` [P,HV,K,V] fp32 (updated in place).
+
+    q, k bf16 [R,1,H,K]; v bf16 [R,1,HV,V]; ssm_indices int32 [R] (-1 = PAD).
+    Gates: either g, beta fp32 [R,HV], or A_log, dt_bias fp32 [HV] with a, b bf16
+    [R,HV] (fused gating).  Returns o bf16 [R,1,HV,V]."""
+    if ssm_pool is None or ssm_indices is None:
+        raise ValueError("gdn_recurrent_decode: ssm_pool and ssm_indices are required")
+    dev = q.device
+    for t, n, dt in ((q, "q", torch.bfloat16), (k, "k", torch.bfloat16), (v, "v", torch.bfloat16),
+                     (ssm_pool, "ssm_pool", torch.float32), (ssm_indices, "ssm_indices", torch.int32)):
+        _check(t, n, dt, dev)
+    if q.dim() != 4 or q.shape[1] != 1 or k.shape != q.shape or v.dim() != 4 or v.shape[:2] != q.shape[:2]:
+        raise ValueError("gdn_recurrent_decode: q, k must be [R,1,H,K] and v [R,1,HV,V]")
+    R, _, H, K = q.shape
+    HV, V = v.shape[2], v.shape[3]
+    if ssm_pool.dim() != 4 or tuple(ssm_pool.shape[1:]) != (HV, K, V):
+        raise ValueError(f"ssm_pool must be [P,{HV},{K},{V}]")
+    if ssm_indices.numel() != R:
+        raise ValueError("ssm_indices must have one entry per request")
+    for t, n, dt in ((g, "g", torch.float32), (beta, "beta", torch.float32),
+                     (A_log, "A_log", torch.float32), (dt_bias, "dt_bias", torch.float32),
+                     (a, "a", torch.bfloat16), (b, "b", torch.bfloat16)):
+        _check(t, n, dt, dev)
+    if o is None:
+        o = torch.empty((R, 1, HV, V), dtype=torch.bfloat16, device=dev)
+    _check(o, "o", torch.bfloat16, dev)
+    if dev_status is not None:
+        _check(dev_status, "dev_status", torch.int32, dev)
+    rc = load_library().gdn_recurrent_decode(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A_log), _ptr(a), _ptr(b), _ptr(dt_bias),
+        _scale_arg(scale), int(bool(use_qk_l2norm)), _ptr(ssm_pool), ssm_pool.shape[0],
+        _ptr(ssm_indices), R, H, HV, K, V, _ptr(o), _ptr(dev_status), _stream(dev))
+    if rc != GDN_OK:
+        raise GDNError("gdn_recurrent_decode", rc)
+    return o
+
+
+# Short aliases mirroring the pages' Python names.
+chunk_gated_delta_rule = gdn_chunk_fwd
+fused_gdn_gating = gdn_gating

@@ -1,0 +1,73 @@
+// gdn_common.cuh -- small device helpers shared by the libgdn kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gdn.h"
+
+#define GDN_CHUNK 64
+#define GDN_L2_EPS 1e-6f
+
+namespace gdn {
+
+__device__ __forceinline__ float bf2f(uint16_t x) {
+  return __uint_as_float(static_cast<uint32_t>(x) << 16);
+}
+
+__device__ __forceinline__ uint16_t f2bf(float x) {
+  __nv_bfloat16 h = __float2bfloat16_rn(x);
+  return *reinterpret_cast<uint16_t *>(&h);
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// softplus(x) = log1p(exp(x)), and x itself above 20 (where the two agree
+// to well under one fp32 ulp).
+__device__ __forceinline__ float softplus_f(float x) {
+  return x > 20.f ? x : log1pf(expf(x));
+}
+
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + expf(-x)); }
+
+__device__ __forceinline__ void set_status(int32_t *st, int bits) {
+  if (st) atomicOr(st, bits);
+}
+
+}  // namespace gdn
+
+// Host-side launchers implemented in the kernel translation units.
+namespace gdn_host {
+cudaError_t launch_gating(const float *A_log, const uint16_t *a,
+                          const uint16_t *b, const float *dt_bias,
+                          int64_t Ttok, int HV, float *g, float *beta,
+                          cudaStream_t s);
+cudaError_t launch_decode(const uint16_t *q, const uint16_t *k,
+                          const uint16_t *v, const float *g, const float *beta,
+                          const float *A_log, const uint16_t *a,
+                          const uint16_t *b, const float *dt_bias, float scale,
+                          int l2, float *pool, int P, const int32_t *idx, int R,
+                          int H, int HV, int K, int V, uint16_t *o,
+                          int32_t *dev_status, cudaStream_t s);
+struct ChunkArgs {
+  const uint16_t *q, *k, *v;
+  const float *g, *beta;
+  float scale;
+  const float *h0;
+  const int32_t *cu;
+  int N, B, T, H, HV, K, V, l2;
+  uint16_t *o;
+  float *ht;
+  void *ws;
+  size_t ws_bytes;
+  int32_t *dev_status;
+};
+size_t chunk_workspace_bytes(int B, int T, int H, int HV, int K, int V, int N,
+                             int varlen);
+cudaError_t launch_chunk(const ChunkArgs &a, cudaStream_t s);
+}  // namespace gdn_host

@@ -1,0 +1,163 @@
+/*
+ * gdn.h -- C ABI of libgdn: the Gated DeltaNet forward on one GB300 (sm_103a).
+ *
+ * Operation (shared by all entry points).  For one sequence and one value
+ * head hv, with key head h = hv / (HV / H) (contiguous grouped value heads,
+ * the usual repeat-interleave expansion; the FastDeploy PR "support fla
+ * triton kernel for qwen3.5", Usage section 1, states HV >= H for GVA and the
+ * LightLLM "gdn.py" backend requires HV % H == 0):
+ *
+ *     a_t = exp(g_t)
+ *     S_t = a_t S_{t-1} + beta_t k_t (v_t - a_t S_{t-1}^T k_t)^T      S in R^{K x V}
+ *     o_t = scale * S_t^T q_t
+ *
+ * g is the log-space forget gate and beta the delta-update strength ("NPU
+ * Training Operators - GDN", section "Operator semantics").  With
+ * use_qk_l2norm != 0, q and k are first replaced per token by
+ * x / sqrt(sum(x^2) + 1e-6).  States are fp32 and laid out [.., HV, K, V]
+ * (S[k][v], v fastest).
+ *
+ * Conventions for every entry point:
+ *  - Pointers are DEVICE pointers unless stated otherwise; buffers are dense
+ *    and contiguous in the stated layout (the library checks nothing it cannot
+ *    see: it does not copy, and it does not check strides).  bf16 tensors are
+ *    passed as uint16_t bit patterns.
+ *  - The caller owns every buffer.  The library never allocates or frees
+ *    device memory.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and returns without synchronising.  Host-side checks happen
+ *    before any launch; on error nothing is enqueued.
+ *  - Return value: GDN_OK, or a GDN_E* code; gdn_status_string() gives text.
+ *  - dev_status (optional, may be NULL): an int32 in device memory into which
+ *    kernels OR GDN_DEV_* bits for problems only the device can see.  Kernels
+ *    never trap.  The caller zeroes it and reads it back when it wishes.
+ *  - Supported head dims: K, V in {64, 128}.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum gdn_status_code {
+  GDN_OK = 0,
+  GDN_EINVAL = 1,        /* null required pointer, bad shape, HV % H != 0, ... */
+  GDN_EUNSUPPORTED = 2,  /* K or V outside {64, 128}, no sm_103a device, ... */
+  GDN_ECUDA = 3,         /* a CUDA call or kernel launch failed */
+  GDN_EWORKSPACE = 4     /* workspace missing or smaller than required */
+};
+
+/* Bits OR-ed into *dev_status by kernels. */
+enum gdn_device_status_bits {
+  GDN_DEV_BAD_CU_SEQLENS = 1, /* cu_seqlens not non-decreasing from 0, or past T */
+  GDN_DEV_BAD_SLOT = 2,       /* decode slot index < -1 or >= P (row treated as PAD) */
+  GDN_DEV_WAIT_TIMEOUT = 4    /* a bounded wait inside a kernel gave up */
+};
+
+/* Static text for a gdn_status_code.  Never NULL. */
+const char *gdn_status_string(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int gdn_version(void);
+
+/*
+ * gdn_gating -- fused gate computation, one launch.
+ * FastDeploy PR "support fla triton kernel for qwen3.5", Usage section 5
+ * ("Fused GDN Gating"):
+ *     g    = -exp(A_log[h]) * softplus(a + dt_bias[h])
+ *     beta = sigmoid(b)
+ * with softplus(x) = log1p(exp(x)), taken as x for x > 20.
+ *
+ *   A_log, dt_bias : fp32 [HV]
+ *   a, b           : bf16 [Ttok, HV]  (row-major, head fastest)
+ *   g, beta        : fp32 [Ttok, HV]  outputs
+ * Ttok = 0 is a no-op.  Errors: GDN_EINVAL for null pointers or HV <= 0.
+ */
+int gdn_gating(const float *A_log, const uint16_t *a, const uint16_t *b,
+               const float *dt_bias, int64_t Ttok, int HV, float *g,
+               float *beta, void *stream);
+
+/*
+ * gdn_chunk_fwd_workspace_size -- bytes of device workspace gdn_chunk_fwd
+ * needs for these sizes (0 means none; pass workspace = NULL then).
+ */
+size_t gdn_chunk_fwd_workspace_size(int B, int T, int H, int HV, int K, int V,
+                                    int N, int varlen);
+
+/*
+ * gdn_chunk_fwd -- chunked prefill (chunk size 64).
+ * FastDeploy PR "support fla triton kernel for qwen3.5", Usage section 1
+ * (chunk_gated_delta_rule with initial_state / output_final_state /
+ * use_qk_l2norm_in_kernel); the six steps of "NPU Training Operators - GDN",
+ * section "Operator semantics" (chunk-local cumsum of g, beta K K^T with gate
+ * decay, triangular solve, w/u recompute, inter-chunk state propagation,
+ * output).  The result equals the per-token recurrence above up to rounding.
+ *
+ *   q, k          : bf16 [B, T, H, K]
+ *   v             : bf16 [B, T, HV, V]
+ *   g, beta       : fp32 [B, T, HV]  (g = log decay, finite, <= 0 expected)
+ *   scale         : output scale; <= 0 or NaN selects 1/sqrt(K)
+ *   initial_state : fp32 [N, HV, K, V], or NULL for zero states (NULL is a
+ *                   flag: nothing is read)
+ *   cu_seqlens    : NULL for dense input (N must equal B), or int32 [N + 1]
+ *                   device offsets of N packed sequences (B must be 1,
+ *                   cu_seqlens[0] = 0, non-decreasing, cu_seqlens[N] = T).
+ *                   N comes from the host so no device-to-host copy happens.
+ *                   Offsets that break these rules set GDN_DEV_BAD_CU_SEQLENS
+ *                   and the offending sequence is skipped.
+ *   use_qk_l2norm : nonzero to L2-normalise q and k per token
+ *   o             : bf16 [B, T, HV, V] output (every row is written)
+ *   final_state   : fp32 [N, HV, K, V] output, or NULL to skip it
+ *   workspace     : device buffer of gdn_chunk_fwd_workspace_size() bytes
+ *                   (NULL when that size is 0)
+ * Chunks restart at every sequence start; the last chunk of a sequence may be
+ * partial.  A sequence of length 0 writes final_state = initial_state (or 0).
+ */
+int gdn_chunk_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                  const float *g, const float *beta, float scale,
+                  const float *initial_state, const int32_t *cu_seqlens, int N,
+                  int B, int T, int H, int HV, int K, int V, int use_qk_l2norm,
+                  uint16_t *o, float *final_state, void *workspace,
+                  size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/*
+ * gdn_recurrent_decode -- one token per request against a state pool,
+ * updated in place.  FastDeploy PR "support fla triton kernel for qwen3.5",
+ * Usage section 2 ("Decode (fused recurrent, pool-index)") and its file table
+ * entry for fused_recurrent.py (PAD_SLOT_ID = -1 is safe); the LightLLM
+ * "gdn.py" decode path passes A_log, dt_bias and the raw a, b so gating is
+ * fused into the same kernel.
+ *
+ *   q, k        : bf16 [R, 1, H, K]
+ *   v           : bf16 [R, 1, HV, V]
+ *   gates, either (exactly one group non-NULL):
+ *     g, beta   : fp32 [R, HV], or
+ *     A_log, a, b, dt_bias : fp32 [HV], bf16 [R, HV], bf16 [R, HV], fp32 [HV]
+ *                 (g and beta computed in-kernel as in gdn_gating)
+ *   scale, use_qk_l2norm : as in gdn_chunk_fwd
+ *   ssm_pool    : fp32 [P, HV, K, V], read and written in place
+ *   ssm_indices : int32 [R]; -1 (PAD) leaves the pool untouched and writes a
+ *                 zero output row; other values outside [0, P) set
+ *                 GDN_DEV_BAD_SLOT and are treated like PAD.  Two requests
+ *                 naming the same slot is a caller error (undefined result).
+ *   o           : bf16 [R, 1, HV, V] output
+ * R = 0 is a no-op.
+ */
+int gdn_recurrent_decode(const uint16_t *q, const uint16_t *k,
+                         const uint16_t *v, const float *g, const float *beta,
+                         const float *A_log, const uint16_t *a,
+                         const uint16_t *b, const float *dt_bias, float scale,
+                         int use_qk_l2norm, float *ssm_pool, int P,
+                         const int32_t *ssm_indices, int R, int H, int HV,
+                         int K, int V, uint16_t *o, int32_t *dev_status,
+                         void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

@@ -1,0 +1,103 @@
+"""CPU-side checks of the C ABI: the library builds/loads, exports every symbol
+include/gdn.h declares, and rejects bad arguments on the host (these calls
+return before any CUDA work, so they run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gated_deltanet_chunked_chunk_gb300 as gdn
+from gated_deltanet_chunked_chunk_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return gdn.load_library()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_and_binding_agree():
+    assert sorted(gdn.EXPORTED_SYMBOLS) == _declared_functions()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        s = gdn.status_string(code)
+        assert isinstance(s, str) and s
+    assert gdn.status_string(999) == "unknown status"
+    assert lib.gdn_version() >= 100
+
+
+NULL = None
+
+
+def _chunk(lib, **kw):
+    a = dict(q=NULL, k=NULL, v=NULL, g=NULL, beta=NULL, scale=-1.0, h0=NULL, cu=NULL, N=1, B=1, T=8,
+             H=2, HV=4, K=128, V=128, l2=1, o=NULL, ht=NULL, ws=NULL, wsb=0, st=NULL, stream=NULL)
+    a.update(kw)
+    return lib.gdn_chunk_fwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["scale"], a["h0"], a["cu"],
+                             a["N"], a["B"], a["T"], a["H"], a["HV"], a["K"], a["V"], a["l2"], a["o"],
+                             a["ht"], a["ws"], a["wsb"], a["st"], a["stream"])
+
+
+def test_chunk_fwd_host_validation(lib):
+    fake = ctypes.c_void_p(16)  # never dereferenced: every call below fails validation first
+    assert _chunk(lib) == gdn.GDN_EINVAL                      # null tensors
+    assert _chunk(lib, HV=3) == gdn.GDN_EINVAL                # HV % H != 0
+    assert _chunk(lib, K=96, q=fake, k=fake, v=fake, g=fake, beta=fake, o=fake) == gdn.GDN_EUNSUPPORTED
+    assert _chunk(lib, V=32) == gdn.GDN_EUNSUPPORTED
+    assert _chunk(lib, cu=fake, B=2, N=3) == gdn.GDN_EINVAL   # varlen needs B == 1
+    assert _chunk(lib, N=3) == gdn.GDN_EINVAL                 # dense needs N == B
+    assert _chunk(lib, T=-1) == gdn.GDN_EINVAL
+    assert _chunk(lib, N=0, B=0, T=0) == gdn.GDN_OK           # nothing to do, nothing launched
+
+
+def test_decode_host_validation(lib):
+    fake = ctypes.c_void_p(16)
+
+    def call(**kw):
+        a = dict(q=fake, k=fake, v=fake, g=fake, beta=fake, A_log=NULL, a=NULL, b=NULL, dt=NULL,
+                 scale=-1.0, l2=1, pool=fake, P=4, idx=fake, R=2, H=2, HV=4, K=128, V=128, o=fake,
+                 st=NULL, stream=NULL)
+        a.update(kw)
+        return lib.gdn_recurrent_decode(a["q"], a["k"], a["v"], a["g"], a["beta"], a["A_log"], a["a"],
+                                        a["b"], a["dt"], a["scale"], a["l2"], a["pool"], a["P"],
+                                        a["idx"], a["R"], a["H"], a["HV"], a["K"], a["V"], a["o"],
+                                        a["st"], a["stream"])
+    assert call(pool=NULL) == gdn.GDN_EINVAL                  # missing pool: readable error, no crash
+    assert call(idx=NULL) == gdn.GDN_EINVAL                   # missing indices
+    assert call(A_log=fake, a=fake, b=fake, dt=fake) == gdn.GDN_EINVAL  # both gate groups
+    assert call(g=NULL, beta=NULL) == gdn.GDN_EINVAL          # no gate group
+    assert call(beta=NULL) == gdn.GDN_EINVAL                  # half a group
+    assert call(HV=6, H=4) == gdn.GDN_EINVAL
+    assert call(K=32) == gdn.GDN_EUNSUPPORTED
+    assert call(R=0) == gdn.GDN_OK
+
+
+def test_gating_host_validation(lib):
+    assert lib.gdn_gating(NULL, NULL, NULL, NULL, 0, 4, NULL, NULL, NULL) == gdn.GDN_OK
+    assert lib.gdn_gating(NULL, NULL, NULL, NULL, 5, 4, NULL, NULL, NULL) == gdn.GDN_EINVAL
+    assert lib.gdn_gating(NULL, NULL, NULL, NULL, 5, 0, NULL, NULL, NULL) == gdn.GDN_EINVAL
+
+
+def test_python_binding_checks_before_calling():
+    import torch
+    q = torch.zeros(1, 4, 2, 64, dtype=torch.float32)
+    with pytest.raises(TypeError):
+        gdn.gdn_chunk_fwd(q, q, q, q[..., 0], q[..., 0])
+    with pytest.raises(ValueError):
+        gdn.gdn_recurrent_decode(q, q, q, None, None)

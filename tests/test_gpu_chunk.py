@@ -1,0 +1,155 @@
+"""GPU parity of gdn_chunk_fwd against the fp64 oracle (through the C ABI)."""
+import numpy as np
+import pytest
+import torch
+
+from gated_deltanet_chunked_chunk_gb300 import workloads as W
+import parity_util as P
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from gated_deltanet_chunked_chunk_gb300 import build
+    build.build()
+
+
+def _check_case(case, items=None):
+    g, beta = P.oracle_gates(case)
+    o_gpu, ht_gpu = P.run_chunk_gpu(case, g, beta)
+    o_ref, ht_ref = P.run_chunk_oracle(case, g, beta, items=items)
+    if items is None:
+        P.assert_o_close(o_gpu, o_ref)
+        if case.output_final_state:
+            P.assert_state_close(ht_gpu, ht_ref)
+        else:
+            assert ht_gpu is None
+    return o_gpu, ht_gpu, o_ref, ht_ref
+
+
+GRID = []
+for i, (K, V) in enumerate([(64, 64), (128, 128), (64, 128), (128, 64)]):
+    for j, T in enumerate([1, 63, 64, 65, 200]):
+        G = (1, 2, 4)[(i + j) % 3]
+        GRID.append((K, V, T, G, (i + j) % 2 == 0, (i * 5 + j) % 3 != 1))
+
+
+@pytest.mark.parametrize("K,V,T,G,init,final", GRID)
+def test_shape_grid(K, V, T, G, init, final):
+    case = W.prefill_case(f"grid", 100 + K + V + T + G, 2, T, 2, 2 * G, K, V,
+                          init="all" if init else "none", output_final_state=final)
+    _check_case(case)
+
+
+def test_config0_tiny():
+    _check_case(W.config0())
+
+
+def test_config1_dense_gva_with_state():
+    _check_case(W.config1())
+
+
+def test_config2_varlen_packed():
+    _check_case(W.config2())
+
+
+@pytest.mark.slow
+def test_config3_long_context_sampled_heads():
+    """T = 65536 (1024 serial chunks): full oracle on sampled value heads that
+    cover different key heads; every output checked finite."""
+    case = W.config3()
+    g, beta = P.oracle_gates(case)
+    o_gpu, ht_gpu = P.run_chunk_gpu(case, g, beta)
+    assert np.isfinite(o_gpu).all() and np.isfinite(ht_gpu).all()
+    for hv in (0, 17, 31):
+        o_ref, ht_ref, (b0, sl) = P.oracle_single_head(case, g, beta, 0, hv)
+        P.assert_o_close(o_gpu[b0, sl, hv], o_ref, what=f"o[hv={hv}]")
+        P.assert_state_close(ht_gpu[0, hv], ht_ref, what=f"final_state[hv={hv}]")
+        # the late part of the sequence on its own (errors must not grow along T)
+        P.assert_o_close(o_gpu[b0, sl, hv][-4096:], o_ref[-4096:], what=f"o tail[hv={hv}]")
+
+
+def test_no_l2norm_and_explicit_scale():
+    case = W.prefill_case("nol2", 7, 1, 130, 2, 4, 64, 64, init="all", scale=0.05,
+                          use_qk_l2norm=False)
+    case.q = (case.q.float() / 8).to(torch.bfloat16)
+    case.k = (case.k.float() / 8).to(torch.bfloat16)
+    _check_case(case)
+
+
+def test_varlen_with_empty_and_short_sequences():
+    lens = [0, 1, 64, 0, 65, 130, 7]
+    cu = W.cu_from_lengths(lens)
+    case = W.prefill_case("varlen_edge", 8, 1, cu[-1], 2, 4, 128, 128, cu_seqlens=cu, init="all")
+    o_gpu, ht_gpu, o_ref, ht_ref = _check_case(case)
+    h0 = case.initial_state.numpy()
+    for n, L in enumerate(lens):
+        if L == 0:
+            np.testing.assert_array_equal(ht_gpu[n], h0[n])
+
+
+def test_varlen_equals_separate_dense_calls_bitwise():
+    lens = [70, 1, 129, 64]
+    cu = W.cu_from_lengths(lens)
+    case = W.prefill_case("packed", 9, 1, cu[-1], 2, 4, 128, 128, cu_seqlens=cu, init="all")
+    g, beta = P.oracle_gates(case)
+    o_p, ht_p = P.run_chunk_gpu(case, g, beta)
+    import gated_deltanet_chunked_chunk_gb300 as gdn
+    for n in range(len(lens)):
+        sl = slice(cu[n], cu[n + 1])
+        o1, h1 = gdn.gdn_chunk_fwd(case.q[:, sl].cuda(), case.k[:, sl].cuda(), case.v[:, sl].cuda(),
+                                   g[:, sl].contiguous().cuda(), beta[:, sl].contiguous().cuda(),
+                                   initial_state=case.initial_state[n:n + 1].cuda())
+        np.testing.assert_array_equal(o1.float().cpu().numpy()[0], o_p[0, sl])
+        np.testing.assert_array_equal(h1.cpu().numpy()[0], ht_p[n])
+
+
+def test_split_at_chunk_boundary_with_state_carry_is_bitwise():
+    case = W.prefill_case("split", 10, 1, 320, 2, 4, 128, 128, init="all")
+    g, beta = P.oracle_gates(case)
+    import gated_deltanet_chunked_chunk_gb300 as gdn
+    d = lambda t: t.cuda().contiguous()
+    o_full, h_full = gdn.gdn_chunk_fwd(d(case.q), d(case.k), d(case.v), d(g), d(beta),
+                                       initial_state=d(case.initial_state))
+    cut = 192
+    oa, ha = gdn.gdn_chunk_fwd(d(case.q[:, :cut]), d(case.k[:, :cut]), d(case.v[:, :cut]),
+                               d(g[:, :cut]), d(beta[:, :cut]), initial_state=d(case.initial_state))
+    ob, hb = gdn.gdn_chunk_fwd(d(case.q[:, cut:]), d(case.k[:, cut:]), d(case.v[:, cut:]),
+                               d(g[:, cut:]), d(beta[:, cut:]), initial_state=ha)
+    assert torch.equal(torch.cat([oa, ob], 1), o_full)
+    assert torch.equal(hb, h_full)
+
+
+def test_deterministic_and_guard_bands():
+    case = W.config1()
+    g, beta = P.oracle_gates(case)
+    import gated_deltanet_chunked_chunk_gb300 as gdn
+    d = lambda t: t.cuda().contiguous()
+    q, k, v, gg, bb, h0 = map(d, (case.q, case.k, case.v, g, beta, case.initial_state))
+    pad = 4096
+    o_buf = torch.full((case.B * case.T * case.HV * case.V + 2 * pad,), 0x7FBF, dtype=torch.int16,
+                       device="cuda").view(torch.bfloat16)
+    s_buf = torch.full((h0.numel() + 2 * pad,), 12345.0, device="cuda")
+    o = o_buf[pad:-pad].view(case.B, case.T, case.HV, case.V)
+    ht = s_buf[pad:-pad].view_as(h0)
+    gdn.gdn_chunk_fwd(q, k, v, gg, bb, initial_state=h0, o=o, final_state=ht)
+    o2, h2 = gdn.gdn_chunk_fwd(q, k, v, gg, bb, initial_state=h0)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(ht, h2)
+    canary = o_buf.view(torch.int16)
+    assert bool((canary[:pad] == 0x7FBF).all()) and bool((canary[-pad:] == 0x7FBF).all())
+    assert bool((s_buf[:pad] == 12345.0).all()) and bool((s_buf[-pad:] == 12345.0).all())
+
+
+def test_bad_cu_seqlens_sets_device_status():
+    import gated_deltanet_chunked_chunk_gb300 as gdn
+    T, H, HV, K = 100, 2, 2, 64
+    x = torch.zeros(1, T, H, K, dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros(1, T, HV, K, dtype=torch.bfloat16, device="cuda")
+    gz = torch.zeros(1, T, HV, device="cuda")
+    cu = torch.tensor([0, 60, 40, 100], dtype=torch.int32, device="cuda")  # decreasing
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gdn.gdn_chunk_fwd(x, x, v, gz, gz, cu_seqlens=cu, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & gdn.DEV_BAD_CU_SEQLENS
