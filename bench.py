@@ -41,7 +41,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--e2e-steps", type=int, default=3)
-    p.add_argument("--cpu-tokens", type=int, default=16384,
+    p.add_argument("--cpu-tokens", type=int, default=65536,
                    help="tokens of the workload (all heads) in the CPU oracle sample")
     p.add_argument("--no-extras", action="store_true", help="skip e2e, CPU baseline, decode, gating")
     return p.parse_args()
