@@ -22,6 +22,7 @@ from typing import Optional, Tuple
 import torch
 
 __all__ = ["gdn_gating", "gdn_chunk_fwd", "gdn_recurrent_decode", "chunk_fwd_workspace_size",
+           "gdn_chunk_fwd_noalloc", "NOALLOC_SCRATCH_BYTES",
            "GDNError", "lib_path", "load_library", "status_string", "DEV_BAD_CU_SEQLENS",
            "DEV_BAD_SLOT", "DEV_WAIT_TIMEOUT", "EXPORTED_SYMBOLS"]
 
@@ -30,12 +31,15 @@ _LIB_PATH = os.path.join(_PKG, "_build", "libgdn.so")
 _lib = None
 _lock = threading.Lock()
 
-GDN_OK, GDN_EINVAL, GDN_EUNSUPPORTED, GDN_ECUDA, GDN_EWORKSPACE = 0, 1, 2, 3, 4
+GDN_OK, GDN_EINVAL, GDN_EUNSUPPORTED, GDN_ECUDA, GDN_EWORKSPACE, GDN_ESCRATCH_LIMIT = 0, 1, 2, 3, 4, 5
 DEV_BAD_CU_SEQLENS, DEV_BAD_SLOT, DEV_WAIT_TIMEOUT = 1, 2, 4
 
 #: Every symbol include/gdn.h declares (checked by the tests).
 EXPORTED_SYMBOLS = ("gdn_status_string", "gdn_version", "gdn_gating", "gdn_chunk_fwd_workspace_size",
-                    "gdn_chunk_fwd", "gdn_recurrent_decode")
+                    "gdn_chunk_fwd", "gdn_recurrent_decode", "gdn_chunk_fwd_noalloc")
+
+#: Size of the fixed scratch buffer behind gdn_chunk_fwd_noalloc (bytes).
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class GDNError(RuntimeError):
@@ -72,6 +76,8 @@ def load_library():
         lib.gdn_recurrent_decode.argtypes = [P, P, P, P, P, P, P, P, P, F, I, P, I, P, I, I, I, I, I,
                                              P, P, P]
         lib.gdn_recurrent_decode.restype = I
+        lib.gdn_chunk_fwd_noalloc.argtypes = [P, P, P, P, P, F, P, P, I, I, I, I, I, I, I, I, P, P, P, P]
+        lib.gdn_chunk_fwd_noalloc.restype = I
         _lib = lib
         return lib
 
@@ -193,6 +199,57 @@ def gdn_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
         _ptr(dev_status), _stream(dev))
     if rc != GDN_OK:
         raise GDNError("gdn_chunk_fwd", rc)
+    return o, final_state
+
+
+def gdn_chunk_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                          beta: torch.Tensor, scale: Optional[float] = None,
+                          initial_state: Optional[torch.Tensor] = None, output_final_state: bool = True,
+                          cu_seqlens: Optional[torch.Tensor] = None, use_qk_l2norm: bool = True,
+                          num_seqs: Optional[int] = None, dev_status: Optional[torch.Tensor] = None,
+                          o: Optional[torch.Tensor] = None, final_state: Optional[torch.Tensor] = None
+                          ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """gdn_chunk_fwd for callers that cannot allocate device memory at call time
+    (for example a serving runtime whose device memory is all reserved by its own
+    pool).  The library keeps the workspace in a fixed buffer of
+    NOALLOC_SCRATCH_BYTES per GPU; larger inputs raise GDNError with
+    GDN_ESCRATCH_LIMIT.  The C call allocates nothing; pass ``o`` and
+    ``final_state`` to keep this wrapper from allocating its outputs either.
+    Calls sharing a device must not overlap on the GPU."""
+    dev = q.device
+    for t, n_, dt in ((q, "q", torch.bfloat16), (k, "k", torch.bfloat16), (v, "v", torch.bfloat16),
+                      (g, "g", torch.float32), (beta, "beta", torch.float32)):
+        _check(t, n_, dt, dev)
+    if q.dim() != 4 or k.shape != q.shape or v.dim() != 4 or v.shape[:2] != q.shape[:2]:
+        raise ValueError("gdn_chunk_fwd_noalloc: q, k must be [B,T,H,K] and v [B,T,HV,V]")
+    B, T, H, K = q.shape
+    HV, V = v.shape[2], v.shape[3]
+    if tuple(g.shape) != (B, T, HV) or tuple(beta.shape) != (B, T, HV):
+        raise ValueError(f"gdn_chunk_fwd_noalloc: g and beta must be [B,T,HV] = {(B, T, HV)}")
+    if cu_seqlens is not None:
+        _check(cu_seqlens, "cu_seqlens", torch.int32, dev, ndim=1)
+        N = int(num_seqs) if num_seqs is not None else cu_seqlens.numel() - 1
+    else:
+        N = B
+    if initial_state is not None:
+        _check(initial_state, "initial_state", torch.float32, dev)
+        if tuple(initial_state.shape) != (N, HV, K, V):
+            raise ValueError(f"initial_state must be [N,HV,K,V] = {(N, HV, K, V)}")
+    if o is None:
+        o = torch.empty((B, T, HV, V), dtype=torch.bfloat16, device=dev)
+    _check(o, "o", torch.bfloat16, dev)
+    if output_final_state and final_state is None:
+        final_state = torch.empty((N, HV, K, V), dtype=torch.float32, device=dev)
+    if final_state is not None:
+        _check(final_state, "final_state", torch.float32, dev)
+    if dev_status is not None:
+        _check(dev_status, "dev_status", torch.int32, dev)
+    rc = load_library().gdn_chunk_fwd_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _scale_arg(scale), _ptr(initial_state),
+        _ptr(cu_seqlens), N, B, T, H, HV, K, V, int(bool(use_qk_l2norm)), _ptr(o), _ptr(final_state),
+        _ptr(dev_status), _stream(dev))
+    if rc != GDN_OK:
+        raise GDNError("gdn_chunk_fwd_noalloc", rc)
     return o, final_state
 
 

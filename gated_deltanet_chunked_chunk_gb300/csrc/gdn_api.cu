@@ -21,6 +21,7 @@ const char *gdn_status_string(int status) {
     case GDN_EUNSUPPORTED: return "unsupported configuration (head dims K and V must be 64 or 128)";
     case GDN_ECUDA: return "CUDA error while launching";
     case GDN_EWORKSPACE: return "workspace missing or too small";
+    case GDN_ESCRATCH_LIMIT: return "input needs more workspace than the fixed no-allocation scratch holds; call gdn_chunk_fwd with a workspace";
     default: return "unknown status";
   }
 }

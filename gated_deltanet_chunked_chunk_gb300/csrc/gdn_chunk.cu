@@ -44,6 +44,8 @@
 #include <cuda.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "gdn_common.cuh"
 #include "gdn_sm103.cuh"
 
@@ -908,3 +910,60 @@ cudaError_t launch_chunk(const ChunkArgs &a, cudaStream_t s) {
 }
 
 }  // namespace gdn_host
+
+// ------------------------------------------------ no-allocation entry point
+//
+// Some callers cannot allocate device memory at call time: serving runtimes
+// that hand all device memory to their own pool at start-up and forbid any
+// later cudaMalloc, and hot loops that must not take the driver's allocation
+// path.  For them gdn_chunk_fwd_noalloc runs the same two kernels with the
+// workspace in a fixed buffer compiled into this library instead of a
+// caller-provided one.
+//
+// The buffer is a file-scope __device__ array: every GPU that loads the
+// library holds GDN_NOALLOC_SCRATCH_BYTES of it until the process exits.  In
+// host code the array's name is only a host-side stand-in, so its device
+// address is looked up once per device (with that device current) through
+// cudaGetSymbolAddress and cached.  Every call on a device shares the buffer
+// and leaves the last call's contents in it; nothing in it must start at zero
+// (each record the walk kernel reads is written by the prep kernel of the same
+// call), but two calls that overlap on the GPU race on it.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[GDN_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices] = {nullptr};
+
+// Device address of the scratch buffer on the current device (set-up on the
+// first call per device).
+int noalloc_scratch(void **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDN_ECUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return GDN_ECUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return GDN_OK;
+}
+}  // namespace
+
+extern "C" int gdn_chunk_fwd_noalloc(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *g,
+                                     const float *beta, float scale, const float *initial_state,
+                                     const int32_t *cu_seqlens, int N, int B, int T, int H, int HV, int K, int V,
+                                     int use_qk_l2norm, uint16_t *o, float *final_state, int32_t *dev_status,
+                                     void *stream) {
+  if (B < 0 || T < 0 || N < 0 || HV <= 0 || K <= 0) return GDN_EINVAL;
+  const size_t need = gdn_chunk_fwd_workspace_size(B, T, H, HV, K, V, N, cu_seqlens != nullptr);
+  if (need > GDN_NOALLOC_SCRATCH_BYTES) return GDN_ESCRATCH_LIMIT;
+  void *ws = nullptr;
+  if (need > 0) {
+    const int rc = noalloc_scratch(&ws);
+    if (rc != GDN_OK) return rc;
+  }
+  return gdn_chunk_fwd(q, k, v, g, beta, scale, initial_state, cu_seqlens, N, B, T, H, HV, K, V, use_qk_l2norm, o,
+                       final_state, ws, need > 0 ? GDN_NOALLOC_SCRATCH_BYTES : 0, dev_status, stream);
+}

@@ -48,7 +48,8 @@ enum gdn_status_code {
   GDN_EINVAL = 1,        /* null required pointer, bad shape, HV % H != 0, ... */
   GDN_EUNSUPPORTED = 2,  /* K or V outside {64, 128}, no sm_103a device, ... */
   GDN_ECUDA = 3,         /* a CUDA call or kernel launch failed */
-  GDN_EWORKSPACE = 4     /* workspace missing or smaller than required */
+  GDN_EWORKSPACE = 4,    /* workspace missing or smaller than required */
+  GDN_ESCRATCH_LIMIT = 5 /* gdn_chunk_fwd_noalloc: input needs more than its fixed scratch */
 };
 
 /* Bits OR-ed into *dev_status by kernels. */
@@ -155,6 +156,36 @@ int gdn_recurrent_decode(const uint16_t *q, const uint16_t *k,
                          const int32_t *ssm_indices, int R, int H, int HV,
                          int K, int V, uint16_t *o, int32_t *dev_status,
                          void *stream);
+
+/*
+ * gdn_chunk_fwd_noalloc -- gdn_chunk_fwd for callers that cannot allocate
+ * device memory at call time (a serving runtime that reserves all device
+ * memory for its own pool at start-up and forbids later cudaMalloc, or a hot
+ * loop that must stay off the driver's allocation path).  The pages describe
+ * nothing of the kind: this entry point only changes where the workspace lives.
+ *
+ * Same arguments and results as gdn_chunk_fwd, without workspace arguments:
+ * the workspace is a fixed GDN_NOALLOC_SCRATCH_BYTES buffer compiled into the
+ * library (a __device__ array that every GPU loading the library holds until
+ * the process exits).  Inputs whose gdn_chunk_fwd_workspace_size() exceeds it
+ * return GDN_ESCRATCH_LIMIT before anything is launched; use gdn_chunk_fwd
+ * with a workspace for those (about 1.3 MB per 64 tokens at HV = 32, K = 128,
+ * so up to 24 chunks of 64 tokens per call at that size).
+ *
+ * The first call on a device looks up the buffer's device address (with that
+ * device current) and caches it; make that first call before any stream
+ * capture.  The call allocates nothing and calls no allocating library
+ * routine.  All calls on a device share the buffer: calls that overlap on the
+ * GPU (different streams without ordering) race on it.  Nothing in the buffer
+ * needs to start at zero.
+ */
+#define GDN_NOALLOC_SCRATCH_BYTES (32u << 20)
+int gdn_chunk_fwd_noalloc(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                          const float *g, const float *beta, float scale,
+                          const float *initial_state, const int32_t *cu_seqlens,
+                          int N, int B, int T, int H, int HV, int K, int V,
+                          int use_qk_l2norm, uint16_t *o, float *final_state,
+                          int32_t *dev_status, void *stream);
 
 #ifdef __cplusplus
 }
