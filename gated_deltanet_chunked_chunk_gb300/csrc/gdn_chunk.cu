@@ -527,6 +527,12 @@ __global__ void __launch_bounds__(NTH, 2) chunk_prep_kernel(
 }
 
 // ============================================================== walk kernel
+// Sixteen warps in two groups that hand data to each other through mbarriers:
+//   chain (warps 0-7): u = beta v + Ts V, W h, v_new = u - W h, the state update
+//     h <- e^{gamma_L} h + K^T (s v_new) and the bf16 copy of h;
+//   side (warps 8-15): Q h (hi + lo) while the chain works, o = scale (e^gamma rq
+//     Q h + P v_new) once v_new is out, and (thread 256) the TMA / bulk loads of
+//     chunk c+2 once both groups are done with chunk c.
 template <int K>
 struct WalkLay {
   static constexpr int KQB = KQ<K>::BYTES;
@@ -534,17 +540,20 @@ struct WalkLay {
   static constexpr int STAGE = KQB + V_BYTES + Rec<K>::BYTES;  // [K;Q] | V slice | record
   static constexpr int NS = 2;
   static constexpr int OFF_H = NS * STAGE;                     // h bf16 hi [K][HROW] then lo
-  static constexpr int OFF_VS = OFF_H + 2 * K * HROW;          // s v_new hi, lo; v_new hi, lo: [64][HROW] each
-  static constexpr int OFF_BAR = OFF_VS + 4 * 64 * HROW;
-  static constexpr int OFF_MISC = OFF_BAR + 8 * NS;
+  static constexpr int OFF_VS = OFF_H + 2 * K * HROW;          // s v_new hi, lo (chain only)
+  static constexpr int OFF_VH = OFF_VS + 2 * 64 * HROW;        // v_new hi, lo (chain -> side)
+  static constexpr int OFF_BAR = OFF_VH + 2 * 64 * HROW;
+  static constexpr int NBAR = 2 * 7;
+  static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr uint32_t TX = KQB + V_BYTES + Rec<K>::BYTES;
   static_assert(STAGE % 1024 == 0, "stage alignment");
   static_assert(BYTES + 1024 <= 232448, "shared memory budget (227 KB per CTA)");
 };
+constexpr int WNTH = 2 * NTH;  // 512 threads
 
 template <int K>
-__global__ void __launch_bounds__(NTH, 1) chunk_walk_kernel(
+__global__ void __launch_bounds__(WNTH, 1) chunk_walk_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, float scale, const float *__restrict__ h0,
     const int32_t *__restrict__ cu, int T, int H, int HV, int V, const unsigned char *__restrict__ ws,
@@ -560,6 +569,9 @@ __global__ void __launch_bounds__(NTH, 1) chunk_walk_kernel(
   const int h = hv / (HV / H);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g4 = lane >> 2, t4 = lane & 3;
+  const bool chain = warp < 8;
+  const int gw = warp & 7;                  // warp index within its group
+  const int mi = gw & 3, nh = gw >> 2;      // 16-row tile, 16-column half (64-row products)
 
   int64_t tok0, len;
   if (!seq_bounds(cu, n, T, tok0, len)) {
@@ -570,137 +582,134 @@ __global__ void __launch_bounds__(NTH, 1) chunk_walk_kernel(
   const int64_t cb = chunk_base(cu, n, T);
   uint32_t *misc = reinterpret_cast<uint32_t *>(sm + Ly::OFF_MISC);
   volatile uint32_t *abort_flag = misc + 1;
-  auto b_full = [&](int s) { return sb + Ly::OFF_BAR + 8 * s; };
+  // Barriers, two of each (indexed by chunk parity): TMA full; (unused); h ready;
+  // v_new ready; chain done with the stage; side done with h; side done with v_new.
+  auto bar = [&](int kind, int b) { return sb + Ly::OFF_BAR + 8 * (2 * kind + b); };
+  enum { FULL = 0, HREADY = 2, VREADY = 3, CDONE = 4, SHDONE = 5, SVDONE = 6 };
   if (tid == 0) {
-    for (int s = 0; s < NS; ++s) mbar_init(b_full(s), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(FULL, b), 1);
+      for (int kd = 1; kd < 7; ++kd) mbar_init(bar(kd, b), 8);
+    }
     misc[1] = 0;
-    misc[2] = 0;
     mbar_fence_init();
   }
   __syncthreads();
-
-  int tma_hi = 0;  // chunks whose loads have been issued (thread 0)
-  auto issue = [&](int c) {
-    const int s = c % NS;
-    const uint32_t st = sb + s * Ly::STAGE;
-    const int trow = static_cast<int>(tok0) + c * C;
-    mbar_arrive_expect_tx(b_full(s), Ly::TX);
-#pragma unroll
-    for (int a = 0; a < KA; ++a) {
-      tma_load_3d(st + a * 16384, &tm_k, b_full(s), 64 * a, h, trow);
-      tma_load_3d(st + a * 16384 + 8192, &tm_q, b_full(s), 64 * a, h, trow);
+  // Waits on chunk c's use of a barrier (each barrier serves every other chunk).
+  // Lane 0 polls; __syncwarp orders the other lanes' later reads after its
+  // acquire, and the result is warp-uniform.  After any expired wait every
+  // later wait returns false at once: the loops then run to their end without
+  // work but still pass every named barrier, so no warp is left waiting.
+  auto waitc = [&](int kind, int c) -> bool {
+    uint32_t ok = 0;
+    if (lane == 0) {
+      ok = !*abort_flag;
+      if (ok && !mbar_wait_bounded(bar(kind, c & 1), (c >> 1) & 1, kWaitLimit)) {
+        *abort_flag = 1;
+        ok = 0;
+      }
     }
-    tma_load_3d(st + Ly::KQB, &tm_v, b_full(s), vt0, hv, trow);
-    bulk_load(st + Ly::KQB + Ly::V_BYTES, ws + (static_cast<size_t>(cb + c) * HV + hv) * R::BYTES, R::BYTES,
-              b_full(s));
-    tma_hi = c + 1;
+    __syncwarp();
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
   };
-  if (tid == 0)
-    for (int c = 0; c < NS && c < NC; ++c) issue(c);
+  auto arrive = [&](int kind, int c) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(kind, c & 1));
+  };
 
-  // State slice: warp -> 16 keys (hm) x NT8 n-tiles of 8 columns from hn0.
-  constexpr int MTH = K / 16;
-  constexpr int NT8 = (K / 16) * 4 / NW;
-  const int hm = warp % MTH;
-  const int hn0 = (warp / MTH) * NT8;
-  const int mi = warp & 3, nh = warp >> 2;  // 16-row tile, 16-column half for the 64-row products
-  float hf[NT8][4];
+  const uint32_t aH = sb + Ly::OFF_H, aHL = aH + K * HROW;
+  const uint32_t aVS = sb + Ly::OFF_VS, aVSL = aVS + 64 * HROW;
+  const uint32_t aVH = sb + Ly::OFF_VH, aVL = aVH + 64 * HROW;
   const int64_t sbase = (static_cast<int64_t>(n) * HV + hv) * K;
-#pragma unroll
-  for (int j = 0; j < NT8; ++j)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int key = 16 * hm + g4 + 8 * (e >> 1);
-      const int col = 8 * (hn0 + j) + 2 * t4 + (e & 1);
-      hf[j][e] = h0 ? h0[(sbase + key) * V + vt0 + col] : 0.f;
-    }
-  unsigned char *Hb = sm + Ly::OFF_H;
-  // h as bf16 hi + lo planes, [key][HROW], the B operand of [Q; W] h.
-  auto write_h = [&]() {
+
+  if (chain) {
+    // ---------------------------------------------------------------- chain
+    constexpr int NT8 = (K / 16) * 4 / 8;  // state n-tiles per warp
+    const int hm = gw % (K / 16);
+    const int hn0 = (gw / (K / 16)) * NT8;
+    float hf[NT8][4];
 #pragma unroll
     for (int j = 0; j < NT8; ++j)
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int key = 16 * hm + g4 + 8 * hh;
-        const int col = 8 * (hn0 + j) + 2 * t4;
-        const float x0 = hf[j][2 * hh], x1 = hf[j][2 * hh + 1];
-        const uint32_t hi = pack_bf16(x0, x1);
-        *reinterpret_cast<uint32_t *>(Hb + key * HROW + col * 2) = hi;
-        *reinterpret_cast<uint32_t *>(Hb + (K + key) * HROW + col * 2) = pack_bf16(x0 - bf16lo_f(hi), x1 - bf16hi_f(hi));
+      for (int e = 0; e < 4; ++e) {
+        const int key = 16 * hm + g4 + 8 * (e >> 1);
+        const int col = 8 * (hn0 + j) + 2 * t4 + (e & 1);
+        hf[j][e] = h0 ? h0[(sbase + key) * V + vt0 + col] : 0.f;
       }
-  };
-  write_h();
-  __syncthreads();
-
-  const uint32_t aH = sb + Ly::OFF_H, aHL = aH + K * HROW;
-  const uint32_t aVS = sb + Ly::OFF_VS, aVSL = aVS + 64 * HROW, aVH = aVSL + 64 * HROW, aVL = aVH + 64 * HROW;
-  const float dscale = scale;
-
-  for (int c = 0; c < NC; ++c) {
-    const int s = c % NS;
-    const uint32_t st = sb + s * Ly::STAGE;
-    const uint32_t stV = st + Ly::KQB;
-    const uint32_t rc = stV + Ly::V_BYTES;  // record image
-    const unsigned char *stp = sm + s * Ly::STAGE;
-    const float *rsc = reinterpret_cast<const float *>(stp + Ly::KQB + Ly::V_BYTES + R::SC);
-    const int64_t remc = len - static_cast<int64_t>(c) * C;
-    const int L = static_cast<int>(remc < C ? remc : C);
-    const int64_t trow0 = tok0 + static_cast<int64_t>(c) * C;
-
-    if (!mbar_wait_bounded(b_full(s), (c / NS) & 1, kWaitLimit)) *abort_flag = 1;
-    if (tid == 0) misc[2] = *abort_flag;
-    __syncthreads();
-    if (misc[2]) break;
-
-    // u = beta v + Ts V for rows 16 mi.., columns 16 nh..: kept in registers.
-    // Rows >= L of the V slice may hold the next sequence's values; beta and
-    // the Ts columns are zero there, so they do not contribute.
-    float u[2][4];
-    {
-      float au[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    unsigned char *Hb = sm + Ly::OFF_H;
+    auto write_h = [&]() {
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        uint32_t as[4], bv[4];
-        ldsm_x4(rc + R::TS + sw128(16 * mi + (lane & 15), 2 * kk + (lane >> 4)), as);
-        const int mq = lane >> 3;
-        ldsm_x4_t(stV + (16 * kk + (lane & 7) + 8 * (mq & 1)) * 64 + (2 * nh + (mq >> 1)) * 16, bv);
-        mma_bf16(au[0], as, bv[0], bv[1]);
-        mma_bf16(au[1], as, bv[2], bv[3]);
-      }
+      for (int j = 0; j < NT8; ++j)
 #pragma unroll
-      for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int r = 16 * mi + g4 + 8 * (e >> 1);
-          const int col = 16 * nh + 8 * j + 2 * t4 + (e & 1);
-          const float bt = rsc[RS_BET + r];
-          const float vv = bt != 0.f ? bf2f(*reinterpret_cast<const uint16_t *>(stp + Ly::KQB + r * 64 + col * 2)) : 0.f;
-          u[j][e] = fmaf(bt, vv, au[j][e]);
+        for (int hh = 0; hh < 2; ++hh) {
+          const int key = 16 * hm + g4 + 8 * hh;
+          const int col = 8 * (hn0 + j) + 2 * t4;
+          const float x0 = hf[j][2 * hh], x1 = hf[j][2 * hh + 1];
+          const uint32_t hi = pack_bf16(x0, x1);
+          *reinterpret_cast<uint32_t *>(Hb + key * HROW + col * 2) = hi;
+          *reinterpret_cast<uint32_t *>(Hb + (K + key) * HROW + col * 2) = pack_bf16(x0 - bf16lo_f(hi), x1 - bf16hi_f(hi));
         }
-    }
+    };
+    write_h();
+    named_bar_sync(1, NTH);
+    arrive(HREADY, 0);
 
-    // [Q; W] h: W h with the bf16 hi part of h (it only corrects u), Q h with hi + lo.
-    float aq[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    float aql[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    {
+    for (int c = 0; c < NC; ++c) {
+      const int s = c % NS;
+      const uint32_t st = sb + s * Ly::STAGE;
+      const uint32_t rc = st + Ly::KQB + Ly::V_BYTES;
+      const float *rsc = reinterpret_cast<const float *>(sm + s * Ly::STAGE + Ly::KQB + Ly::V_BYTES + R::SC);
+      bool go = waitc(FULL, c);
+      if (go) {
+      // u = beta v + Ts V for rows 16 mi.., columns 16 nh.. (registers).  Rows >= L
+      // of the V slice may hold the next sequence's values; beta and the Ts
+      // columns are zero there, so they do not contribute.
+      float u[2][4];
+      {
+        const uint32_t stV = st + Ly::KQB;
+        const unsigned char *stp = sm + s * Ly::STAGE;
+        float au[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          uint32_t as[4], bv[4];
+          ldsm_x4(rc + R::TS + sw128(16 * mi + (lane & 15), 2 * kk + (lane >> 4)), as);
+          const int mq = lane >> 3;
+          ldsm_x4_t(stV + (16 * kk + (lane & 7) + 8 * (mq & 1)) * 64 + (2 * nh + (mq >> 1)) * 16, bv);
+          mma_bf16(au[0], as, bv[0], bv[1]);
+          mma_bf16(au[1], as, bv[2], bv[3]);
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int r = 16 * mi + g4 + 8 * hh;
+            const int col = 16 * nh + 8 * j + 2 * t4;
+            const float bt = rsc[RS_BET + r];
+            float v0 = 0.f, v1 = 0.f;
+            if (bt != 0.f) {
+              const uint32_t vv = *reinterpret_cast<const uint32_t *>(stp + Ly::KQB + r * 64 + col * 2);
+              v0 = bf16lo_f(vv);
+              v1 = bf16hi_f(vv);
+            }
+            u[j][2 * hh] = fmaf(bt, v0, au[j][2 * hh]);
+            u[j][2 * hh + 1] = fmaf(bt, v1, au[j][2 * hh + 1]);
+          }
+      }
+
+      // W h (hi part of h): rows 16 mi.., columns 16 nh..
       float aw[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
       for (int kk = 0; kk < K / 16; ++kk) {
-        uint32_t fq[4], fw[4], b[4], bl[4];
-        const int kc = 2 * kk + (lane >> 4);
-        ldsm_x4(tile_addr(rc + R::W, 64, 16 * mi + (lane & 15), kc), fw);
-        ldsm_x4(tile_addr(st, 128, 64 + 16 * mi + (lane & 15), kc), fq);
+        uint32_t fw[4], b[4];
+        ldsm_x4(tile_addr(rc + R::W, 64, 16 * mi + (lane & 15), 2 * kk + (lane >> 4)), fw);
         const int mq = lane >> 3;
-        const uint32_t ho = (16 * kk + (lane & 7) + 8 * (mq & 1)) * HROW + (2 * nh + (mq >> 1)) * 16;
-        ldsm_x4_t(aH + ho, b);
-        ldsm_x4_t(aHL + ho, bl);
+        ldsm_x4_t(aH + (16 * kk + (lane & 7) + 8 * (mq & 1)) * HROW + (2 * nh + (mq >> 1)) * 16, b);
         mma_bf16(aw[0], fw, b[0], b[1]);
         mma_bf16(aw[1], fw, b[2], b[3]);
-        mma_bf16(aq[0], fq, b[0], b[1]);
-        mma_bf16(aq[1], fq, b[2], b[3]);
-        mma_bf16(aql[0], fq, bl[0], bl[1]);
-        mma_bf16(aql[1], fq, bl[2], bl[3]);
       }
+      // v_new = u - W h; s v_new (hi, lo) for the state update, v_new (hi, lo) for o.
+      if (c >= 1) go = waitc(SVDONE, c - 1) && go;
+      if (go) {
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const int col = 16 * nh + 8 * j + 2 * t4;
@@ -714,55 +723,124 @@ __global__ void __launch_bounds__(NTH, 1) chunk_walk_kernel(
           const float y0 = sr * x0, y1 = sr * x1;
           const uint32_t yh = pack_bf16(y0, y1);
           const uint32_t yl = pack_bf16(y0 - bf16lo_f(yh), y1 - bf16hi_f(yh));
-          unsigned char *vb = sm + Ly::OFF_VS + r * HROW + col * 2;
-          *reinterpret_cast<uint32_t *>(vb) = yh;
-          *reinterpret_cast<uint32_t *>(vb + 64 * HROW) = yl;
-          *reinterpret_cast<uint32_t *>(vb + 2 * 64 * HROW) = hi;
-          *reinterpret_cast<uint32_t *>(vb + 3 * 64 * HROW) = lo;
+          unsigned char *vs = sm + Ly::OFF_VS + r * HROW + col * 2;
+          *reinterpret_cast<uint32_t *>(vs) = yh;
+          *reinterpret_cast<uint32_t *>(vs + 64 * HROW) = yl;
+          unsigned char *vh = sm + Ly::OFF_VH + r * HROW + col * 2;
+          *reinterpret_cast<uint32_t *>(vh) = hi;
+          *reinterpret_cast<uint32_t *>(vh + 64 * HROW) = lo;
         }
       }
-    }
-    __syncthreads();
+      }
+      }
+      named_bar_sync(1, NTH);
+      if (go) arrive(VREADY, c);
 
-    // h = e^{gamma_L} h + K^T (s v_new) (hi + lo), then the bf16 copy for the next chunk.
-    {
-      const float dL = rsc[RS_DL];
-      float hl[NT8][4];
+      // h = e^{gamma_L} h + K^T (s v_new), hi and lo parts.
+      if (go) {
+        const float dL = rsc[RS_DL];
+        float hl[NT8][4];
+#pragma unroll
+        for (int j = 0; j < NT8; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            hf[j][e] *= dL;
+            hl[j][e] = 0.f;
+          }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const int mq = lane >> 3;
+          uint32_t a[4];
+          ldsm_x4_t(tile_addr(st, 128, 16 * kk + (lane & 7) + 8 * (mq >> 1), 2 * hm + (mq & 1)), a);
+#pragma unroll
+          for (int j = 0; j < NT8; j += 2) {
+            uint32_t b[4], bl[4];
+            const uint32_t ro = (16 * kk + (lane & 7) + 8 * (mq & 1)) * HROW + (hn0 + j + (mq >> 1)) * 16;
+            ldsm_x4_t(aVS + ro, b);
+            ldsm_x4_t(aVSL + ro, bl);
+            mma_bf16(hf[j], a, b[0], b[1]);
+            mma_bf16(hf[j + 1], a, b[2], b[3]);
+            mma_bf16(hl[j], a, bl[0], bl[1]);
+            mma_bf16(hl[j + 1], a, bl[2], bl[3]);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < NT8; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) hf[j][e] += hl[j][e];
+      }
+      if (go) arrive(CDONE, c);  // this chunk's stage is no longer read by the chain
+      go = waitc(SHDONE, c) && go;  // the side group has read h_c
+      if (go) write_h();
+      named_bar_sync(1, NTH);
+      if (go) arrive(HREADY, c + 1);
+    }
+    if (ht && !*abort_flag) {
 #pragma unroll
       for (int j = 0; j < NT8; ++j)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          hf[j][e] *= dL;
-          hl[j][e] = 0.f;
+        for (int hh = 0; hh < 2; ++hh) {
+          const int key = 16 * hm + g4 + 8 * hh;
+          const int col = 8 * (hn0 + j) + 2 * t4;
+          *reinterpret_cast<float2 *>(ht + (sbase + key) * V + vt0 + col) = make_float2(hf[j][2 * hh], hf[j][2 * hh + 1]);
         }
+    }
+  } else {
+    // ----------------------------------------------------------------- side
+    const bool issuer = (tid == NTH);
+    int tma_hi = 0;
+    auto issue = [&](int c) {
+      const int s = c % NS;
+      const uint32_t st = sb + s * Ly::STAGE;
+      const int trow = static_cast<int>(tok0) + c * C;
+      mbar_arrive_expect_tx(bar(FULL, s), Ly::TX);
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
+      for (int a = 0; a < KA; ++a) {
+        tma_load_3d(st + a * 16384, &tm_k, bar(FULL, s), 64 * a, h, trow);
+        tma_load_3d(st + a * 16384 + 8192, &tm_q, bar(FULL, s), 64 * a, h, trow);
+      }
+      tma_load_3d(st + Ly::KQB, &tm_v, bar(FULL, s), vt0, hv, trow);
+      bulk_load(st + Ly::KQB + Ly::V_BYTES, ws + (static_cast<size_t>(cb + c) * HV + hv) * R::BYTES, R::BYTES,
+                bar(FULL, s));
+      tma_hi = c + 1;
+    };
+    if (issuer)
+      for (int c = 0; c < NS && c < NC; ++c) issue(c);
+    __syncwarp();
+    const float dscale = scale;
+    for (int c = 0; c < NC; ++c) {
+      const int s = c % NS;
+      const uint32_t st = sb + s * Ly::STAGE;
+      const uint32_t rc = st + Ly::KQB + Ly::V_BYTES;
+      const float *rsc = reinterpret_cast<const float *>(sm + s * Ly::STAGE + Ly::KQB + Ly::V_BYTES + R::SC);
+      const int64_t remc = len - static_cast<int64_t>(c) * C;
+      const int L = static_cast<int>(remc < C ? remc : C);
+      const int64_t trow0 = tok0 + static_cast<int64_t>(c) * C;
+      // Q h_c, h as hi + lo.
+      bool go = waitc(FULL, c);
+      go = waitc(HREADY, c) && go;
+      float aq[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      float aql[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      if (go) {
+#pragma unroll
+      for (int kk = 0; kk < K / 16; ++kk) {
+        uint32_t fq[4], b[4], bl[4];
+        ldsm_x4(tile_addr(st, 128, 64 + 16 * mi + (lane & 15), 2 * kk + (lane >> 4)), fq);
         const int mq = lane >> 3;
-        uint32_t a[4];
-        // A = K^T: rows = keys 16 hm.., k = tokens 16 kk..; K is stored [token][key].
-        ldsm_x4_t(tile_addr(st, 128, 16 * kk + (lane & 7) + 8 * (mq >> 1), 2 * hm + (mq & 1)), a);
-#pragma unroll
-        for (int j = 0; j < NT8; j += 2) {
-          uint32_t b[4], bl[4];
-          const uint32_t ro = (16 * kk + (lane & 7) + 8 * (mq & 1)) * HROW + (hn0 + j + (mq >> 1)) * 16;
-          ldsm_x4_t(aVS + ro, b);
-          ldsm_x4_t(aVSL + ro, bl);
-          mma_bf16(hf[j], a, b[0], b[1]);
-          mma_bf16(hf[j + 1], a, b[2], b[3]);
-          mma_bf16(hl[j], a, bl[0], bl[1]);
-          mma_bf16(hl[j + 1], a, bl[2], bl[3]);
-        }
+        const uint32_t ho = (16 * kk + (lane & 7) + 8 * (mq & 1)) * HROW + (2 * nh + (mq >> 1)) * 16;
+        ldsm_x4_t(aH + ho, b);
+        ldsm_x4_t(aHL + ho, bl);
+        mma_bf16(aq[0], fq, b[0], b[1]);
+        mma_bf16(aq[1], fq, b[2], b[3]);
+        mma_bf16(aql[0], fq, bl[0], bl[1]);
+        mma_bf16(aql[1], fq, bl[2], bl[3]);
       }
-#pragma unroll
-      for (int j = 0; j < NT8; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) hf[j][e] += hl[j][e];
-      write_h();
-    }
-
-    // o = scale (e^gamma rq (Q h) + P v_new), P and v_new as bf16 hi + lo.
-    {
+      arrive(SHDONE, c);
+      }
+      // o = scale (e^gamma rq (Q h) + P v_new), P and v_new as bf16 hi + lo.
+      go = waitc(VREADY, c) && go;
       float ac[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      if (go) {
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         uint32_t ph[4], pl[4], bh[4], bl[4];
@@ -779,6 +857,7 @@ __global__ void __launch_bounds__(NTH, 1) chunk_walk_kernel(
         mma_bf16(ac[0], pl, bh[0], bh[1]);
         mma_bf16(ac[1], pl, bh[2], bh[3]);
       }
+      arrive(SVDONE, c);
 #pragma unroll
       for (int j = 0; j < 2; ++j)
 #pragma unroll
@@ -792,28 +871,24 @@ __global__ void __launch_bounds__(NTH, 1) chunk_walk_kernel(
             *reinterpret_cast<uint32_t *>(o + ((trow0 + r) * HV + hv) * V + vt0 + col) = pack_bf16(o0, o1);
           }
         }
-    }
-    __syncthreads();
-    // Stage s is free: thread 0 refills it with chunk c + NS.
-    if (tid == 0 && c + NS < NC) issue(c + NS);
-  }
-  if (tid == 0) {
-    // Only after an abort can a copy of this CTA still be in flight here.
-    if (*abort_flag)
-      for (int k = (tma_hi > NS ? tma_hi - NS : 0); k < tma_hi; ++k)
-        mbar_wait_bounded(b_full(k % NS), (k / NS) & 1, kWaitLimit);
-    if (*abort_flag) set_status(dev_status, GDN_DEV_WAIT_TIMEOUT);
-  }
-  if (ht && !misc[2]) {
-#pragma unroll
-    for (int j = 0; j < NT8; ++j)
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int key = 16 * hm + g4 + 8 * hh;
-        const int col = 8 * (hn0 + j) + 2 * t4;
-        *reinterpret_cast<float2 *>(ht + (sbase + key) * V + vt0 + col) = make_float2(hf[j][2 * hh], hf[j][2 * hh + 1]);
       }
+      // Both groups are done with stage s once the chain has signalled and every
+      // side warp is past this point: refill it with chunk c + 2.
+      named_bar_sync(2, NTH);
+      if (warp == 8 && c + NS < NC) {
+        const bool can = waitc(CDONE, c) && go;
+        if (issuer && can) issue(c + NS);
+        __syncwarp();
+      }
+    }
+    if (issuer && *abort_flag) {
+      // Nothing of this CTA may still be in flight at exit.
+      for (int k = (tma_hi > NS ? tma_hi - NS : 0); k < tma_hi; ++k)
+        mbar_wait_bounded(bar(FULL, k % NS), (k / NS) & 1, kWaitLimit);
+    }
   }
+  __syncthreads();
+  if (tid == 0 && *abort_flag) set_status(dev_status, GDN_DEV_WAIT_TIMEOUT);
 }
 
 // ---------------------------------------------------------------- host side
@@ -885,7 +960,7 @@ cudaError_t launch_k(const gdn_host::ChunkArgs &a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(chunk_walk_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, wsmem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.V / VT, a.HV, a.N);
-  chunk_walk_kernel<K><<<grid, NTH, wsmem, s>>>(mq, mk, mv, a.scale, a.h0, a.cu, a.T, a.H, a.HV, a.V,
+  chunk_walk_kernel<K><<<grid, WNTH, wsmem, s>>>(mq, mk, mv, a.scale, a.h0, a.cu, a.T, a.H, a.HV, a.V,
                                                 static_cast<const unsigned char *>(a.ws), a.o, a.ht, a.dev_status);
   return cudaGetLastError();
 }
