@@ -26,15 +26,16 @@
 // 128B-swizzled smem operands, fp32 accumulator in TMEM), whose diagonal gives
 // the row norms; A and P are built from TMEM; T by 16x16 diagonal-block
 // substitution plus tf32 mma.sync for the off-diagonal blocks, in place; W by
-// mma.sync.  The CTA writes one record [W | P hi | P lo | Ts | scalars] per
+// mma.sync.  The CTA writes one record [W | P hi | P lo | Ts^T | scalars] per
 // (chunk, value head) to the workspace, laid out exactly as the walk kernel
 // wants it in shared memory.
 //
 // gdn_chunk_walk (one CTA per (32-column slice, value head, sequence)): keeps
-// the fp32 state slice in registers; per chunk one thread issues the TMA
-// loads of K, Q, the V slice and a bulk copy of the record into a two-stage
-// ring, and the eight warps run u, [Q; W] h, v_new, the state update and o
-// with mma.sync, two CTA barriers per chunk.
+// the fp32 state slice in registers; a producer warp streams K, Q, a 64-column
+// V box and the record into a two-stage ring with TMA / bulk copies, and eight
+// compute warps run the four products of a chunk on tcgen05 (TMEM
+// accumulators, smem operands): [W; Q] h, K^T (s v_new), [P_hi; P_lo] v_new
+// and Ts V, with v_new, the state update and o in the epilogues.
 //
 // Precision: the main terms of o (P v_new and Q h) and the state update split
 // their computed factor into bf16 hi + lo parts (the raw bf16 q, k, v are
@@ -58,7 +59,6 @@ constexpr int VT = 32;
 constexpr int NW = 8;
 constexpr int NTH = NW * 32;
 constexpr long long kWaitLimit = 2000000000LL;  // clock cycles (about 1 s) before a wait gives up
-constexpr int HROW = 80;                        // bytes per padded row of 32 bf16
 constexpr int FROW = 68;                        // floats per padded fp32 row of 64
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -482,7 +482,14 @@ __global__ void __launch_bounds__(NTH, 2) chunk_prep_kernel(
       tsv = make_uint4(ts[0], ts[1], ts[2], ts[3]);
     }
     *reinterpret_cast<uint4 *>(sm + Ly::OFF_TP + sw128(i, ch)) = tpv;
-    *reinterpret_cast<uint4 *>(rec + R::TS + sw128(i, ch)) = tsv;
+    // Ts goes out transposed (row j holds column j of Ts), the MN-major A
+    // operand of the walk's u = Ts V product.
+    const uint32_t tsw[4] = {tsv.x, tsv.y, tsv.z, tsv.w};
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      const uint16_t x = static_cast<uint16_t>((jj & 1) ? (tsw[jj >> 1] >> 16) : (tsw[jj >> 1] & 0xFFFFu));
+      *reinterpret_cast<uint16_t *>(rec + R::TS + sw128(8 * ch + jj, i >> 3) + (i & 7) * 2) = x;
+    }
   }
   __syncthreads();
 
@@ -527,33 +534,58 @@ __global__ void __launch_bounds__(NTH, 2) chunk_prep_kernel(
 }
 
 // ============================================================== walk kernel
-// Sixteen warps in two groups that hand data to each other through mbarriers:
-//   chain (warps 0-7): u = beta v + Ts V, W h, v_new = u - W h, the state update
-//     h <- e^{gamma_L} h + K^T (s v_new) and the bf16 copy of h;
-//   side (warps 8-15): Q h (hi + lo) while the chain works, o = scale (e^gamma rq
-//     Q h + P v_new) once v_new is out, and (thread 256) the TMA / bulk loads of
-//     chunk c+2 once both groups are done with chunk c.
+// Nine warps.  Every product runs on tcgen05 with fp32 accumulators in TMEM.
+// A thread needs about 100 cycles to issue one tcgen05.mma while issues from
+// different warps overlap, and every hand-off through an mbarrier costs far
+// more while the tensor core and TMA keep shared memory busy; so the compute
+// warps issue all products themselves, each split over two warps into two
+// partial accumulators that the epilogues add up.
+//  * Compute warps 0-7: thread (lane group w & 3, column half w >> 2) owns TMEM
+//    lane r = 32 (w & 3) + lane and 16 of the slice's 32 columns, and holds the
+//    fp32 state h[r][16 columns] in registers.  Per chunk c:
+//      [W; Q] [h_hi | h_lo] -> ACC1 (warps 0-1);
+//      meanwhile the output of chunk c - 1 from ACC3 and the staged Q h;
+//      lanes 0-63: v_new = beta v + u - W h -> s v_new, v_new (bf16 hi | lo);
+//      lanes 64-127: e^gamma rq (Q h) -> QH, kept for the output;
+//      then K^T [s v_new hi | lo] -> ACC2 (warps 0-1),
+//      [P_hi; P_lo] [v_new hi | lo] -> ACC3 (warps 2-3) and
+//      u(c + 1) = Ts V -> ACC4 (warps 6-7);
+//      h <- e^{gamma_L} h + ACC2, written back as [h_hi | h_lo].
+//  * Warp 8: TMA / bulk loads of chunk c + 2 into the stage chunk c released.
 template <int K>
 struct WalkLay {
-  static constexpr int KQB = KQ<K>::BYTES;
-  static constexpr int V_BYTES = C * VT * 2;
-  static constexpr int STAGE = KQB + V_BYTES + Rec<K>::BYTES;  // [K;Q] | V slice | record
+  static constexpr int KA = K / 64;
+  static constexpr int KT = 0;                           // K tile [token][key], KA x 8 KB (TMA)
+  static constexpr int WQ = KT + KA * 8192;              // [W; Q], KA x 16 KB (W: record, Q: TMA)
+  static constexpr int VB = WQ + KA * 16384;             // V [token][64 columns] SW128 (TMA)
+  static constexpr int RR = VB + 8192;                   // record from P hi on: PH | PL | TS | SC
+  static constexpr int RR_BYTES = Rec<K>::BYTES - Rec<K>::PH;
+  static constexpr int STAGE = RR + RR_BYTES;
   static constexpr int NS = 2;
-  static constexpr int OFF_H = NS * STAGE;                     // h bf16 hi [K][HROW] then lo
-  static constexpr int OFF_VS = OFF_H + 2 * K * HROW;          // s v_new hi, lo (chain only)
-  static constexpr int OFF_VH = OFF_VS + 2 * 64 * HROW;        // v_new hi, lo (chain -> side)
-  static constexpr int OFF_BAR = OFF_VH + 2 * 64 * HROW;
-  static constexpr int NBAR = 2 * 7;
+  static constexpr int OFF_H = NS * STAGE;               // [K][64] bf16 (h hi | h lo), MN-major SW128
+  static constexpr int OFF_VS = OFF_H + K * 128;         // [64][64] bf16 (s v_new hi | lo), MN-major SW128
+  static constexpr int OFF_VN = OFF_VS + 8192;           // [64][64] bf16 (v_new hi | lo), MN-major SW128
+  static constexpr int OFF_Z = OFF_VN + 8192;            // 8 KB of zeros: missing rows 64-127 of an M = 128 operand
+  static constexpr int XROW = 36;
+  static constexpr int OFF_X = OFF_Z + 8192;             // fp32 [64][XROW]: P_hi v_new of the output
+  static constexpr int OFF_QH = OFF_X + 64 * XROW * 4;   // fp32 [64][XROW]: e^gamma rq Q h
+  static constexpr int OFF_BAR = OFF_QH + 64 * XROW * 4;
+  static constexpr int NBAR = 12;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
   static constexpr int BYTES = OFF_MISC + 16;
-  static constexpr uint32_t TX = KQB + V_BYTES + Rec<K>::BYTES;
-  static_assert(STAGE % 1024 == 0, "stage alignment");
+  static constexpr uint32_t TX = STAGE;                  // every byte of a stage is loaded per chunk
+  // TMEM columns: two partials of 64 each for ACC1, ACC2, ACC3 and ACC4.
+  static constexpr uint32_t ACC1 = 0, ACC2 = 128, ACC3 = 256, ACC4 = 384;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static_assert(STAGE % 1024 == 0 && OFF_H % 1024 == 0 && OFF_VS % 1024 == 0 && OFF_Z % 1024 == 0,
+                "swizzled tile alignment");
   static_assert(BYTES + 1024 <= 232448, "shared memory budget (227 KB per CTA)");
 };
-constexpr int WNTH = 2 * NTH;  // 512 threads
+constexpr int WALK_COMPUTE = 256;
+constexpr int WALK_THREADS = WALK_COMPUTE + 32;
 
 template <int K>
-__global__ void __launch_bounds__(WNTH, 1) chunk_walk_kernel(
+__global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, float scale, const float *__restrict__ h0,
     const int32_t *__restrict__ cu, int T, int H, int HV, int V, const unsigned char *__restrict__ ws,
@@ -562,16 +594,16 @@ __global__ void __launch_bounds__(WNTH, 1) chunk_walk_kernel(
   using R = Rec<K>;
   constexpr int KA = K / 64;
   constexpr int NS = Ly::NS;
+  constexpr int XROW = Ly::XROW;
+  constexpr int TSO = Ly::RR + (R::TS - R::PH);          // Ts^T within a stage
+  constexpr int SCO = Ly::RR + (R::SC - R::PH);          // scalars within a stage
   extern __shared__ unsigned char smem_raw[];
   unsigned char *sm = align1024(smem_raw);
   const uint32_t sb = smem_u32(sm);
   const int vt0 = blockIdx.x * VT, hv = blockIdx.y, n = blockIdx.z;
+  const int vhalf = vt0 & 32;                            // this slice within its 64-column V box
   const int h = hv / (HV / H);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g4 = lane >> 2, t4 = lane & 3;
-  const bool chain = warp < 8;
-  const int gw = warp & 7;                  // warp index within its group
-  const int mi = gw & 3, nh = gw >> 2;      // 16-row tile, 16-column half (64-row products)
 
   int64_t tok0, len;
   if (!seq_bounds(cu, n, T, tok0, len)) {
@@ -582,29 +614,42 @@ __global__ void __launch_bounds__(WNTH, 1) chunk_walk_kernel(
   const int64_t cb = chunk_base(cu, n, T);
   uint32_t *misc = reinterpret_cast<uint32_t *>(sm + Ly::OFF_MISC);
   volatile uint32_t *abort_flag = misc + 1;
-  // Barriers, two of each (indexed by chunk parity): TMA full; (unused); h ready;
-  // v_new ready; chain done with the stage; side done with h; side done with v_new.
+  // Two-slot barriers, slot c & 1 serving chunk c: FULL (loads landed),
+  // UREADY (ACC4 holds u), CDONE (the compute warps and their first two
+  // products are done with the stage), M3 (the output product is done); then
+  // the completions of the first and second products.
+  enum { FULL = 0, UREADY = 1, CDONE = 2, M3 = 3 };
   auto bar = [&](int kind, int b) { return sb + Ly::OFF_BAR + 8 * (2 * kind + b); };
-  enum { FULL = 0, HREADY = 2, VREADY = 3, CDONE = 4, SHDONE = 5, SVDONE = 6 };
+  const uint32_t b_m1 = sb + Ly::OFF_BAR + 64, b_m2 = sb + Ly::OFF_BAR + 72;
   if (tid == 0) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(FULL, b), 1);
-      for (int kd = 1; kd < 7; ++kd) mbar_init(bar(kd, b), 8);
+      mbar_init(bar(UREADY, b), 2);
+      mbar_init(bar(CDONE, b), 1);
+      mbar_init(bar(M3, b), 2);
     }
+    mbar_init(b_m1, 2);
+    mbar_init(b_m2, 2);
     misc[1] = 0;
     mbar_fence_init();
   }
+  for (int e = tid; e < 8192 / 16; e += WALK_THREADS)
+    reinterpret_cast<uint4 *>(sm + Ly::OFF_Z)[e] = make_uint4(0, 0, 0, 0);
+  if (warp == 0) tmem_alloc(sb + Ly::OFF_MISC, Ly::TMEM_COLS);
+  fence_proxy_async_smem();
+  tc_fence_before();
   __syncthreads();
-  // Waits on chunk c's use of a barrier (each barrier serves every other chunk).
-  // Lane 0 polls; __syncwarp orders the other lanes' later reads after its
-  // acquire, and the result is warp-uniform.  After any expired wait every
-  // later wait returns false at once: the loops then run to their end without
-  // work but still pass every named barrier, so no warp is left waiting.
-  auto waitc = [&](int kind, int c) -> bool {
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+
+  // Bounded wait; lane 0 polls and the result is warp-uniform.  After an
+  // expired wait every later wait returns false at once: loops run to their
+  // end without work but still pass every named barrier.
+  auto waitb = [&](uint32_t b, uint32_t parity) -> bool {
     uint32_t ok = 0;
     if (lane == 0) {
       ok = !*abort_flag;
-      if (ok && !mbar_wait_bounded(bar(kind, c & 1), (c >> 1) & 1, kWaitLimit)) {
+      if (ok && !mbar_spin_bounded(b, parity, kWaitLimit)) {
         *abort_flag = 1;
         ok = 0;
       }
@@ -612,282 +657,325 @@ __global__ void __launch_bounds__(WNTH, 1) chunk_walk_kernel(
     __syncwarp();
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
   };
-  auto arrive = [&](int kind, int c) {
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar(kind, c & 1));
+  auto waitc = [&](int kind, int c) { return waitb(bar(kind, c & 1), (c >> 1) & 1); };
+  auto chunk_rows = [&](int c) {
+    const int64_t rem = len - static_cast<int64_t>(c) * C;
+    return static_cast<int>(rem < C ? rem : C);
   };
-
-  const uint32_t aH = sb + Ly::OFF_H, aHL = aH + K * HROW;
-  const uint32_t aVS = sb + Ly::OFF_VS, aVSL = aVS + 64 * HROW;
-  const uint32_t aVH = sb + Ly::OFF_VH, aVL = aVH + 64 * HROW;
   const int64_t sbase = (static_cast<int64_t>(n) * HV + hv) * K;
+  float *X = reinterpret_cast<float *>(sm + Ly::OFF_X);
+  float *QH = reinterpret_cast<float *>(sm + Ly::OFF_QH);
 
-  if (chain) {
-    // ---------------------------------------------------------------- chain
-    constexpr int NT8 = (K / 16) * 4 / 8;  // state n-tiles per warp
-    const int hm = gw % (K / 16);
-    const int hn0 = (gw / (K / 16)) * NT8;
-    float hf[NT8][4];
+  if (warp < 8) {
+    // ------------------------------------------------------- compute warps
+    const int r = 32 * (warp & 3) + lane;                // TMEM lane
+    const int hs = warp >> 2;                            // column half: columns 16 hs .. 16 hs + 15
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    const bool krow = r < K;
+    float hr[16];
 #pragma unroll
-    for (int j = 0; j < NT8; ++j)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int key = 16 * hm + g4 + 8 * (e >> 1);
-        const int col = 8 * (hn0 + j) + 2 * t4 + (e & 1);
-        hf[j][e] = h0 ? h0[(sbase + key) * V + vt0 + col] : 0.f;
-      }
-    unsigned char *Hb = sm + Ly::OFF_H;
+    for (int j = 0; j < 16; ++j) hr[j] = (h0 && krow) ? h0[(sbase + r) * V + vt0 + 16 * hs + j] : 0.f;
+    // Row r of h -> columns [16 hs, 16 hs + 16) of the hi and lo halves of the
+    // MN-major SW128 H tile.
     auto write_h = [&]() {
+      if (!krow) return;
+      unsigned char *row = sm + Ly::OFF_H + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
-      for (int j = 0; j < NT8; ++j)
+      for (int m = 0; m < 2; ++m) {
+        uint32_t hi[4], lo[4];
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int key = 16 * hm + g4 + 8 * hh;
-          const int col = 8 * (hn0 + j) + 2 * t4;
-          const float x0 = hf[j][2 * hh], x1 = hf[j][2 * hh + 1];
-          const uint32_t hi = pack_bf16(x0, x1);
-          *reinterpret_cast<uint32_t *>(Hb + key * HROW + col * 2) = hi;
-          *reinterpret_cast<uint32_t *>(Hb + (K + key) * HROW + col * 2) = pack_bf16(x0 - bf16lo_f(hi), x1 - bf16hi_f(hi));
+        for (int e = 0; e < 4; ++e) {
+          const float x0 = hr[8 * m + 2 * e], x1 = hr[8 * m + 2 * e + 1];
+          hi[e] = pack_bf16(x0, x1);
+          lo[e] = pack_bf16(x0 - bf16lo_f(hi[e]), x1 - bf16hi_f(hi[e]));
         }
+        const int chh = 2 * hs + m;
+        *reinterpret_cast<uint4 *>(row + ((chh ^ (r & 7)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4 *>(row + (((4 + chh) ^ (r & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+    };
+    // Sum of the hi and lo column blocks of NP partial accumulators at `base`.
+    auto sum_partials = [&](uint32_t base, int np, float *acc) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+      for (int p = 0; p < np; p += 2) {
+        uint32_t x0[16], y0[16], x1[16], y1[16];
+        tmem_ld16_issue(tl + base + 64 * p + 16 * hs, x0);
+        tmem_ld16_issue(tl + base + 64 * p + 32 + 16 * hs, y0);
+        tmem_ld16_issue(tl + base + 64 * (p + 1) + 16 * hs, x1);
+        tmem_ld16_issue(tl + base + 64 * (p + 1) + 32 + 16 * hs, y1);
+        tmem_ld_wait16(x0);
+        tmem_ld_wait16(y0);
+        tmem_ld_wait16(x1);
+        tmem_ld_wait16(y1);
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          acc[j] += (__uint_as_float(x0[j]) + __uint_as_float(y0[j])) + (__uint_as_float(x1[j]) + __uint_as_float(y1[j]));
+      }
+    };
+    // Output of chunk c, from ACC3 (P_hi rows in lanes 0-63, P_lo rows in
+    // lanes 64-127; two partials) and the staged e^gamma rq Q h.
+    auto output = [&](int c, bool go) {
+      go = waitc(M3, c) && go;
+      if (go && r < 64) {
+        tc_fence_after();
+        float pv[16];
+        sum_partials(Ly::ACC3, 2, pv);
+        float *x = X + r * XROW + 16 * hs;
+#pragma unroll
+        for (int j = 0; j < 16; j += 4) *reinterpret_cast<float4 *>(x + j) = make_float4(pv[j], pv[j + 1], pv[j + 2], pv[j + 3]);
+      }
+      named_bar_sync(1, WALK_COMPUTE);
+      if (go && r >= 64) {
+        tc_fence_after();
+        const int i = r - 64;
+        uint32_t a[16], b[16];
+        tmem_ld16_issue(tl + Ly::ACC3 + 16 * hs, a);
+        tmem_ld16_issue(tl + Ly::ACC3 + 64 + 16 * hs, b);
+        tmem_ld_wait16(a);
+        tmem_ld_wait16(b);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) a[j] = __float_as_uint(__uint_as_float(a[j]) + __uint_as_float(b[j]));
+        if (i < chunk_rows(c)) {
+          const float *x = X + i * XROW + 16 * hs;
+          const float *qh = QH + i * XROW + 16 * hs;
+          const int64_t trow = tok0 + static_cast<int64_t>(c) * C + i;
+          uint4 *dst = reinterpret_cast<uint4 *>(o + (trow * HV + hv) * V + vt0 + 16 * hs);
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int j = 8 * m + 2 * e;
+              w[e] = pack_bf16(scale * (qh[j] + x[j] + __uint_as_float(a[j])),
+                               scale * (qh[j + 1] + x[j + 1] + __uint_as_float(a[j + 1])));
+            }
+            dst[m] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+      return go;
+    };
+    // u(c) = Ts V, k-steps 2q, 2q + 1 into partial q of ACC4; Ts^T is the
+    // MN-major A operand whose rows 64-127 come from the zero block.
+    auto issue_u = [&](int c, int q) {
+      const int s = c % NS;
+      const uint32_t st = sb + s * Ly::STAGE;
+      tc_fence_after();
+      constexpr uint32_t id4 = umma_idesc_bf16(128, 64, 1, 1);
+      const uint32_t lbo = static_cast<uint32_t>(Ly::OFF_Z - s * Ly::STAGE - TSO);
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        const int kk = 2 * q + m;
+        const uint64_t a = umma_desc_sw128_mn(st + TSO + kk * 2048, lbo);
+        const uint64_t b = umma_desc_sw128_mn(st + Ly::VB + kk * 2048, 8192);
+        umma_bf16(tmem + Ly::ACC4 + 64 * q, a, b, id4, m > 0 ? 1u : 0u);
+      }
+      umma_commit(bar(UREADY, c & 1));
     };
     write_h();
-    named_bar_sync(1, NTH);
-    arrive(HREADY, 0);
-
+    fence_proxy_async_smem();
+    named_bar_sync(1, WALK_COMPUTE);
+    int n1 = 0, n2 = 0, n3 = 0, n4 = 0;  // products issued by this thread
+    if ((warp == 6 || warp == 7) && NC > 0) {
+      if (waitc(FULL, 0) && lane == 0) {
+        issue_u(0, warp - 6);
+        ++n4;
+      }
+      __syncwarp();
+    }
+    bool go = true;
     for (int c = 0; c < NC; ++c) {
       const int s = c % NS;
       const uint32_t st = sb + s * Ly::STAGE;
-      const uint32_t rc = st + Ly::KQB + Ly::V_BYTES;
-      const float *rsc = reinterpret_cast<const float *>(sm + s * Ly::STAGE + Ly::KQB + Ly::V_BYTES + R::SC);
-      bool go = waitc(FULL, c);
-      if (go) {
-      // u = beta v + Ts V for rows 16 mi.., columns 16 nh.. (registers).  Rows >= L
-      // of the V slice may hold the next sequence's values; beta and the Ts
-      // columns are zero there, so they do not contribute.
-      float u[2][4];
-      {
-        const uint32_t stV = st + Ly::KQB;
-        const unsigned char *stp = sm + s * Ly::STAGE;
-        float au[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      const unsigned char *stp = sm + s * Ly::STAGE;
+      const float *rsc = reinterpret_cast<const float *>(stp + SCO);
+      go = waitc(FULL, c) && go;
+      // [W; Q] [h_hi | h_lo]: warp p < 2 takes k-steps [p K / 32, p K / 32 + K / 32).
+      if (warp < 2 && lane == 0 && go) {
+        tc_fence_after();
+        constexpr uint32_t id1 = umma_idesc_bf16(128, 64, 0, 1);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          uint32_t as[4], bv[4];
-          ldsm_x4(rc + R::TS + sw128(16 * mi + (lane & 15), 2 * kk + (lane >> 4)), as);
-          const int mq = lane >> 3;
-          ldsm_x4_t(stV + (16 * kk + (lane & 7) + 8 * (mq & 1)) * 64 + (2 * nh + (mq >> 1)) * 16, bv);
-          mma_bf16(au[0], as, bv[0], bv[1]);
-          mma_bf16(au[1], as, bv[2], bv[3]);
+        for (int m = 0; m < K / 32; ++m) {
+          const int kk = warp * (K / 32) + m;
+          const uint64_t a = umma_desc_sw128(st + Ly::WQ + (kk >> 2) * 16384 + (kk & 3) * 32);
+          const uint64_t b = umma_desc_sw128_mn(sb + Ly::OFF_H + kk * 2048, 8192);
+          umma_bf16(tmem + Ly::ACC1 + 64 * warp, a, b, id1, m > 0 ? 1u : 0u);
         }
+        umma_commit(b_m1);
+        ++n1;
+      }
+      __syncwarp();
+      // Output of the previous chunk while this product runs.
+      if (c >= 1) go = output(c - 1, go);
+      go = waitb(b_m1, c & 1) && go;
+      go = waitc(UREADY, c) && go;
+      const float dL = go ? rsc[RS_DL] : 0.f;
+      if (go) {
+        tc_fence_after();
+        float wh[16];
+        sum_partials(Ly::ACC1, 2, wh);
+        if (r < 64) {
+          // v_new = beta v + u - W (h_hi + h_lo); s v_new and v_new as bf16 hi | lo.
+          const int i = r;
+          uint32_t u[16];
+          uint32_t u2[16];
+          tmem_ld16_issue(tl + Ly::ACC4 + vhalf + 16 * hs, u);
+          tmem_ld16_issue(tl + Ly::ACC4 + 64 + vhalf + 16 * hs, u2);
+          const float bt = rsc[RS_BET + i], sv = rsc[RS_SV + i];
+          const int vc = (vhalf + 16 * hs) >> 3;
+          uint4 vv[2];
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
+          for (int m = 0; m < 2; ++m)
+            vv[m] = *reinterpret_cast<const uint4 *>(stp + Ly::VB + i * 128 + (((vc + m) ^ (i & 7)) << 4));
+          tmem_ld_wait16(u);
+          tmem_ld_wait16(u2);
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int r = 16 * mi + g4 + 8 * hh;
-            const int col = 16 * nh + 8 * j + 2 * t4;
-            const float bt = rsc[RS_BET + r];
-            float v0 = 0.f, v1 = 0.f;
-            if (bt != 0.f) {
-              const uint32_t vv = *reinterpret_cast<const uint32_t *>(stp + Ly::KQB + r * 64 + col * 2);
-              v0 = bf16lo_f(vv);
-              v1 = bf16hi_f(vv);
+          for (int j = 0; j < 16; ++j) u[j] = __float_as_uint(__uint_as_float(u[j]) + __uint_as_float(u2[j]));
+          unsigned char *vsr = sm + Ly::OFF_VS + (i >> 3) * 1024 + (i & 7) * 128;
+          unsigned char *vnr = sm + Ly::OFF_VN + (i >> 3) * 1024 + (i & 7) * 128;
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {
+            const uint32_t vw[4] = {vv[m].x, vv[m].y, vv[m].z, vv[m].w};
+            uint32_t yh[4], yl[4], xh[4], xl[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int j = 8 * m + 2 * e;
+              const float x0 = fmaf(bt, bf16lo_f(vw[e]), __uint_as_float(u[j])) - wh[j];
+              const float x1 = fmaf(bt, bf16hi_f(vw[e]), __uint_as_float(u[j + 1])) - wh[j + 1];
+              xh[e] = pack_bf16(x0, x1);
+              xl[e] = pack_bf16(x0 - bf16lo_f(xh[e]), x1 - bf16hi_f(xh[e]));
+              const float y0 = sv * x0, y1 = sv * x1;
+              yh[e] = pack_bf16(y0, y1);
+              yl[e] = pack_bf16(y0 - bf16lo_f(yh[e]), y1 - bf16hi_f(yh[e]));
             }
-            u[j][2 * hh] = fmaf(bt, v0, au[j][2 * hh]);
-            u[j][2 * hh + 1] = fmaf(bt, v1, au[j][2 * hh + 1]);
+            const int chh = 2 * hs + m;
+            *reinterpret_cast<uint4 *>(vsr + ((chh ^ (i & 7)) << 4)) = make_uint4(yh[0], yh[1], yh[2], yh[3]);
+            *reinterpret_cast<uint4 *>(vsr + (((4 + chh) ^ (i & 7)) << 4)) = make_uint4(yl[0], yl[1], yl[2], yl[3]);
+            *reinterpret_cast<uint4 *>(vnr + ((chh ^ (i & 7)) << 4)) = make_uint4(xh[0], xh[1], xh[2], xh[3]);
+            *reinterpret_cast<uint4 *>(vnr + (((4 + chh) ^ (i & 7)) << 4)) = make_uint4(xl[0], xl[1], xl[2], xl[3]);
           }
-      }
-
-      // W h (hi part of h): rows 16 mi.., columns 16 nh..
-      float aw[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        } else {
+          const int i = r - 64;
+          const float og = rsc[RS_OG + i];
+          float *q = QH + i * XROW + 16 * hs;
 #pragma unroll
-      for (int kk = 0; kk < K / 16; ++kk) {
-        uint32_t fw[4], b[4];
-        ldsm_x4(tile_addr(rc + R::W, 64, 16 * mi + (lane & 15), 2 * kk + (lane >> 4)), fw);
-        const int mq = lane >> 3;
-        ldsm_x4_t(aH + (16 * kk + (lane & 7) + 8 * (mq & 1)) * HROW + (2 * nh + (mq >> 1)) * 16, b);
-        mma_bf16(aw[0], fw, b[0], b[1]);
-        mma_bf16(aw[1], fw, b[2], b[3]);
-      }
-      // v_new = u - W h; s v_new (hi, lo) for the state update, v_new (hi, lo) for o.
-      if (c >= 1) go = waitc(SVDONE, c - 1) && go;
-      if (go) {
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int col = 16 * nh + 8 * j + 2 * t4;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int r = 16 * mi + g4 + 8 * hh;
-          const float x0 = u[j][2 * hh] - aw[j][2 * hh], x1 = u[j][2 * hh + 1] - aw[j][2 * hh + 1];
-          const uint32_t hi = pack_bf16(x0, x1);
-          const uint32_t lo = pack_bf16(x0 - bf16lo_f(hi), x1 - bf16hi_f(hi));
-          const float sr = rsc[RS_SV + r];
-          const float y0 = sr * x0, y1 = sr * x1;
-          const uint32_t yh = pack_bf16(y0, y1);
-          const uint32_t yl = pack_bf16(y0 - bf16lo_f(yh), y1 - bf16hi_f(yh));
-          unsigned char *vs = sm + Ly::OFF_VS + r * HROW + col * 2;
-          *reinterpret_cast<uint32_t *>(vs) = yh;
-          *reinterpret_cast<uint32_t *>(vs + 64 * HROW) = yl;
-          unsigned char *vh = sm + Ly::OFF_VH + r * HROW + col * 2;
-          *reinterpret_cast<uint32_t *>(vh) = hi;
-          *reinterpret_cast<uint32_t *>(vh + 64 * HROW) = lo;
+          for (int j = 0; j < 16; j += 4)
+            *reinterpret_cast<float4 *>(q + j) = make_float4(og * wh[j], og * wh[j + 1], og * wh[j + 2], og * wh[j + 3]);
         }
       }
-      }
-      }
-      named_bar_sync(1, NTH);
-      if (go) arrive(VREADY, c);
-
-      // h = e^{gamma_L} h + K^T (s v_new), hi and lo parts.
-      if (go) {
-        const float dL = rsc[RS_DL];
-        float hl[NT8][4];
+      tc_fence_before();
+      fence_proxy_async_smem();
+      named_bar_sync(1, WALK_COMPUTE);
+      // K^T [s v_new hi | lo]: warp q < 2 takes k-steps 2q, 2q + 1.  For K = 64
+      // the keys 64-127 of the M = 128 operand come from the zero block.
+      if (warp < 2 && lane == 0 && go) {
+        tc_fence_after();
+        constexpr uint32_t id2 = umma_idesc_bf16(128, 64, 1, 1);
+        const uint32_t lbo = (K == 64) ? static_cast<uint32_t>(Ly::OFF_Z - s * Ly::STAGE - Ly::KT) : 8192u;
 #pragma unroll
-        for (int j = 0; j < NT8; ++j)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            hf[j][e] *= dL;
-            hl[j][e] = 0.f;
-          }
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const int mq = lane >> 3;
-          uint32_t a[4];
-          ldsm_x4_t(tile_addr(st, 128, 16 * kk + (lane & 7) + 8 * (mq >> 1), 2 * hm + (mq & 1)), a);
-#pragma unroll
-          for (int j = 0; j < NT8; j += 2) {
-            uint32_t b[4], bl[4];
-            const uint32_t ro = (16 * kk + (lane & 7) + 8 * (mq & 1)) * HROW + (hn0 + j + (mq >> 1)) * 16;
-            ldsm_x4_t(aVS + ro, b);
-            ldsm_x4_t(aVSL + ro, bl);
-            mma_bf16(hf[j], a, b[0], b[1]);
-            mma_bf16(hf[j + 1], a, b[2], b[3]);
-            mma_bf16(hl[j], a, bl[0], bl[1]);
-            mma_bf16(hl[j + 1], a, bl[2], bl[3]);
-          }
+        for (int m = 0; m < 2; ++m) {
+          const int kk = 2 * warp + m;
+          const uint64_t a = umma_desc_sw128_mn(st + Ly::KT + kk * 2048, lbo);
+          const uint64_t b = umma_desc_sw128_mn(sb + Ly::OFF_VS + kk * 2048, 8192);
+          umma_bf16(tmem + Ly::ACC2 + 64 * warp, a, b, id2, m > 0 ? 1u : 0u);
         }
+        umma_commit(b_m2);
+        ++n2;
+      } else if ((warp == 2 || warp == 3) && lane == 0 && go) {
+        // [P_hi; P_lo] [v_new hi | lo]: warp 2 + q takes k-steps 2q, 2q + 1.
+        tc_fence_after();
+        const int q = warp - 2;
+        constexpr uint32_t id3 = umma_idesc_bf16(128, 64, 0, 1);
 #pragma unroll
-        for (int j = 0; j < NT8; ++j)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) hf[j][e] += hl[j][e];
+        for (int m = 0; m < 2; ++m) {
+          const int kk = 2 * q + m;
+          const uint64_t a = umma_desc_sw128(st + Ly::RR + kk * 32);
+          const uint64_t b = umma_desc_sw128_mn(sb + Ly::OFF_VN + kk * 2048, 8192);
+          umma_bf16(tmem + Ly::ACC3 + 64 * q, a, b, id3, m > 0 ? 1u : 0u);
+        }
+        umma_commit(bar(M3, c & 1));
+        ++n3;
       }
-      if (go) arrive(CDONE, c);  // this chunk's stage is no longer read by the chain
-      go = waitc(SHDONE, c) && go;  // the side group has read h_c
-      if (go) write_h();
-      named_bar_sync(1, NTH);
-      if (go) arrive(HREADY, c + 1);
+      __syncwarp();
+      if ((warp == 6 || warp == 7) && c + 1 < NC) {
+        // u(c + 1) = Ts V: warp 6 + q takes k-steps 2q, 2q + 1.  ACC4 was read
+        // for chunk c before the barrier above.
+        const bool g2 = waitc(FULL, c + 1) && go;
+        if (g2 && lane == 0) {
+          issue_u(c + 1, warp - 6);
+          ++n4;
+        }
+        __syncwarp();
+      }
+      go = waitb(b_m2, c & 1) && go;
+      if (tid == 0 && go) mbar_arrive(bar(CDONE, c & 1));  // nothing of this stage is read any more
+      if (go) {
+        tc_fence_after();
+        float dh[16];
+        sum_partials(Ly::ACC2, 2, dh);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) hr[j] = fmaf(dL, hr[j], dh[j]);
+        write_h();
+      }
+      tc_fence_before();
+      fence_proxy_async_smem();
+      named_bar_sync(1, WALK_COMPUTE);
     }
-    if (ht && !*abort_flag) {
+    if (NC > 0) go = output(NC - 1, go);
+    if (lane == 0 && *abort_flag) {
+      // After an abort a product may still be in flight: wait for the last of each.
+      if (n1 > 0) mbar_wait_bounded(b_m1, (n1 - 1) & 1, kWaitLimit);
+      if (n2 > 0) mbar_wait_bounded(b_m2, (n2 - 1) & 1, kWaitLimit);
+      if (n3 > 0) mbar_wait_bounded(bar(M3, (n3 - 1) & 1), ((n3 - 1) >> 1) & 1, kWaitLimit);
+      if (n4 > 0) mbar_wait_bounded(bar(UREADY, (n4 - 1) & 1), ((n4 - 1) >> 1) & 1, kWaitLimit);
+    }
+    if (ht && krow && !*abort_flag) {
 #pragma unroll
-      for (int j = 0; j < NT8; ++j)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int key = 16 * hm + g4 + 8 * hh;
-          const int col = 8 * (hn0 + j) + 2 * t4;
-          *reinterpret_cast<float2 *>(ht + (sbase + key) * V + vt0 + col) = make_float2(hf[j][2 * hh], hf[j][2 * hh + 1]);
-        }
+      for (int j = 0; j < 16; j += 4)
+        *reinterpret_cast<float4 *>(ht + (sbase + r) * V + vt0 + 16 * hs + j) =
+            make_float4(hr[j], hr[j + 1], hr[j + 2], hr[j + 3]);
     }
   } else {
-    // ----------------------------------------------------------------- side
-    const bool issuer = (tid == NTH);
-    int tma_hi = 0;
+    // ------------------------------------------------------------- producer
+    int issued = 0;
     auto issue = [&](int c) {
       const int s = c % NS;
       const uint32_t st = sb + s * Ly::STAGE;
       const int trow = static_cast<int>(tok0) + c * C;
+      const unsigned char *rec = ws + (static_cast<size_t>(cb + c) * HV + hv) * R::BYTES;
       mbar_arrive_expect_tx(bar(FULL, s), Ly::TX);
 #pragma unroll
       for (int a = 0; a < KA; ++a) {
-        tma_load_3d(st + a * 16384, &tm_k, bar(FULL, s), 64 * a, h, trow);
-        tma_load_3d(st + a * 16384 + 8192, &tm_q, bar(FULL, s), 64 * a, h, trow);
+        tma_load_3d(st + Ly::KT + a * 8192, &tm_k, bar(FULL, s), 64 * a, h, trow);
+        tma_load_3d(st + Ly::WQ + a * 16384 + 8192, &tm_q, bar(FULL, s), 64 * a, h, trow);
+        bulk_load(st + Ly::WQ + a * 16384, rec + R::W + a * 8192, 8192, bar(FULL, s));
       }
-      tma_load_3d(st + Ly::KQB, &tm_v, bar(FULL, s), vt0, hv, trow);
-      bulk_load(st + Ly::KQB + Ly::V_BYTES, ws + (static_cast<size_t>(cb + c) * HV + hv) * R::BYTES, R::BYTES,
-                bar(FULL, s));
-      tma_hi = c + 1;
+      tma_load_3d(st + Ly::VB, &tm_v, bar(FULL, s), vt0 - vhalf, hv, trow);
+      bulk_load(st + Ly::RR, rec + R::PH, Ly::RR_BYTES, bar(FULL, s));
+      issued = c + 1;
     };
-    if (issuer)
+    if (lane == 0)
       for (int c = 0; c < NS && c < NC; ++c) issue(c);
     __syncwarp();
-    const float dscale = scale;
-    for (int c = 0; c < NC; ++c) {
-      const int s = c % NS;
-      const uint32_t st = sb + s * Ly::STAGE;
-      const uint32_t rc = st + Ly::KQB + Ly::V_BYTES;
-      const float *rsc = reinterpret_cast<const float *>(sm + s * Ly::STAGE + Ly::KQB + Ly::V_BYTES + R::SC);
-      const int64_t remc = len - static_cast<int64_t>(c) * C;
-      const int L = static_cast<int>(remc < C ? remc : C);
-      const int64_t trow0 = tok0 + static_cast<int64_t>(c) * C;
-      // Q h_c, h as hi + lo.
-      bool go = waitc(FULL, c);
-      go = waitc(HREADY, c) && go;
-      float aq[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      float aql[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      if (go) {
-#pragma unroll
-      for (int kk = 0; kk < K / 16; ++kk) {
-        uint32_t fq[4], b[4], bl[4];
-        ldsm_x4(tile_addr(st, 128, 64 + 16 * mi + (lane & 15), 2 * kk + (lane >> 4)), fq);
-        const int mq = lane >> 3;
-        const uint32_t ho = (16 * kk + (lane & 7) + 8 * (mq & 1)) * HROW + (2 * nh + (mq >> 1)) * 16;
-        ldsm_x4_t(aH + ho, b);
-        ldsm_x4_t(aHL + ho, bl);
-        mma_bf16(aq[0], fq, b[0], b[1]);
-        mma_bf16(aq[1], fq, b[2], b[3]);
-        mma_bf16(aql[0], fq, bl[0], bl[1]);
-        mma_bf16(aql[1], fq, bl[2], bl[3]);
-      }
-      arrive(SHDONE, c);
-      }
-      // o = scale (e^gamma rq (Q h) + P v_new), P and v_new as bf16 hi + lo.
-      go = waitc(VREADY, c) && go;
-      float ac[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      if (go) {
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        uint32_t ph[4], pl[4], bh[4], bl[4];
-        ldsm_x4(rc + R::PH + sw128(16 * mi + (lane & 15), 2 * kk + (lane >> 4)), ph);
-        ldsm_x4(rc + R::PL + sw128(16 * mi + (lane & 15), 2 * kk + (lane >> 4)), pl);
-        const int mq = lane >> 3;
-        const uint32_t ro = (16 * kk + (lane & 7) + 8 * (mq & 1)) * HROW + (2 * nh + (mq >> 1)) * 16;
-        ldsm_x4_t(aVH + ro, bh);
-        ldsm_x4_t(aVL + ro, bl);
-        mma_bf16(ac[0], ph, bh[0], bh[1]);
-        mma_bf16(ac[1], ph, bh[2], bh[3]);
-        mma_bf16(ac[0], ph, bl[0], bl[1]);
-        mma_bf16(ac[1], ph, bl[2], bl[3]);
-        mma_bf16(ac[0], pl, bh[0], bh[1]);
-        mma_bf16(ac[1], pl, bh[2], bh[3]);
-      }
-      arrive(SVDONE, c);
-#pragma unroll
-      for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int r = 16 * mi + g4 + 8 * hh;
-          if (r < L) {
-            const int col = 16 * nh + 8 * j + 2 * t4;
-            const float ogr = rsc[RS_OG + r];
-            const float o0 = dscale * (ogr * (aq[j][2 * hh] + aql[j][2 * hh]) + ac[j][2 * hh]);
-            const float o1 = dscale * (ogr * (aq[j][2 * hh + 1] + aql[j][2 * hh + 1]) + ac[j][2 * hh + 1]);
-            *reinterpret_cast<uint32_t *>(o + ((trow0 + r) * HV + hv) * V + vt0 + col) = pack_bf16(o0, o1);
-          }
-        }
-      }
-      // Both groups are done with stage s once the chain has signalled and every
-      // side warp is past this point: refill it with chunk c + 2.
-      named_bar_sync(2, NTH);
-      if (warp == 8 && c + NS < NC) {
-        const bool can = waitc(CDONE, c) && go;
-        if (issuer && can) issue(c + NS);
-        __syncwarp();
-      }
+    for (int c = 0; c + NS < NC; ++c) {
+      bool can = waitc(CDONE, c);
+      can = waitc(M3, c) && can;
+      if (can && lane == 0) issue(c + NS);
+      __syncwarp();
     }
-    if (issuer && *abort_flag) {
+    if (lane == 0 && *abort_flag) {
       // Nothing of this CTA may still be in flight at exit.
-      for (int k = (tma_hi > NS ? tma_hi - NS : 0); k < tma_hi; ++k)
+      for (int k = (issued > NS ? issued - NS : 0); k < issued; ++k)
         mbar_wait_bounded(bar(FULL, k % NS), (k / NS) & 1, kWaitLimit);
     }
   }
+  tc_fence_before();
   __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Ly::TMEM_COLS);
+  }
   if (tid == 0 && *abort_flag) set_status(dev_status, GDN_DEV_WAIT_TIMEOUT);
 }
 
@@ -943,7 +1031,7 @@ cudaError_t launch_k(const gdn_host::ChunkArgs &a, cudaStream_t s) {
   // With no tokens every sequence is empty: the walk only copies states and
   // never touches the (then unused) maps.
   if (rows > 0 && (!make_map(&mq, a.q, K, a.H, rows, 64, true) || !make_map(&mk, a.k, K, a.H, rows, 64, true) ||
-                   !make_map(&mv, a.v, a.V, a.HV, rows, VT, false)))
+                   !make_map(&mv, a.v, a.V, a.HV, rows, 64, true)))
     return cudaErrorInvalidValue;
   const int64_t slots = total_chunk_slots(a.B, a.T, a.N, a.cu != nullptr);
   if (rows > 0 && slots > 0) {
@@ -960,7 +1048,7 @@ cudaError_t launch_k(const gdn_host::ChunkArgs &a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(chunk_walk_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, wsmem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.V / VT, a.HV, a.N);
-  chunk_walk_kernel<K><<<grid, WNTH, wsmem, s>>>(mq, mk, mv, a.scale, a.h0, a.cu, a.T, a.H, a.HV, a.V,
+  chunk_walk_kernel<K><<<grid, WALK_THREADS, wsmem, s>>>(mq, mk, mv, a.scale, a.h0, a.cu, a.T, a.H, a.HV, a.V,
                                                 static_cast<const unsigned char *>(a.ws), a.o, a.ht, a.dev_status);
   return cudaGetLastError();
 }
