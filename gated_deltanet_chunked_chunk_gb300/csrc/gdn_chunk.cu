@@ -536,20 +536,21 @@ __global__ void __launch_bounds__(NTH, 2) chunk_prep_kernel(
 // ============================================================== walk kernel
 // Nine warps.  Every product runs on tcgen05 with fp32 accumulators in TMEM.
 // A thread needs about 100 cycles to issue one tcgen05.mma while issues from
-// different warps overlap, and every hand-off through an mbarrier costs far
-// more while the tensor core and TMA keep shared memory busy; so the compute
-// warps issue all products themselves, each split over two warps into two
-// partial accumulators that the epilogues add up.
+// different warps overlap, and every wait on an mbarrier costs several hundred
+// cycles while the tensor core and TMA keep shared memory busy; so the compute
+// warps issue all products themselves (the serial ones split over several
+// warps into partial accumulators that the epilogues add up), and completions
+// that are always needed together share one barrier.
 //  * Compute warps 0-7: thread (lane group w & 3, column half w >> 2) owns TMEM
 //    lane r = 32 (w & 3) + lane and 16 of the slice's 32 columns, and holds the
 //    fp32 state h[r][16 columns] in registers.  Per chunk c:
-//      [W; Q] [h_hi | h_lo] -> ACC1 (warps 0-1);
-//      meanwhile the output of chunk c - 1 from ACC3 and the staged Q h;
+//      [W; Q] [h_hi | h_lo] -> ACC1 (4 partials, warps 0-3) and
+//      u(c) = Ts V -> ACC4 (warp 6);
+//      meanwhile the output of chunk c - 1 from ACC3 and Q h;
 //      lanes 0-63: v_new = beta v + u - W h -> s v_new, v_new (bf16 hi | lo);
-//      lanes 64-127: e^gamma rq (Q h) -> QH, kept for the output;
-//      then K^T [s v_new hi | lo] -> ACC2 (warps 0-1),
-//      [P_hi; P_lo] [v_new hi | lo] -> ACC3 (warps 2-3) and
-//      u(c + 1) = Ts V -> ACC4 (warps 6-7);
+//      lanes 64-127: e^gamma rq (Q h), kept in registers for the output;
+//      then K^T [s v_new hi | lo] -> ACC2 (2 partials, warps 0-1),
+//      [P_hi; P_lo] [v_new hi | lo] -> ACC3 (warp 2);
 //      h <- e^{gamma_L} h + ACC2, written back as [h_hi | h_lo].
 //  * Warp 8: TMA / bulk loads of chunk c + 2 into the stage chunk c released.
 template <int K>
@@ -568,14 +569,13 @@ struct WalkLay {
   static constexpr int OFF_Z = OFF_VN + 8192;            // 8 KB of zeros: missing rows 64-127 of an M = 128 operand
   static constexpr int XROW = 36;
   static constexpr int OFF_X = OFF_Z + 8192;             // fp32 [64][XROW]: P_hi v_new of the output
-  static constexpr int OFF_QH = OFF_X + 64 * XROW * 4;   // fp32 [64][XROW]: e^gamma rq Q h
-  static constexpr int OFF_BAR = OFF_QH + 64 * XROW * 4;
+  static constexpr int OFF_BAR = OFF_X + 64 * XROW * 4;
   static constexpr int NBAR = 12;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr uint32_t TX = STAGE;                  // every byte of a stage is loaded per chunk
-  // TMEM columns: two partials of 64 each for ACC1, ACC2, ACC3 and ACC4.
-  static constexpr uint32_t ACC1 = 0, ACC2 = 128, ACC3 = 256, ACC4 = 384;
+  // TMEM columns: ACC1 four partials of 64, ACC2 two, ACC3 and ACC4 one each.
+  static constexpr uint32_t ACC1 = 0, ACC2 = 256, ACC3 = 384, ACC4 = 448;
   static constexpr uint32_t TMEM_COLS = 512;
   static_assert(STAGE % 1024 == 0 && OFF_H % 1024 == 0 && OFF_VS % 1024 == 0 && OFF_Z % 1024 == 0,
                 "swizzled tile alignment");
@@ -614,24 +614,29 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
   const int64_t cb = chunk_base(cu, n, T);
   uint32_t *misc = reinterpret_cast<uint32_t *>(sm + Ly::OFF_MISC);
   volatile uint32_t *abort_flag = misc + 1;
-  // Two-slot barriers, slot c & 1 serving chunk c: FULL (loads landed),
-  // UREADY (ACC4 holds u), CDONE (the compute warps and their first two
-  // products are done with the stage), M3 (the output product is done); then
-  // the completions of the first and second products.
-  enum { FULL = 0, UREADY = 1, CDONE = 2, M3 = 3 };
+  // Two-slot barriers, slot c & 1 serving chunk c:
+  //   FULL(c):  the loads of chunk c landed and the output product of chunk
+  //             c - 1 is done (producer arrive with the byte count, plus the
+  //             output product's commit; thread 0 stands in for the missing
+  //             chunk -1, and for chunk NC after the loop);
+  //   CDONE(c): the compute warps and the first two products of chunk c no
+  //             longer read the stage.
+  // Single-slot: M1 (phase c: u(c) and the four parts of [W; Q] h of chunk c
+  // are done) and M2 (phase c: K^T (s v_new) of chunk c is done).
+  enum { FULL = 0, CDONE = 1 };
   auto bar = [&](int kind, int b) { return sb + Ly::OFF_BAR + 8 * (2 * kind + b); };
-  const uint32_t b_m1 = sb + Ly::OFF_BAR + 64, b_m2 = sb + Ly::OFF_BAR + 72;
+  const uint32_t b_m1 = sb + Ly::OFF_BAR + 32, b_m2 = sb + Ly::OFF_BAR + 40, b_drain = sb + Ly::OFF_BAR + 48;
   if (tid == 0) {
     for (int b = 0; b < 2; ++b) {
-      mbar_init(bar(FULL, b), 1);
-      mbar_init(bar(UREADY, b), 2);
+      mbar_init(bar(FULL, b), 2);
       mbar_init(bar(CDONE, b), 1);
-      mbar_init(bar(M3, b), 2);
     }
-    mbar_init(b_m1, 2);
+    mbar_init(b_m1, 5);
     mbar_init(b_m2, 2);
+    mbar_init(b_drain, 5);
     misc[1] = 0;
     mbar_fence_init();
+    mbar_arrive(bar(FULL, 0));  // no output product precedes chunk 0
   }
   for (int e = tid; e < 8192 / 16; e += WALK_THREADS)
     reinterpret_cast<uint4 *>(sm + Ly::OFF_Z)[e] = make_uint4(0, 0, 0, 0);
@@ -649,7 +654,7 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
     uint32_t ok = 0;
     if (lane == 0) {
       ok = !*abort_flag;
-      if (ok && !mbar_spin_bounded(b, parity, kWaitLimit)) {
+      if (ok && !mbar_wait_bounded(b, parity, kWaitLimit)) {
         *abort_flag = 1;
         ok = 0;
       }
@@ -664,7 +669,6 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
   };
   const int64_t sbase = (static_cast<int64_t>(n) * HV + hv) * K;
   float *X = reinterpret_cast<float *>(sm + Ly::OFF_X);
-  float *QH = reinterpret_cast<float *>(sm + Ly::OFF_QH);
 
   if (warp < 8) {
     // ------------------------------------------------------- compute warps
@@ -672,9 +676,12 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
     const int hs = warp >> 2;                            // column half: columns 16 hs .. 16 hs + 15
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
     const bool krow = r < K;
-    float hr[16];
+    float hr[16], qh[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) hr[j] = (h0 && krow) ? h0[(sbase + r) * V + vt0 + 16 * hs + j] : 0.f;
+    for (int j = 0; j < 16; ++j) {
+      hr[j] = (h0 && krow) ? h0[(sbase + r) * V + vt0 + 16 * hs + j] : 0.f;
+      qh[j] = 0.f;
+    }
     // Row r of h -> columns [16 hs, 16 hs + 16) of the hi and lo halves of the
     // MN-major SW128 H tile.
     auto write_h = [&]() {
@@ -714,31 +721,32 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
       }
     };
     // Output of chunk c, from ACC3 (P_hi rows in lanes 0-63, P_lo rows in
-    // lanes 64-127; two partials) and the staged e^gamma rq Q h.
+    // lanes 64-127) and the e^gamma rq Q h that lanes 64-127 hold; the caller
+    // has seen the output product complete.
     auto output = [&](int c, bool go) {
-      go = waitc(M3, c) && go;
       if (go && r < 64) {
         tc_fence_after();
-        float pv[16];
-        sum_partials(Ly::ACC3, 2, pv);
+        uint32_t a[16], b[16];
+        tmem_ld16_issue(tl + Ly::ACC3 + 16 * hs, a);
+        tmem_ld16_issue(tl + Ly::ACC3 + 32 + 16 * hs, b);
+        tmem_ld_wait16(a);
+        tmem_ld_wait16(b);
         float *x = X + r * XROW + 16 * hs;
 #pragma unroll
-        for (int j = 0; j < 16; j += 4) *reinterpret_cast<float4 *>(x + j) = make_float4(pv[j], pv[j + 1], pv[j + 2], pv[j + 3]);
+        for (int j = 0; j < 16; j += 4)
+          *reinterpret_cast<float4 *>(x + j) =
+              make_float4(__uint_as_float(a[j]) + __uint_as_float(b[j]), __uint_as_float(a[j + 1]) + __uint_as_float(b[j + 1]),
+                          __uint_as_float(a[j + 2]) + __uint_as_float(b[j + 2]), __uint_as_float(a[j + 3]) + __uint_as_float(b[j + 3]));
       }
       named_bar_sync(1, WALK_COMPUTE);
       if (go && r >= 64) {
         tc_fence_after();
         const int i = r - 64;
-        uint32_t a[16], b[16];
+        uint32_t a[16];
         tmem_ld16_issue(tl + Ly::ACC3 + 16 * hs, a);
-        tmem_ld16_issue(tl + Ly::ACC3 + 64 + 16 * hs, b);
         tmem_ld_wait16(a);
-        tmem_ld_wait16(b);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) a[j] = __float_as_uint(__uint_as_float(a[j]) + __uint_as_float(b[j]));
         if (i < chunk_rows(c)) {
           const float *x = X + i * XROW + 16 * hs;
-          const float *qh = QH + i * XROW + 16 * hs;
           const int64_t trow = tok0 + static_cast<int64_t>(c) * C + i;
           uint4 *dst = reinterpret_cast<uint4 *>(o + (trow * HV + hv) * V + vt0 + 16 * hs);
 #pragma unroll
@@ -756,72 +764,61 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
       }
       return go;
     };
-    // u(c) = Ts V, k-steps 2q, 2q + 1 into partial q of ACC4; Ts^T is the
+    // u(c) = Ts V into ACC4, completing on phase c of M1; Ts^T is the
     // MN-major A operand whose rows 64-127 come from the zero block.
-    auto issue_u = [&](int c, int q) {
+    auto issue_u = [&](int c) {
       const int s = c % NS;
       const uint32_t st = sb + s * Ly::STAGE;
       tc_fence_after();
       constexpr uint32_t id4 = umma_idesc_bf16(128, 64, 1, 1);
       const uint32_t lbo = static_cast<uint32_t>(Ly::OFF_Z - s * Ly::STAGE - TSO);
 #pragma unroll
-      for (int m = 0; m < 2; ++m) {
-        const int kk = 2 * q + m;
+      for (int kk = 0; kk < 4; ++kk) {
         const uint64_t a = umma_desc_sw128_mn(st + TSO + kk * 2048, lbo);
         const uint64_t b = umma_desc_sw128_mn(st + Ly::VB + kk * 2048, 8192);
-        umma_bf16(tmem + Ly::ACC4 + 64 * q, a, b, id4, m > 0 ? 1u : 0u);
+        umma_bf16(tmem + Ly::ACC4, a, b, id4, kk > 0 ? 1u : 0u);
       }
-      umma_commit(bar(UREADY, c & 1));
+      umma_commit(b_m1);
     };
     write_h();
     fence_proxy_async_smem();
     named_bar_sync(1, WALK_COMPUTE);
-    int n1 = 0, n2 = 0, n3 = 0, n4 = 0;  // products issued by this thread
-    if ((warp == 6 || warp == 7) && NC > 0) {
-      if (waitc(FULL, 0) && lane == 0) {
-        issue_u(0, warp - 6);
-        ++n4;
-      }
-      __syncwarp();
-    }
     bool go = true;
     for (int c = 0; c < NC; ++c) {
       const int s = c % NS;
       const uint32_t st = sb + s * Ly::STAGE;
       const unsigned char *stp = sm + s * Ly::STAGE;
       const float *rsc = reinterpret_cast<const float *>(stp + SCO);
-      go = waitc(FULL, c) && go;
-      // [W; Q] [h_hi | h_lo]: warp p < 2 takes k-steps [p K / 32, p K / 32 + K / 32).
-      if (warp < 2 && lane == 0 && go) {
+      go = waitc(FULL, c) && go;  // also: the output product of chunk c - 1 is done
+      // [W; Q] [h_hi | h_lo]: warp p < 4 takes k-steps [p KA, p KA + KA).
+      if (warp < 4 && lane == 0 && go) {
         tc_fence_after();
         constexpr uint32_t id1 = umma_idesc_bf16(128, 64, 0, 1);
 #pragma unroll
-        for (int m = 0; m < K / 32; ++m) {
-          const int kk = warp * (K / 32) + m;
+        for (int m = 0; m < KA; ++m) {
+          const int kk = warp * KA + m;
           const uint64_t a = umma_desc_sw128(st + Ly::WQ + (kk >> 2) * 16384 + (kk & 3) * 32);
           const uint64_t b = umma_desc_sw128_mn(sb + Ly::OFF_H + kk * 2048, 8192);
           umma_bf16(tmem + Ly::ACC1 + 64 * warp, a, b, id1, m > 0 ? 1u : 0u);
         }
         umma_commit(b_m1);
-        ++n1;
+      } else if (warp == 6 && lane == 0 && go) {
+        issue_u(c);  // ACC4 was last read for chunk c - 1, before its barrier F
       }
       __syncwarp();
-      // Output of the previous chunk while this product runs.
+      // Output of the previous chunk while these products run.
       if (c >= 1) go = output(c - 1, go);
-      go = waitb(b_m1, c & 1) && go;
-      go = waitc(UREADY, c) && go;
+      go = waitb(b_m1, c & 1) && go;  // [W; Q] h and u of this chunk
       const float dL = go ? rsc[RS_DL] : 0.f;
       if (go) {
         tc_fence_after();
         float wh[16];
-        sum_partials(Ly::ACC1, 2, wh);
+        sum_partials(Ly::ACC1, 4, wh);
         if (r < 64) {
           // v_new = beta v + u - W (h_hi + h_lo); s v_new and v_new as bf16 hi | lo.
           const int i = r;
           uint32_t u[16];
-          uint32_t u2[16];
           tmem_ld16_issue(tl + Ly::ACC4 + vhalf + 16 * hs, u);
-          tmem_ld16_issue(tl + Ly::ACC4 + 64 + vhalf + 16 * hs, u2);
           const float bt = rsc[RS_BET + i], sv = rsc[RS_SV + i];
           const int vc = (vhalf + 16 * hs) >> 3;
           uint4 vv[2];
@@ -829,9 +826,6 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
           for (int m = 0; m < 2; ++m)
             vv[m] = *reinterpret_cast<const uint4 *>(stp + Ly::VB + i * 128 + (((vc + m) ^ (i & 7)) << 4));
           tmem_ld_wait16(u);
-          tmem_ld_wait16(u2);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) u[j] = __float_as_uint(__uint_as_float(u[j]) + __uint_as_float(u2[j]));
           unsigned char *vsr = sm + Ly::OFF_VS + (i >> 3) * 1024 + (i & 7) * 128;
           unsigned char *vnr = sm + Ly::OFF_VN + (i >> 3) * 1024 + (i & 7) * 128;
 #pragma unroll
@@ -856,12 +850,9 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
             *reinterpret_cast<uint4 *>(vnr + (((4 + chh) ^ (i & 7)) << 4)) = make_uint4(xl[0], xl[1], xl[2], xl[3]);
           }
         } else {
-          const int i = r - 64;
-          const float og = rsc[RS_OG + i];
-          float *q = QH + i * XROW + 16 * hs;
+          const float og = rsc[RS_OG + r - 64];
 #pragma unroll
-          for (int j = 0; j < 16; j += 4)
-            *reinterpret_cast<float4 *>(q + j) = make_float4(og * wh[j], og * wh[j + 1], og * wh[j + 2], og * wh[j + 3]);
+          for (int j = 0; j < 16; ++j) qh[j] = og * wh[j];
         }
       }
       tc_fence_before();
@@ -881,33 +872,19 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
           umma_bf16(tmem + Ly::ACC2 + 64 * warp, a, b, id2, m > 0 ? 1u : 0u);
         }
         umma_commit(b_m2);
-        ++n2;
-      } else if ((warp == 2 || warp == 3) && lane == 0 && go) {
-        // [P_hi; P_lo] [v_new hi | lo]: warp 2 + q takes k-steps 2q, 2q + 1.
+      } else if (warp == 2 && lane == 0 && go) {
+        // [P_hi; P_lo] [v_new hi | lo], completing on FULL(c + 1).
         tc_fence_after();
-        const int q = warp - 2;
         constexpr uint32_t id3 = umma_idesc_bf16(128, 64, 0, 1);
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {
-          const int kk = 2 * q + m;
+        for (int kk = 0; kk < 4; ++kk) {
           const uint64_t a = umma_desc_sw128(st + Ly::RR + kk * 32);
           const uint64_t b = umma_desc_sw128_mn(sb + Ly::OFF_VN + kk * 2048, 8192);
-          umma_bf16(tmem + Ly::ACC3 + 64 * q, a, b, id3, m > 0 ? 1u : 0u);
+          umma_bf16(tmem + Ly::ACC3, a, b, id3, kk > 0 ? 1u : 0u);
         }
-        umma_commit(bar(M3, c & 1));
-        ++n3;
+        umma_commit(bar(FULL, (c + 1) & 1));
       }
       __syncwarp();
-      if ((warp == 6 || warp == 7) && c + 1 < NC) {
-        // u(c + 1) = Ts V: warp 6 + q takes k-steps 2q, 2q + 1.  ACC4 was read
-        // for chunk c before the barrier above.
-        const bool g2 = waitc(FULL, c + 1) && go;
-        if (g2 && lane == 0) {
-          issue_u(c + 1, warp - 6);
-          ++n4;
-        }
-        __syncwarp();
-      }
       go = waitb(b_m2, c & 1) && go;
       if (tid == 0 && go) mbar_arrive(bar(CDONE, c & 1));  // nothing of this stage is read any more
       if (go) {
@@ -922,13 +899,21 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
       fence_proxy_async_smem();
       named_bar_sync(1, WALK_COMPUTE);
     }
-    if (NC > 0) go = output(NC - 1, go);
+    if (NC > 0) {
+      // The output product of the last chunk completes on FULL(NC), which no
+      // load feeds: thread 0 stands in for the producer.
+      if (tid == 0) mbar_arrive(bar(FULL, NC & 1));
+      go = waitc(FULL, NC) && go;
+      go = output(NC - 1, go);
+    }
     if (lane == 0 && *abort_flag) {
-      // After an abort a product may still be in flight: wait for the last of each.
-      if (n1 > 0) mbar_wait_bounded(b_m1, (n1 - 1) & 1, kWaitLimit);
-      if (n2 > 0) mbar_wait_bounded(b_m2, (n2 - 1) & 1, kWaitLimit);
-      if (n3 > 0) mbar_wait_bounded(bar(M3, (n3 - 1) & 1), ((n3 - 1) >> 1) & 1, kWaitLimit);
-      if (n4 > 0) mbar_wait_bounded(bar(UREADY, (n4 - 1) & 1), ((n4 - 1) >> 1) & 1, kWaitLimit);
+      // After an abort products may still be in flight: one more commit by
+      // each issuing thread completes once all of that thread's products have.
+      if (warp < 4 || warp == 6) {
+        tc_fence_after();
+        umma_commit(b_drain);
+        mbar_wait_bounded(b_drain, 0, kWaitLimit);
+      }
     }
     if (ht && krow && !*abort_flag) {
 #pragma unroll
@@ -960,7 +945,7 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
     __syncwarp();
     for (int c = 0; c + NS < NC; ++c) {
       bool can = waitc(CDONE, c);
-      can = waitc(M3, c) && can;
+      can = waitc(FULL, c + 1) && can;  // includes: the output product of chunk c read P hi / lo
       if (can && lane == 0) issue(c + NS);
       __syncwarp();
     }
