@@ -155,8 +155,7 @@ __device__ __forceinline__ int64_t chunk_base(const int32_t *cu, int n, int T) {
 template <int K>
 struct PrepLay {
   static constexpr int OFF_KQ = 0;                              // [K;Q] tile
-  static constexpr int OFF_REC = KQ<K>::BYTES;                  // record image
-  static constexpr int OFF_AT = OFF_REC + Rec<K>::BYTES;        // A then T, fp32 [64][FROW], in place
+  static constexpr int OFF_AT = KQ<K>::BYTES;                   // A then T, fp32 [64][FROW], in place
   static constexpr int OFF_TP = OFF_AT + 64 * FROW * 4;         // T diag(beta e^g rk), bf16 SW128
   static constexpr int OFF_X = OFF_TP + 8192;                   // 4 x [16][17] fp32
   static constexpr int OFF_SC = OFF_X + 4352;                   // gl, bet, rk, rq, rowA, rowP, colf, ftp
@@ -168,7 +167,7 @@ struct PrepLay {
 enum { PS_GL = 0, PS_BET = 1, PS_RK = 2, PS_RQ = 3, PS_RA = 4, PS_RP = 5, PS_CF = 6, PS_FTP = 7 };
 
 template <int K>
-__global__ void __launch_bounds__(NTH, 2) chunk_prep_kernel(
+__global__ void __launch_bounds__(NTH, 3) chunk_prep_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k, const float *__restrict__ g,
     const float *__restrict__ beta, const int32_t *__restrict__ cu, int N, int T, int H, int HV, int l2,
     unsigned char *__restrict__ ws, int32_t *dev_status) {
@@ -214,7 +213,9 @@ __global__ void __launch_bounds__(NTH, 2) chunk_prep_kernel(
   float *rowA = scal + PS_RA * 64, *rowP = scal + PS_RP * 64, *colf = scal + PS_CF * 64, *ftp = scal + PS_FTP * 64;
   float *AT = reinterpret_cast<float *>(sm + Ly::OFF_AT);
   float *Xs = reinterpret_cast<float *>(sm + Ly::OFF_X);
-  unsigned char *rec = sm + Ly::OFF_REC;
+  // The record goes straight to the workspace: every byte the walk reads is
+  // written below (16-byte stores for P, Ts^T; the mma fragments of W).
+  unsigned char *rec = ws + (static_cast<size_t>(gc) * HV + hv) * R::BYTES;
   float *rsc = reinterpret_cast<float *>(rec + R::SC);
   uint32_t *misc = reinterpret_cast<uint32_t *>(sm + Ly::OFF_MISC);
   const uint32_t b_tma = sb + Ly::OFF_BAR, b_mma = sb + Ly::OFF_BAR + 8;
@@ -451,45 +452,50 @@ __global__ void __launch_bounds__(NTH, 2) chunk_prep_kernel(
     __syncthreads();
   }
 
-  // Tp = T diag(beta e^gamma rk) (j <= i, for W) and Ts = (T - I) diag(beta) (j < i), bf16.
+  // Tp = T diag(beta e^gamma rk) (j <= i, for W), bf16 SW128 in shared memory.
   for (int e = tid; e < 64 * 8; e += NTH) {
     const int i = e >> 3, ch = e & 7;
-    uint4 tpv = make_uint4(0, 0, 0, 0), tsv = make_uint4(0, 0, 0, 0);
+    uint4 tpv = make_uint4(0, 0, 0, 0);
     if (8 * ch <= i) {
       const float4 t0 = *reinterpret_cast<const float4 *>(AT + i * FROW + 8 * ch);
       const float4 t1 = *reinterpret_cast<const float4 *>(AT + i * FROW + 8 * ch + 4);
       const float4 f0 = *reinterpret_cast<const float4 *>(ftp + 8 * ch);
       const float4 f1 = *reinterpret_cast<const float4 *>(ftp + 8 * ch + 4);
-      const float4 c0 = *reinterpret_cast<const float4 *>(bet + 8 * ch);
-      const float4 c1 = *reinterpret_cast<const float4 *>(bet + 8 * ch + 4);
       const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
       const float fv[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
-      const float bv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-      uint32_t tp[4], ts[4];
+      uint32_t tp[4];
 #pragma unroll
       for (int q2 = 0; q2 < 4; ++q2) {
-        float a2[2], b2[2];
+        float a2[2];
 #pragma unroll
         for (int u2 = 0; u2 < 2; ++u2) {
           const int jj = 2 * q2 + u2, j = 8 * ch + jj;
           a2[u2] = (j <= i) ? tv[jj] * fv[jj] : 0.f;
-          b2[u2] = (j < i) ? tv[jj] * bv[jj] : 0.f;
         }
         tp[q2] = pack_bf16(a2[0], a2[1]);
-        ts[q2] = pack_bf16(b2[0], b2[1]);
       }
       tpv = make_uint4(tp[0], tp[1], tp[2], tp[3]);
-      tsv = make_uint4(ts[0], ts[1], ts[2], ts[3]);
     }
     *reinterpret_cast<uint4 *>(sm + Ly::OFF_TP + sw128(i, ch)) = tpv;
-    // Ts goes out transposed (row j holds column j of Ts), the MN-major A
-    // operand of the walk's u = Ts V product.
-    const uint32_t tsw[4] = {tsv.x, tsv.y, tsv.z, tsv.w};
+  }
+  // Ts = (T - I) diag(beta) (j < i), written transposed (row j holds column j
+  // of Ts): the MN-major A operand of the walk's u = Ts V product.  A warp
+  // takes 32 consecutive columns j, so its reads of T hit distinct banks.
+  for (int e = tid; e < 64 * 8; e += NTH) {
+    const int j = e & 63, ich = e >> 6;
+    const float bj = bet[j];
+    uint32_t w[4];
 #pragma unroll
-    for (int jj = 0; jj < 8; ++jj) {
-      const uint16_t x = static_cast<uint16_t>((jj & 1) ? (tsw[jj >> 1] >> 16) : (tsw[jj >> 1] & 0xFFFFu));
-      *reinterpret_cast<uint16_t *>(rec + R::TS + sw128(8 * ch + jj, i >> 3) + (i & 7) * 2) = x;
+    for (int q2 = 0; q2 < 4; ++q2) {
+      float v2[2];
+#pragma unroll
+      for (int u2 = 0; u2 < 2; ++u2) {
+        const int i = 8 * ich + 2 * q2 + u2;
+        v2[u2] = (j < i) ? AT[i * FROW + j] * bj : 0.f;
+      }
+      w[q2] = pack_bf16(v2[0], v2[1]);
     }
+    *reinterpret_cast<uint4 *>(rec + R::TS + sw128(j, ich)) = make_uint4(w[0], w[1], w[2], w[3]);
   }
   __syncthreads();
 
@@ -525,12 +531,6 @@ __global__ void __launch_bounds__(NTH, 2) chunk_prep_kernel(
       *reinterpret_cast<uint32_t *>(base + sw128(r0 + 8, (key & 63) >> 3)) = pack_bf16(acc[j][2], acc[j][3]);
     }
   }
-  __syncthreads();
-
-  // Record -> workspace (16-byte coalesced stores).
-  uint4 *dst = reinterpret_cast<uint4 *>(ws + (static_cast<size_t>(gc) * HV + hv) * R::BYTES);
-  const uint4 *src = reinterpret_cast<const uint4 *>(rec);
-  for (int e = tid; e < R::BYTES / 16; e += NTH) dst[e] = src[e];
 }
 
 // ============================================================== walk kernel
@@ -648,19 +648,21 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
   const uint32_t tmem = misc[0];
 
   // Bounded wait; lane 0 polls and the result is warp-uniform.  After an
-  // expired wait every later wait returns false at once: loops run to their
-  // end without work but still pass every named barrier.
+  // expired wait every later wait of this warp returns false at once (loops
+  // run to their end without work but still pass every named barrier); other
+  // warps see their own waits expire.  The shared flag only records the abort
+  // (reading it on every wait would queue behind the TMA traffic).
+  bool dead = false;
   auto waitb = [&](uint32_t b, uint32_t parity) -> bool {
     uint32_t ok = 0;
-    if (lane == 0) {
-      ok = !*abort_flag;
-      if (ok && !mbar_wait_bounded(b, parity, kWaitLimit)) {
-        *abort_flag = 1;
-        ok = 0;
-      }
+    if (lane == 0 && !dead) {
+      ok = mbar_wait_bounded(b, parity, kWaitLimit) ? 1u : 0u;
+      if (!ok) *abort_flag = 1;
     }
     __syncwarp();
-    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    dead = dead || !ok;
+    return ok != 0;
   };
   auto waitc = [&](int kind, int c) { return waitb(bar(kind, c & 1), (c >> 1) & 1); };
   auto chunk_rows = [&](int c) {
