@@ -204,3 +204,86 @@ def config4() -> DecodeCase:
 
 
 CONFIGS = {0: config0, 1: config1, 2: config2, 3: config3, 4: config4}
+
+
+# ---------------------------------------------------------------- causal conv1d
+# Shapes follow the FastDeploy PR's Usage sections 3 and 4 (x channel-first
+# [dim, total] for prefill, token-major [batch, dim] for decode, a conv-state
+# pool [slots, dim, state_len]) with dim = 2 H K + HV V, the packed q | k | v
+# channels of the LightLLM "gdn.py" backends, and width 4.  Draws: x ~ N(0, 1),
+# weight ~ U(-0.5, 0.5), bias ~ N(0, 0.1^2), states ~ N(0, 1), all bf16.
+
+
+@dataclasses.dataclass
+class ConvPrefillCase:
+    name: str
+    x: torch.Tensor                # [dim, total] bf16
+    weight: torch.Tensor           # [dim, W] bf16
+    bias: torch.Tensor             # [dim] bf16
+    conv_states: torch.Tensor      # [P, dim, S] bf16
+    query_start_loc: torch.Tensor  # [N + 1] int32
+    cache_indices: torch.Tensor    # [N] int32 (-1 = no slot)
+    has_initial_state: torch.Tensor  # [N] bool
+
+
+@dataclasses.dataclass
+class ConvDecodeCase:
+    name: str
+    x: torch.Tensor                # [R, dim] bf16
+    weight: torch.Tensor           # [dim, W] bf16
+    bias: torch.Tensor             # [dim] bf16
+    conv_state: torch.Tensor       # [P, dim, S] bf16
+    indices: torch.Tensor          # [R] int32 (-1 = PAD)
+
+
+def _uniform(shape, gen, lo, hi):
+    return (torch.rand(shape, generator=gen) * (hi - lo) + lo).to(torch.bfloat16)
+
+
+def conv_prefill_case(name: str, seed: int, dim: int, lengths, W: int = 4, S: int = 3, P: Optional[int] = None,
+                      init_every: int = 2, pad_slot_every: int = 0) -> ConvPrefillCase:
+    """Packed sequences of the given lengths.  Sequence n uses slot P - 1 - n
+    (so slots are not the identity); every ``init_every``-th sequence starts
+    from its slot's state; with ``pad_slot_every`` > 0 every such sequence has
+    slot -1."""
+    gen = _gen(seed)
+    N = len(lengths)
+    P = P if P is not None else N + 2
+    total = int(sum(lengths))
+    x = _normal((dim, total), gen)
+    weight = _uniform((dim, W), gen, -0.5, 0.5)
+    bias = _normal((dim,), gen, std=0.1)
+    states = _normal((P, dim, S), gen)
+    qsl = torch.tensor(cu_from_lengths(lengths), dtype=torch.int32)
+    slots = torch.tensor([P - 1 - n for n in range(N)], dtype=torch.int32)
+    if pad_slot_every:
+        for n in range(0, N, pad_slot_every):
+            slots[n] = -1
+    init = torch.tensor([(n % init_every) == 0 for n in range(N)], dtype=torch.bool)
+    return ConvPrefillCase(name, x, weight, bias, states, qsl, slots, init)
+
+
+def conv_decode_case(name: str, seed: int, R: int, P: int, dim: int, W: int = 4, S: int = 3,
+                     pad_prob: float = 0.1) -> ConvDecodeCase:
+    """R one-token requests; slots are the first R entries of a permutation of
+    the P slots, each replaced by -1 (PAD) with probability ``pad_prob``."""
+    gen = _gen(seed)
+    x = _normal((R, dim), gen)
+    weight = _uniform((dim, W), gen, -0.5, 0.5)
+    bias = _normal((dim,), gen, std=0.1)
+    states = _normal((P, dim, S), gen)
+    perm = torch.randperm(P, generator=gen)[:R].to(torch.int32)
+    pad = torch.rand(R, generator=gen) < pad_prob
+    idx = torch.where(pad, torch.full_like(perm, -1), perm)
+    return ConvDecodeCase(name, x, weight, bias, states, idx)
+
+
+def conv_prefill_long() -> ConvPrefillCase:
+    """The long-context prefill's conv: dim = 2*16*128 + 32*128 = 8192 channels,
+    one 65536-token sequence with an initial state; seed 13."""
+    return conv_prefill_case("conv_prefill_T65536_dim8192", 13, 8192, [65536], init_every=1, P=4)
+
+
+def conv_decode_r256() -> ConvDecodeCase:
+    """The batched decode's conv: 256 requests, 512 slots, dim 8192; seed 14."""
+    return conv_decode_case("conv_decode_R256_P512_dim8192", 14, 256, 512, 8192)
