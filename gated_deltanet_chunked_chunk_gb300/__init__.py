@@ -22,7 +22,8 @@ from typing import Optional, Tuple
 import torch
 
 __all__ = ["gdn_gating", "gdn_chunk_fwd", "gdn_recurrent_decode", "chunk_fwd_workspace_size",
-           "gdn_chunk_fwd_noalloc", "NOALLOC_SCRATCH_BYTES",
+           "gdn_chunk_fwd_noalloc", "NOALLOC_SCRATCH_BYTES", "gdn_causal_conv1d_fwd",
+           "gdn_causal_conv1d_update", "gdn_conv_decode_pack",
            "GDNError", "lib_path", "load_library", "status_string", "DEV_BAD_CU_SEQLENS",
            "DEV_BAD_SLOT", "DEV_WAIT_TIMEOUT", "EXPORTED_SYMBOLS"]
 
@@ -36,7 +37,8 @@ DEV_BAD_CU_SEQLENS, DEV_BAD_SLOT, DEV_WAIT_TIMEOUT = 1, 2, 4
 
 #: Every symbol include/gdn.h declares (checked by the tests).
 EXPORTED_SYMBOLS = ("gdn_status_string", "gdn_version", "gdn_gating", "gdn_chunk_fwd_workspace_size",
-                    "gdn_chunk_fwd", "gdn_recurrent_decode", "gdn_chunk_fwd_noalloc")
+                    "gdn_chunk_fwd", "gdn_recurrent_decode", "gdn_chunk_fwd_noalloc",
+                    "gdn_causal_conv1d_fwd", "gdn_causal_conv1d_update", "gdn_conv_decode_pack")
 
 #: Size of the fixed scratch buffer behind gdn_chunk_fwd_noalloc (bytes).
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -78,6 +80,12 @@ def load_library():
         lib.gdn_recurrent_decode.restype = I
         lib.gdn_chunk_fwd_noalloc.argtypes = [P, P, P, P, P, F, P, P, I, I, I, I, I, I, I, I, P, P, P, P]
         lib.gdn_chunk_fwd_noalloc.restype = I
+        lib.gdn_causal_conv1d_fwd.argtypes = [P, P, P, P, I, I, P, P, P, I, I, I64, I, I, P, P, P]
+        lib.gdn_causal_conv1d_fwd.restype = I
+        lib.gdn_causal_conv1d_update.argtypes = [P, P, I, I, P, P, P, I, I, I, I, P, P, P]
+        lib.gdn_causal_conv1d_update.restype = I
+        lib.gdn_conv_decode_pack.argtypes = [P, P, I, I, P, P, P, I, I, I, I, I, I, I, P, P, P, P, P]
+        lib.gdn_conv_decode_pack.restype = I
         _lib = lib
         return lib
 
@@ -301,3 +309,96 @@ def gdn_recurrent_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
 # Short aliases mirroring the pages' Python names.
 chunk_gated_delta_rule = gdn_chunk_fwd
 fused_gdn_gating = gdn_gating
+
+
+# ------------------------------------------------------------------ conv1d
+_ACT = {None: 0, "none": 0, "silu": 1, "swish": 1}
+
+
+def _act_code(activation) -> int:
+    if activation not in _ACT:
+        raise ValueError(f"activation must be None or 'silu', got {activation!r}")
+    return _ACT[activation]
+
+
+def gdn_causal_conv1d_fwd(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor],
+                          conv_states: Optional[torch.Tensor], query_start_loc: torch.Tensor,
+                          cache_indices: Optional[torch.Tensor] = None,
+                          has_initial_state: Optional[torch.Tensor] = None, activation="silu",
+                          out: Optional[torch.Tensor] = None, dev_status: Optional[torch.Tensor] = None):
+    """Packed causal conv1d prefill; see ``gdn_causal_conv1d_fwd`` in include/gdn.h.
+
+    x [dim, total] bf16 (channel-first), weight [dim, W], bias [dim] or None,
+    conv_states [P, dim, S] (updated in place), query_start_loc int32 [N + 1],
+    cache_indices int32 [N], has_initial_state bool [N].  Returns out [dim, total].
+    """
+    dev = x.device
+    _check(x, "x", torch.bfloat16, dev, 2)
+    _check(weight, "weight", torch.bfloat16, dev, 2)
+    _check(bias, "bias", torch.bfloat16, dev, 1)
+    _check(conv_states, "conv_states", torch.bfloat16, dev, 3)
+    _check(query_start_loc, "query_start_loc", torch.int32, dev, 1)
+    _check(cache_indices, "cache_indices", torch.int32, dev, 1)
+    if has_initial_state is not None:
+        _check(has_initial_state, "has_initial_state", torch.bool, dev, 1)
+    dim, total = x.shape
+    W = weight.shape[1]
+    P, S = (conv_states.shape[0], conv_states.shape[2]) if conv_states is not None else (0, max(W - 1, 1))
+    N = query_start_loc.shape[0] - 1
+    if out is None:
+        out = torch.empty_like(x)
+    rc = load_library().gdn_causal_conv1d_fwd(
+        _ptr(x), _ptr(weight), _ptr(bias), _ptr(conv_states), P, S, _ptr(query_start_loc),
+        _ptr(cache_indices), _ptr(has_initial_state), N, dim, total, W, _act_code(activation), _ptr(out),
+        _ptr(dev_status), _stream(dev))
+    if rc != GDN_OK:
+        raise GDNError("gdn_causal_conv1d_fwd", rc)
+    return out
+
+
+def gdn_causal_conv1d_update(x: torch.Tensor, conv_state: torch.Tensor, weight: torch.Tensor,
+                             bias: Optional[torch.Tensor], conv_state_indices: torch.Tensor, activation="silu",
+                             out: Optional[torch.Tensor] = None, dev_status: Optional[torch.Tensor] = None):
+    """One-token conv against the state pool; see include/gdn.h.  x [R, dim] bf16,
+    conv_state [P, dim, S] (in place), conv_state_indices int32 [R] (-1 = PAD).
+    Returns out [R, dim]."""
+    dev = x.device
+    _check(x, "x", torch.bfloat16, dev, 2)
+    _check(conv_state, "conv_state", torch.bfloat16, dev, 3)
+    _check(weight, "weight", torch.bfloat16, dev, 2)
+    _check(bias, "bias", torch.bfloat16, dev, 1)
+    _check(conv_state_indices, "conv_state_indices", torch.int32, dev, 1)
+    R, dim = x.shape
+    if out is None:
+        out = torch.empty_like(x)
+    rc = load_library().gdn_causal_conv1d_update(
+        _ptr(x), _ptr(conv_state), conv_state.shape[0], conv_state.shape[2], _ptr(weight), _ptr(bias),
+        _ptr(conv_state_indices), R, dim, weight.shape[1], _act_code(activation), _ptr(out), _ptr(dev_status),
+        _stream(dev))
+    if rc != GDN_OK:
+        raise GDNError("gdn_causal_conv1d_update", rc)
+    return out
+
+
+def gdn_conv_decode_pack(mixed_qkv: torch.Tensor, conv_state: torch.Tensor, weight: torch.Tensor,
+                         bias: Optional[torch.Tensor], conv_state_indices: torch.Tensor, H: int, HV: int, K: int,
+                         V: int, activation="silu", dev_status: Optional[torch.Tensor] = None):
+    """Decode conv over the packed q | k | v channels, returned split as
+    q, k [R, 1, H, K] and v [R, 1, HV, V] (the inputs gdn_recurrent_decode takes)."""
+    dev = mixed_qkv.device
+    _check(mixed_qkv, "mixed_qkv", torch.bfloat16, dev, 2)
+    _check(conv_state, "conv_state", torch.bfloat16, dev, 3)
+    _check(weight, "weight", torch.bfloat16, dev, 2)
+    _check(bias, "bias", torch.bfloat16, dev, 1)
+    _check(conv_state_indices, "conv_state_indices", torch.int32, dev, 1)
+    R = mixed_qkv.shape[0]
+    q = torch.empty(R, 1, H, K, dtype=torch.bfloat16, device=dev)
+    k = torch.empty(R, 1, H, K, dtype=torch.bfloat16, device=dev)
+    v = torch.empty(R, 1, HV, V, dtype=torch.bfloat16, device=dev)
+    rc = load_library().gdn_conv_decode_pack(
+        _ptr(mixed_qkv), _ptr(conv_state), conv_state.shape[0], conv_state.shape[2], _ptr(weight), _ptr(bias),
+        _ptr(conv_state_indices), R, H, HV, K, V, weight.shape[1], _act_code(activation), _ptr(q), _ptr(k),
+        _ptr(v), _ptr(dev_status), _stream(dev))
+    if rc != GDN_OK:
+        raise GDNError("gdn_conv_decode_pack", rc)
+    return q, k, v

@@ -1,0 +1,233 @@
+// gdn_conv.cu -- causal depthwise conv1d in front of Gated DeltaNet, and its
+// C ABI (gdn_causal_conv1d_fwd, gdn_causal_conv1d_update, gdn_conv_decode_pack).
+//
+// FastDeploy PR "support fla triton kernel for qwen3.5": Modifications table
+// (causal_conv1d.py: causal_conv1d_update for decode against a conv-state pool
+// addressed by slot ids, causal_conv1d_fn for varlen prefill with
+// query_start_loc / has_initial_state) and Usage sections 3 and 4; LightLLM
+// "gdn.py": the prefill backend convolves the packed q | k | v channels, the
+// decode backend fuses the conv with the split into q, k, v.
+//
+// Per channel d, with the input stream history ++ x of a sequence (history =
+// the slot's state, or zeros), out[d, p] = act(bias[d] + sum_j w[d, j] *
+// stream[d, p + j]) where the last tap multiplies the current token; the slot
+// then holds the last S entries of the stream.  act is identity or SiLU.
+//
+// All three ops are memory-bound (a few multiply-adds per element).
+//  * conv_prefill_kernel: x is channel-first [dim, total]; a CTA takes one
+//    channel and 2048 tokens, a warp 32 consecutive tokens per step, so every
+//    tap load is a 64-byte coalesced segment of one row (the W - 1 re-reads of
+//    a token hit L1).  A thread finds its token's sequence by binary search in
+//    query_start_loc.
+//  * conv_state_kernel (same stream, after the prefill kernel, so every read
+//    of the old states precedes the writes): one thread per (sequence,
+//    channel) writes the slot's new last-S inputs.
+//  * conv_update_kernel: x is token-major [R, dim]; one thread per (request,
+//    channel), consecutive threads on consecutive channels; the output goes to
+//    up to three destination arrays split by channel range (the q | k | v
+//    split of the fused decode form).
+#include <math.h>
+
+#include "gdn_common.cuh"
+
+namespace {
+
+constexpr int kConvMaxW = 8;
+constexpr int kConvMaxS = 64;
+constexpr int kPrefillTile = 2048;
+
+__device__ __forceinline__ float conv_act(float x, int act) { return act ? x / (1.f + expf(-x)) : x; }
+
+// Largest n in [0, N] with qsl[n] <= t (qsl non-decreasing), or -1.
+__device__ __forceinline__ int seq_of(const int32_t *qsl, int N, int64_t t) {
+  if (qsl[0] > t) return -1;
+  int lo = 0, hi = N;  // invariant: qsl[lo] <= t
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (qsl[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(256) conv_prefill_kernel(
+    const uint16_t *__restrict__ x, const uint16_t *__restrict__ w, const uint16_t *__restrict__ bias,
+    const uint16_t *__restrict__ states, int P, int S, const int32_t *__restrict__ qsl,
+    const int32_t *__restrict__ cache, const uint8_t *__restrict__ has_init, int N, int dim, int64_t total,
+    int W, int act, uint16_t *__restrict__ out, int32_t *dev_status) {
+  const int d = blockIdx.x;
+  float wf[kConvMaxW];
+#pragma unroll
+  for (int j = 0; j < kConvMaxW; ++j) wf[j] = j < W ? gdn::bf2f(w[(int64_t)d * W + j]) : 0.f;
+  const float b0 = bias ? gdn::bf2f(bias[d]) : 0.f;
+  const uint16_t *xr = x + (int64_t)d * total;
+  uint16_t *orow = out + (int64_t)d * total;
+  const int64_t t_end = min(total, (int64_t)(blockIdx.y + 1) * kPrefillTile);
+  for (int64_t t = (int64_t)blockIdx.y * kPrefillTile + threadIdx.x; t < t_end; t += blockDim.x) {
+    const int n = seq_of(qsl, N, t);
+    if (n < 0 || n >= N) {  // offsets that do not cover this token
+      gdn::set_status(dev_status, GDN_DEV_BAD_CU_SEQLENS);
+      orow[t] = 0;
+      continue;
+    }
+    const int64_t s0 = qsl[n], p = t - s0;
+    if (s0 < 0) {
+      gdn::set_status(dev_status, GDN_DEV_BAD_CU_SEQLENS);
+      orow[t] = 0;
+      continue;
+    }
+    const int slot = cache ? cache[n] : -1;
+    if (slot < -1 || slot >= P) gdn::set_status(dev_status, GDN_DEV_BAD_SLOT);
+    const bool hist = slot >= 0 && slot < P && has_init && has_init[n];
+    const uint16_t *srow = hist ? states + ((int64_t)slot * dim + d) * S : nullptr;
+    float acc = b0;
+#pragma unroll
+    for (int j = 0; j < kConvMaxW; ++j) {
+      if (j < W) {
+        const int64_t src = p - (W - 1) + j;
+        float v = 0.f;
+        if (src >= 0) v = gdn::bf2f(xr[s0 + src]);
+        else if (hist) v = gdn::bf2f(srow[S + src]);
+        acc = fmaf(wf[j], v, acc);
+      }
+    }
+    orow[t] = gdn::f2bf(conv_act(acc, act));
+  }
+}
+
+__global__ void __launch_bounds__(256) conv_state_kernel(
+    const uint16_t *__restrict__ x, uint16_t *__restrict__ states, int P, int S, const int32_t *__restrict__ qsl,
+    const int32_t *__restrict__ cache, const uint8_t *__restrict__ has_init, int N, int dim, int64_t total,
+    int32_t *dev_status) {
+  const int d = blockIdx.x * blockDim.x + threadIdx.x;
+  const int n = blockIdx.y;
+  if (d >= dim) return;
+  const int64_t s0 = qsl[n], s1 = qsl[n + 1];
+  if (s0 < 0 || s1 < s0 || s1 > total || (n == 0 && s0 != 0)) {
+    if (d == 0) gdn::set_status(dev_status, GDN_DEV_BAD_CU_SEQLENS);
+    return;
+  }
+  const int slot = cache ? cache[n] : -1;
+  if (slot < 0 || slot >= P) return;  // no slot (PAD), or a bad one (flagged by the prefill kernel)
+  const bool hist = has_init && has_init[n];
+  uint16_t *srow = states + ((int64_t)slot * dim + d) * S;
+  const int64_t len = s1 - s0;
+  // New state j = stream position len + j of old (S entries, or zeros) ++ x
+  // (len entries).  Going upward, entry len + j of the old row is read before
+  // any write reaches it.
+  for (int j = 0; j < S; ++j) {
+    const int64_t pos = len + j;
+    srow[j] = pos >= S ? x[(int64_t)d * total + s0 + (pos - S)] : (hist ? srow[pos] : (uint16_t)0);
+  }
+}
+
+__global__ void __launch_bounds__(256) conv_update_kernel(
+    const uint16_t *__restrict__ x, uint16_t *__restrict__ states, int P, int S, const uint16_t *__restrict__ w,
+    const uint16_t *__restrict__ bias, const int32_t *__restrict__ idx, int dim, int W, int act,
+    uint16_t *__restrict__ o0, uint16_t *__restrict__ o1, uint16_t *__restrict__ o2, int c1, int c2,
+    int32_t *dev_status) {
+  const int d = blockIdx.x * blockDim.x + threadIdx.x;
+  const int r = blockIdx.y;
+  if (d >= dim) return;
+  uint16_t *dst = d < c1 ? o0 + (int64_t)r * c1 + d
+                : d < c2 ? o1 + (int64_t)r * (c2 - c1) + (d - c1)
+                         : o2 + (int64_t)r * (dim - c2) + (d - c2);
+  const int slot = idx[r];
+  if (slot < 0 || slot >= P) {
+    if (slot != -1 && d == 0) gdn::set_status(dev_status, GDN_DEV_BAD_SLOT);
+    *dst = 0;  // PAD (or a bad slot treated as PAD): zero row, pool untouched
+    return;
+  }
+  uint16_t *srow = states + ((int64_t)slot * dim + d) * S;
+  const uint16_t xv = x[(int64_t)r * dim + d];
+  float acc = bias ? gdn::bf2f(bias[d]) : 0.f;
+#pragma unroll
+  for (int j = 0; j < kConvMaxW; ++j) {
+    if (j < W) {
+      // tap j reads stream position S - (W - 1) + j of history (S) ++ x
+      const int pos = S - (W - 1) + j;
+      const float v = gdn::bf2f(pos < S ? srow[pos] : xv);
+      acc = fmaf(gdn::bf2f(w[(int64_t)d * W + j]), v, acc);
+    }
+  }
+  *dst = gdn::f2bf(conv_act(acc, act));
+  // Shift the row by one (reads run ahead of writes) and append x.
+  for (int j = 0; j + 1 < S; ++j) srow[j] = srow[j + 1];
+  srow[S - 1] = xv;
+}
+
+bool conv_dims_ok(int dim, int W, int S) {
+  return dim > 0 && W >= 1 && W <= kConvMaxW && S >= W - 1 && S >= 1 && S <= kConvMaxS;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ECUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int gdn_causal_conv1d_fwd(const uint16_t *x, const uint16_t *weight, const uint16_t *bias,
+                          uint16_t *conv_states, int P, int state_len, const int32_t *query_start_loc,
+                          const int32_t *cache_indices, const uint8_t *has_initial_state, int N, int dim,
+                          int64_t total, int width, int activation, uint16_t *out, int32_t *dev_status,
+                          void *stream) {
+  if (N < 0 || P < 0 || total < 0 || dim <= 0 || (activation != 0 && activation != 1)) return GDN_EINVAL;
+  if (!conv_dims_ok(dim, width, state_len)) return GDN_EUNSUPPORTED;
+  if (N == 0) return total == 0 ? GDN_OK : GDN_EINVAL;  // tokens need a sequence
+  if (!query_start_loc || !weight) return GDN_EINVAL;
+  if (total > 0 && (!x || !out)) return GDN_EINVAL;
+  if (P > 0 && !conv_states) return GDN_EINVAL;
+  if (cache_indices && !conv_states) return GDN_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (total > 0) {
+    const int64_t tiles = (total + kPrefillTile - 1) / kPrefillTile;
+    if (tiles > 65535) return GDN_EUNSUPPORTED;
+    conv_prefill_kernel<<<dim3(dim, (unsigned)tiles), 256, 0, s>>>(
+        x, weight, bias, conv_states, P, state_len, query_start_loc, cache_indices, has_initial_state, N, dim,
+        total, width, activation, out, dev_status);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return GDN_ECUDA;
+  }
+  if (N > 0 && cache_indices && P > 0) {
+    if (N > 65535) return GDN_EUNSUPPORTED;
+    conv_state_kernel<<<dim3((dim + 255) / 256, N), 256, 0, s>>>(
+        x, conv_states, P, state_len, query_start_loc, cache_indices, has_initial_state, N, dim, total, dev_status);
+    return cuda_rc(cudaGetLastError());
+  }
+  return GDN_OK;
+}
+
+int gdn_causal_conv1d_update(const uint16_t *x, uint16_t *conv_state, int P, int state_len,
+                             const uint16_t *weight, const uint16_t *bias, const int32_t *conv_state_indices,
+                             int R, int dim, int width, int activation, uint16_t *out, int32_t *dev_status,
+                             void *stream) {
+  if (R < 0 || P < 0 || dim <= 0 || (activation != 0 && activation != 1)) return GDN_EINVAL;
+  if (!conv_dims_ok(dim, width, state_len)) return GDN_EUNSUPPORTED;
+  if (R == 0) return GDN_OK;
+  if (R > 65535) return GDN_EUNSUPPORTED;
+  if (!x || !conv_state || !weight || !conv_state_indices || !out) return GDN_EINVAL;
+  conv_update_kernel<<<dim3((dim + 255) / 256, R), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      x, conv_state, P, state_len, weight, bias, conv_state_indices, dim, width, activation, out, out, out, dim,
+      dim, dev_status);
+  return cuda_rc(cudaGetLastError());
+}
+
+int gdn_conv_decode_pack(const uint16_t *mixed_qkv, uint16_t *conv_state, int P, int state_len,
+                         const uint16_t *weight, const uint16_t *bias, const int32_t *conv_state_indices, int R,
+                         int H, int HV, int K, int V, int width, int activation, uint16_t *q, uint16_t *k,
+                         uint16_t *v, int32_t *dev_status, void *stream) {
+  if (R < 0 || P < 0 || H <= 0 || HV <= 0 || K <= 0 || V <= 0 || (activation != 0 && activation != 1))
+    return GDN_EINVAL;
+  const int64_t dim64 = 2LL * H * K + (int64_t)HV * V;
+  if (dim64 > (1LL << 30)) return GDN_EUNSUPPORTED;
+  const int dim = static_cast<int>(dim64);
+  if (!conv_dims_ok(dim, width, state_len)) return GDN_EUNSUPPORTED;
+  if (R == 0) return GDN_OK;
+  if (R > 65535) return GDN_EUNSUPPORTED;
+  if (!mixed_qkv || !conv_state || !weight || !conv_state_indices || !q || !k || !v) return GDN_EINVAL;
+  conv_update_kernel<<<dim3((dim + 255) / 256, R), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      mixed_qkv, conv_state, P, state_len, weight, bias, conv_state_indices, dim, width, activation, q, k, v,
+      H * K, 2 * H * K, dev_status);
+  return cuda_rc(cudaGetLastError());
+}
+
+}  // extern "C"

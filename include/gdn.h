@@ -187,6 +187,75 @@ int gdn_chunk_fwd_noalloc(const uint16_t *q, const uint16_t *k, const uint16_t *
                           int use_qk_l2norm, uint16_t *o, float *final_state,
                           int32_t *dev_status, void *stream);
 
+/*
+ * Causal depthwise conv1d in front of Gated DeltaNet.  FastDeploy PR "support
+ * fla triton kernel for qwen3.5", Modifications table (causal_conv1d.py:
+ * causal_conv1d_update, causal_conv1d_fn) and Usage sections 3 and 4; LightLLM
+ * "gdn.py" prefill and decode backends (the conv runs over the packed
+ * q | k | v channels; decode fuses it with the split into q, k, v).
+ *
+ * Per channel d, for a sequence whose input stream is history ++ x (history =
+ * its slot's state, or zeros):
+ *     out[d, p] = act(bias[d] + sum_{j<W} weight[d, j] * stream[d, p + j])
+ * where the last tap multiplies the current token; afterwards the slot holds
+ * the last S (= state_len, >= W - 1) entries of the stream.  act: 0 = none,
+ * 1 = SiLU (x * sigmoid(x)).  All tensors bf16 (uint16_t bit patterns) except
+ * the int32 offsets / slots and the uint8 flags; fp32 accumulation.
+ * Supported: 1 <= W <= 8, W - 1 <= S <= 64.  Slot -1 (PAD) reads zeros and
+ * writes no state; other slots outside [0, P) set GDN_DEV_BAD_SLOT and are
+ * treated like PAD.
+ */
+
+/*
+ * gdn_causal_conv1d_fwd -- packed (varlen) prefill.
+ *   x                 : [dim, total] channel-first
+ *   weight            : [dim, width];  bias: [dim] or NULL
+ *   conv_states       : [P, dim, state_len], read and written in place (may be
+ *                       NULL when P = 0)
+ *   query_start_loc   : int32 [N + 1] device offsets (0, non-decreasing, total)
+ *   cache_indices     : int32 [N] slot per sequence, or NULL (no states at all)
+ *   has_initial_state : uint8 [N] (nonzero: start from the slot's state), or
+ *                       NULL (all start from zeros)
+ *   out               : [dim, total]
+ * Two launches on `stream`: the convolution, then the state update (so every
+ * read of an old state precedes the writes).  Offsets that break the rules set
+ * GDN_DEV_BAD_CU_SEQLENS; the tokens they fail to cover get zero output.
+ * Errors: GDN_EINVAL (null pointers, N = 0 with tokens, bad activation),
+ * GDN_EUNSUPPORTED (width / state_len out of range, more than 65535 x 2048
+ * tokens or 65535 sequences).
+ */
+int gdn_causal_conv1d_fwd(const uint16_t *x, const uint16_t *weight, const uint16_t *bias,
+                          uint16_t *conv_states, int P, int state_len,
+                          const int32_t *query_start_loc, const int32_t *cache_indices,
+                          const uint8_t *has_initial_state, int N, int dim, int64_t total,
+                          int width, int activation, uint16_t *out, int32_t *dev_status,
+                          void *stream);
+
+/*
+ * gdn_causal_conv1d_update -- one token per request against the state pool.
+ *   x                  : [R, dim] token-major
+ *   conv_state         : [P, dim, state_len], read and written in place
+ *   conv_state_indices : int32 [R]; -1 = PAD (zero output row, pool untouched)
+ *   out                : [R, dim]
+ * R = 0 is a no-op.  One launch.
+ */
+int gdn_causal_conv1d_update(const uint16_t *x, uint16_t *conv_state, int P, int state_len,
+                             const uint16_t *weight, const uint16_t *bias,
+                             const int32_t *conv_state_indices, int R, int dim, int width,
+                             int activation, uint16_t *out, int32_t *dev_status, void *stream);
+
+/*
+ * gdn_conv_decode_pack -- gdn_causal_conv1d_update over the packed channels
+ * [q (H*K) | k (H*K) | v (HV*V)] (dim = 2*H*K + HV*V) of mixed_qkv [R, dim],
+ * writing the three channel ranges straight into the layouts
+ * gdn_recurrent_decode takes: q, k [R, 1, H, K] and v [R, 1, HV, V].  One launch.
+ */
+int gdn_conv_decode_pack(const uint16_t *mixed_qkv, uint16_t *conv_state, int P, int state_len,
+                         const uint16_t *weight, const uint16_t *bias,
+                         const int32_t *conv_state_indices, int R, int H, int HV, int K, int V,
+                         int width, int activation, uint16_t *q, uint16_t *k, uint16_t *v,
+                         int32_t *dev_status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -101,3 +101,43 @@ def test_python_binding_checks_before_calling():
         gdn.gdn_chunk_fwd(q, q, q, q[..., 0], q[..., 0])
     with pytest.raises(ValueError):
         gdn.gdn_recurrent_decode(q, q, q, None, None)
+
+
+def test_conv_host_validation(lib):
+    NULL = None
+    fake = ctypes.c_void_p(16)
+    I64 = ctypes.c_int64
+
+    def fwd(x=fake, w=fake, st=fake, P=2, S=3, qsl=fake, cache=fake, N=1, dim=8, total=5, W=4, act=1,
+            out=fake):
+        return lib.gdn_causal_conv1d_fwd(x, w, NULL, st, P, S, qsl, cache, NULL, N, dim, I64(total), W, act,
+                                         out, NULL, NULL)
+
+    assert fwd(N=0, total=0) == gdn.GDN_OK                     # nothing to do, nothing launched
+    assert fwd(N=0) == gdn.GDN_EINVAL                          # tokens without a sequence
+    assert fwd(qsl=NULL) == gdn.GDN_EINVAL
+    assert fwd(w=NULL) == gdn.GDN_EINVAL
+    assert fwd(x=NULL) == gdn.GDN_EINVAL
+    assert fwd(st=NULL) == gdn.GDN_EINVAL                      # slots given but no pool
+    assert fwd(act=2) == gdn.GDN_EINVAL
+    assert fwd(W=9) == gdn.GDN_EUNSUPPORTED                    # width above 8
+    assert fwd(S=2) == gdn.GDN_EUNSUPPORTED                    # state shorter than W - 1
+    assert fwd(S=65) == gdn.GDN_EUNSUPPORTED
+
+    def upd(x=fake, st=fake, w=fake, idx=fake, R=3, dim=8, W=4, S=3, out=fake):
+        return lib.gdn_causal_conv1d_update(x, st, 2, S, w, NULL, idx, R, dim, W, 1, out, NULL, NULL)
+
+    assert upd(R=0) == gdn.GDN_OK
+    assert upd(idx=NULL) == gdn.GDN_EINVAL
+    assert upd(st=NULL) == gdn.GDN_EINVAL
+    assert upd(W=0) == gdn.GDN_EUNSUPPORTED
+    assert upd(dim=0) == gdn.GDN_EINVAL
+
+    def pack(q=fake, R=2, H=2, HV=4, K=8, V=8, W=4, S=3):
+        return lib.gdn_conv_decode_pack(fake, fake, 2, S, fake, NULL, fake, R, H, HV, K, V, W, 1, q, fake, fake,
+                                        NULL, NULL)
+
+    assert pack(R=0) == gdn.GDN_OK
+    assert pack(q=NULL) == gdn.GDN_EINVAL
+    assert pack(H=0) == gdn.GDN_EINVAL
+    assert pack(S=1) == gdn.GDN_EUNSUPPORTED
