@@ -232,7 +232,7 @@ def run_ours(args, rank, world, local_rank):
         if ev is not None:
             ev[1].record(stream)
 
-    launches_per_step = 2  # gating kernel + chunk kernel
+    launches_per_step = 3  # gating kernel + the chunk forward's prep and walk kernels
 
     def barrier():
         if world > 1:
@@ -299,6 +299,7 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_extras:
         line["decode"] = bench_decode(dev, stream, hbm, args)
         line["gating"] = bench_gating(dev, stream, hbm, args)
+        line["conv1d"] = bench_conv(dev, stream, hbm, args)
         line["e2e"] = bench_e2e(case, dev, stream, args, world)
         if rank == 0 and world == 1:
             gg, bb = gates_for_cpu(case)
@@ -380,6 +381,53 @@ def bench_gating(dev, stream, hbm, args):
     gbs = gating_bytes(n_tok * HV) / (ms / 1e3) / 1e9
     return {"workload": f"gating {n_tok}x{HV} (bf16 a,b -> fp32 g,beta; 200 MB in+out > L2)",
             "ms": ms, "achieved_GBps": gbs, "peak": hbm, "frac": gbs / hbm}
+
+
+def bench_conv(dev, stream, hbm, args):
+    """Causal conv1d sub-benchmark: the long prefill's conv (8192 packed q|k|v
+    channels x 65536 tokens, 2.1 GB in+out > L2) and the batched decode's conv
+    update (256 requests x 8192 channels against a 512-slot state pool)."""
+    import torch
+    import gated_deltanet_chunked_chunk_gb300 as gdn
+    from gated_deltanet_chunked_chunk_gb300 import workloads as W
+    d = lambda t: t.to(dev).contiguous()
+
+    def timed(fn, reps):
+        for _ in range(3):
+            fn()
+        times = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            times.append(e0.elapsed_time(e1))
+        return statistics.median(times)
+
+    pc = W.conv_prefill_long()
+    x, w, b, st = d(pc.x), d(pc.weight), d(pc.bias), d(pc.conv_states)
+    qsl, ci, hi = d(pc.query_start_loc), d(pc.cache_indices), d(pc.has_initial_state)
+    out = torch.empty_like(x)
+    ms_p = timed(lambda: gdn.gdn_causal_conv1d_fwd(x, w, b, st, qsl, ci, hi, out=out), max(args.steps, 5))
+    dim, total = x.shape
+    S = st.shape[2]
+    bytes_p = 2 * dim * total * 2 + 2 * len(pc.cache_indices) * dim * S * 2 + dim * (w.shape[1] + 1) * 2
+    del x, out
+    dc = W.conv_decode_r256()
+    xd, wd, bd, sd, idx = d(dc.x), d(dc.weight), d(dc.bias), d(dc.conv_state), d(dc.indices)
+    outd = torch.empty_like(xd)
+    ms_d = timed(lambda: gdn.gdn_causal_conv1d_update(xd, sd, wd, bd, idx, out=outd), max(args.steps, 20))
+    valid = int((dc.indices >= 0).sum())
+    R, dimd = xd.shape
+    bytes_d = 2 * R * dimd * 2 + 2 * valid * dimd * sd.shape[2] * 2
+    gb_p = bytes_p / (ms_p / 1e3) / 1e9
+    return {"prefill": {"workload": f"conv1d prefill dim {dim} x {total} tokens, width {w.shape[1]}, SiLU, "
+                                    "initial state", "ms": ms_p, "achieved_GBps": gb_p, "peak": hbm,
+                        "frac": gb_p / hbm},
+            "decode": {"workload": f"conv1d update R={R} (valid {valid}) x {dimd} channels, pool "
+                                   f"{tuple(sd.shape)} bf16", "us": ms_d * 1e3,
+                       "achieved_GBps": bytes_d / (ms_d / 1e3) / 1e9}}
 
 
 def bench_e2e(case, dev, stream, args, world):

@@ -15,10 +15,9 @@
 //
 // All three ops are memory-bound (a few multiply-adds per element).
 //  * conv_prefill_kernel: x is channel-first [dim, total]; a CTA takes one
-//    channel and 2048 tokens, a warp 32 consecutive tokens per step, so every
-//    tap load is a 64-byte coalesced segment of one row (the W - 1 re-reads of
-//    a token hit L1).  A thread finds its token's sequence by binary search in
-//    query_start_loc.
+//    channel and 8192 tokens, a thread 8 consecutive tokens per step with
+//    16-byte loads and stores (the general per-token path, with a binary
+//    search in query_start_loc, serves sequence starts and unaligned rows).
 //  * conv_state_kernel (same stream, after the prefill kernel, so every read
 //    of the old states precedes the writes): one thread per (sequence,
 //    channel) writes the slot's new last-S inputs.
@@ -34,7 +33,7 @@ namespace {
 
 constexpr int kConvMaxW = 8;
 constexpr int kConvMaxS = 64;
-constexpr int kPrefillTile = 2048;
+constexpr int kPrefillTile = 8192;
 
 __device__ __forceinline__ float conv_act(float x, int act) { return act ? x / (1.f + expf(-x)) : x; }
 
@@ -49,11 +48,53 @@ __device__ __forceinline__ int seq_of(const int32_t *qsl, int N, int64_t t) {
   return lo;
 }
 
+// Output of token t (one element), general path: sequence by binary search,
+// taps before the sequence start read the slot's state or zero.
+__device__ __forceinline__ float conv_prefill_one(const uint16_t *__restrict__ xr, const float *wf, float b0,
+                                                  const uint16_t *__restrict__ states, int P, int S,
+                                                  const int32_t *__restrict__ qsl, const int32_t *__restrict__ cache,
+                                                  const uint8_t *__restrict__ has_init, int N, int dim, int d,
+                                                  int64_t t, int W, int32_t *dev_status, bool &ok) {
+  ok = false;
+  const int n = seq_of(qsl, N, t);
+  if (n < 0 || n >= N || qsl[n] < 0) {  // offsets that do not cover this token
+    gdn::set_status(dev_status, GDN_DEV_BAD_CU_SEQLENS);
+    return 0.f;
+  }
+  const int64_t s0 = qsl[n], p = t - s0;
+  const int slot = cache ? cache[n] : -1;
+  if (slot < -1 || slot >= P) gdn::set_status(dev_status, GDN_DEV_BAD_SLOT);
+  const bool hist = slot >= 0 && slot < P && has_init && has_init[n];
+  const uint16_t *srow = hist ? states + ((int64_t)slot * dim + d) * S : nullptr;
+  float acc = b0;
+#pragma unroll
+  for (int j = 0; j < kConvMaxW; ++j) {
+    if (j < W) {
+      const int64_t src = p - (W - 1) + j;
+      float v = 0.f;
+      if (src >= 0) v = gdn::bf2f(xr[s0 + src]);
+      else if (hist) v = gdn::bf2f(srow[S + src]);
+      acc = fmaf(wf[j], v, acc);
+    }
+  }
+  ok = true;
+  return acc;
+}
+
+// One CTA per (channel, 2048-token tile).  Vector path (rows 16-byte aligned):
+// a thread takes 8 consecutive tokens, loads them and the 8 before them with
+// two 16-byte loads (the second mostly an L1 hit) and stores 16 bytes; tokens
+// within W - 1 of a sequence start, or sharing the 8 with a boundary, take the
+// general path.  Without aligned rows every token takes the general path.
+// WT > 0 fixes the width at compile time (so the 16-value window stays in
+// registers); WT = 0 takes it from W at run time.
+template <int WT>
 __global__ void __launch_bounds__(256) conv_prefill_kernel(
     const uint16_t *__restrict__ x, const uint16_t *__restrict__ w, const uint16_t *__restrict__ bias,
     const uint16_t *__restrict__ states, int P, int S, const int32_t *__restrict__ qsl,
     const int32_t *__restrict__ cache, const uint8_t *__restrict__ has_init, int N, int dim, int64_t total,
-    int W, int act, uint16_t *__restrict__ out, int32_t *dev_status) {
+    int W_rt, int act, uint16_t *__restrict__ out, int32_t *dev_status, int vec) {
+  const int W = WT > 0 ? WT : W_rt;
   const int d = blockIdx.x;
   float wf[kConvMaxW];
 #pragma unroll
@@ -61,36 +102,58 @@ __global__ void __launch_bounds__(256) conv_prefill_kernel(
   const float b0 = bias ? gdn::bf2f(bias[d]) : 0.f;
   const uint16_t *xr = x + (int64_t)d * total;
   uint16_t *orow = out + (int64_t)d * total;
-  const int64_t t_end = min(total, (int64_t)(blockIdx.y + 1) * kPrefillTile);
-  for (int64_t t = (int64_t)blockIdx.y * kPrefillTile + threadIdx.x; t < t_end; t += blockDim.x) {
-    const int n = seq_of(qsl, N, t);
-    if (n < 0 || n >= N) {  // offsets that do not cover this token
-      gdn::set_status(dev_status, GDN_DEV_BAD_CU_SEQLENS);
-      orow[t] = 0;
-      continue;
+  const int64_t tile0 = (int64_t)blockIdx.y * kPrefillTile;
+  const int64_t t_end = min(total, tile0 + kPrefillTile);
+  if (!vec) {
+    for (int64_t t = tile0 + threadIdx.x; t < t_end; t += blockDim.x) {
+      bool ok;
+      const float acc = conv_prefill_one(xr, wf, b0, states, P, S, qsl, cache, has_init, N, dim, d, t, W,
+                                         dev_status, ok);
+      orow[t] = ok ? gdn::f2bf(conv_act(acc, act)) : (uint16_t)0;
     }
-    const int64_t s0 = qsl[n], p = t - s0;
-    if (s0 < 0) {
-      gdn::set_status(dev_status, GDN_DEV_BAD_CU_SEQLENS);
-      orow[t] = 0;
-      continue;
-    }
-    const int slot = cache ? cache[n] : -1;
-    if (slot < -1 || slot >= P) gdn::set_status(dev_status, GDN_DEV_BAD_SLOT);
-    const bool hist = slot >= 0 && slot < P && has_init && has_init[n];
-    const uint16_t *srow = hist ? states + ((int64_t)slot * dim + d) * S : nullptr;
-    float acc = b0;
+    return;
+  }
+  for (int64_t t0 = tile0 + 8 * threadIdx.x; t0 < t_end; t0 += 8 * blockDim.x) {
+  // Fast path: all 8 tokens in one sequence, at least W - 1 tokens past its start.
+  bool fast = t0 + 8 <= t_end;
+  if (fast) {
+    const int n = seq_of(qsl, N, t0);
+    fast = n >= 0 && n < N && qsl[n] >= 0 && t0 - qsl[n] >= W - 1 && qsl[n + 1] >= t0 + 8;
+  }
+  if (fast) {
+    const uint4 cur = *reinterpret_cast<const uint4 *>(xr + t0);
+    uint4 prv = make_uint4(0, 0, 0, 0);
+    if (t0 >= 8) prv = *reinterpret_cast<const uint4 *>(xr + t0 - 8);
+    const uint32_t wv[8] = {prv.x, prv.y, prv.z, prv.w, cur.x, cur.y, cur.z, cur.w};
+    float v[16];
 #pragma unroll
-    for (int j = 0; j < kConvMaxW; ++j) {
-      if (j < W) {
-        const int64_t src = p - (W - 1) + j;
-        float v = 0.f;
-        if (src >= 0) v = gdn::bf2f(xr[s0 + src]);
-        else if (hist) v = gdn::bf2f(srow[S + src]);
-        acc = fmaf(wf[j], v, acc);
-      }
+    for (int i = 0; i < 8; ++i) {
+      v[2 * i] = gdn::bf2f(static_cast<uint16_t>(wv[i] & 0xFFFFu));
+      v[2 * i + 1] = gdn::bf2f(static_cast<uint16_t>(wv[i] >> 16));
     }
-    orow[t] = gdn::f2bf(conv_act(acc, act));
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      float a0 = b0, a1 = b0;
+#pragma unroll
+      for (int j = 0; j < kConvMaxW; ++j) {
+        if (j < W) {
+          a0 = fmaf(wf[j], v[8 + e - (W - 1) + j], a0);
+          a1 = fmaf(wf[j], v[9 + e - (W - 1) + j], a1);
+        }
+      }
+      o[e / 2] = static_cast<uint32_t>(gdn::f2bf(conv_act(a0, act))) |
+                 (static_cast<uint32_t>(gdn::f2bf(conv_act(a1, act))) << 16);
+    }
+    *reinterpret_cast<uint4 *>(orow + t0) = make_uint4(o[0], o[1], o[2], o[3]);
+    continue;
+  }
+  for (int64_t t = t0; t < t0 + 8 && t < t_end; ++t) {
+    bool ok;
+    const float acc = conv_prefill_one(xr, wf, b0, states, P, S, qsl, cache, has_init, N, dim, d, t, W,
+                                       dev_status, ok);
+    orow[t] = ok ? gdn::f2bf(conv_act(acc, act)) : (uint16_t)0;
+  }
   }
 }
 
@@ -181,9 +244,17 @@ int gdn_causal_conv1d_fwd(const uint16_t *x, const uint16_t *weight, const uint1
   if (total > 0) {
     const int64_t tiles = (total + kPrefillTile - 1) / kPrefillTile;
     if (tiles > 65535) return GDN_EUNSUPPORTED;
-    conv_prefill_kernel<<<dim3(dim, (unsigned)tiles), 256, 0, s>>>(
-        x, weight, bias, conv_states, P, state_len, query_start_loc, cache_indices, has_initial_state, N, dim,
-        total, width, activation, out, dev_status);
+    // 16-byte vector access needs every row start 16-byte aligned.
+    const int vec = (total % 8 == 0) && ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(out)) & 15) == 0;
+    const dim3 grid(dim, (unsigned)tiles);
+    if (width == 4)
+      conv_prefill_kernel<4><<<grid, 256, 0, s>>>(x, weight, bias, conv_states, P, state_len, query_start_loc,
+                                                  cache_indices, has_initial_state, N, dim, total, width,
+                                                  activation, out, dev_status, vec);
+    else
+      conv_prefill_kernel<0><<<grid, 256, 0, s>>>(x, weight, bias, conv_states, P, state_len, query_start_loc,
+                                                  cache_indices, has_initial_state, N, dim, total, width,
+                                                  activation, out, dev_status, vec);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return GDN_ECUDA;
   }

@@ -221,7 +221,7 @@ int gdn_chunk_fwd_noalloc(const uint16_t *q, const uint16_t *k, const uint16_t *
  * read of an old state precedes the writes).  Offsets that break the rules set
  * GDN_DEV_BAD_CU_SEQLENS; the tokens they fail to cover get zero output.
  * Errors: GDN_EINVAL (null pointers, N = 0 with tokens, bad activation),
- * GDN_EUNSUPPORTED (width / state_len out of range, more than 65535 x 2048
+ * GDN_EUNSUPPORTED (width / state_len out of range, more than 65535 x 8192
  * tokens or 65535 sequences).
  */
 int gdn_causal_conv1d_fwd(const uint16_t *x, const uint16_t *weight, const uint16_t *bias,
