@@ -221,3 +221,63 @@ int oracle_decode(const double *q, const double *k, const double *v,
   free(qn); free(kn); free(r);
   return 0;
 }
+
+/*
+ * Multi-token (MTP) decode against the state pool: LightLLM "gdn.py", the
+ * MTP decode path (mtp_step + 1 tokens per request packed by cu_seqlens,
+ * 2-D read / write state indices of width ld = mtp_step + 1, and
+ * num_accepted_tokens locating the state the step starts from).  Request n
+ * starts from pool[read_idx[n][num_acc[n] - 1]] (column 0 without num_acc),
+ * runs the per-token recurrence over its tokens and stores the state after
+ * its i-th token into pool[write_idx[n][i]] (-1: not stored).  A read slot of
+ * -1 is a PAD request: zero outputs, nothing stored.  Other out-of-range
+ * slots or counts set *bad_index and are treated like PAD (reads) or skipped
+ * (writes).
+ */
+int oracle_decode_mtp(const double *q, const double *k, const double *v,
+                      const double *g, const double *beta, double scale,
+                      int use_l2norm, double *pool, int P, const int *cu, int N,
+                      const int *read_idx, const int *write_idx, int ld,
+                      const int *num_acc, int H, int HV, int K, int V, double *o,
+                      int *bad_index) {
+  if (H <= 0 || HV <= 0 || HV % H != 0 || ld <= 0) return -1;
+  if (!(scale > 0.0)) scale = 1.0 / sqrt((double)K);
+  int G = HV / H;
+  double *qn = (double *)malloc(sizeof(double) * K);
+  double *kn = (double *)malloc(sizeof(double) * K);
+  double *r = (double *)malloc(sizeof(double) * V);
+  double *S = (double *)malloc(sizeof(double) * (size_t)K * V);
+  if (bad_index) *bad_index = 0;
+  for (int n = 0; n < N; ++n) {
+    int t0 = cu[n], t1 = cu[n + 1];
+    int acc = num_acc ? num_acc[n] : 1;
+    int ok = (t1 - t0 >= 0 && t1 - t0 <= ld && acc >= 1 && acc <= ld);
+    int rs = ok ? read_idx[(long)n * ld + acc - 1] : -1;
+    if (!ok && bad_index) *bad_index = 1;
+    int valid = (rs >= 0 && rs < P);
+    if (ok && !valid && rs != -1 && bad_index) *bad_index = 1;
+    for (int hv = 0; hv < HV; ++hv) {
+      if (!valid) {
+        for (int t = t0; t < t1 && t >= 0; ++t)
+          for (int j = 0; j < V; ++j) o[((long)t * HV + hv) * V + j] = 0.0;
+        continue;
+      }
+      int h = hv / G;
+      memcpy(S, pool + ((long)rs * HV + hv) * K * V, sizeof(double) * (size_t)K * V);
+      for (int i = 0; i < t1 - t0; ++i) {
+        long t = t0 + i;
+        const double *qt = q + (t * H + h) * K;
+        const double *kt = k + (t * H + h) * K;
+        if (use_l2norm) { l2norm_d(qt, K, qn); l2norm_d(kt, K, kn); }
+        else { memcpy(qn, qt, sizeof(double) * K); memcpy(kn, kt, sizeof(double) * K); }
+        token_step(S, qn, kn, v + (t * HV + hv) * V, g[t * HV + hv], beta[t * HV + hv], scale, K, V,
+                   o + (t * HV + hv) * V, r);
+        int ws = write_idx[(long)n * ld + i];
+        if (ws >= 0 && ws < P) memcpy(pool + ((long)ws * HV + hv) * K * V, S, sizeof(double) * (size_t)K * V);
+        else if (ws != -1 && bad_index) *bad_index = 1;
+      }
+    }
+  }
+  free(qn); free(kn); free(r); free(S);
+  return 0;
+}

@@ -6,9 +6,12 @@ module imports nothing from the product package.
 
 Contents
 --------
-* ``gating``, ``recurrent``, ``decode``: thin ctypes front-ends to the plain C
-  fp64 oracle in ``gdn_oracle.c`` (the per-token definitions; see that file's
-  header for the passages each one follows).
+* ``gating``, ``recurrent``, ``decode``, ``decode_mtp``: thin ctypes
+  front-ends to the plain C fp64 oracle in ``gdn_oracle.c`` (the per-token
+  definitions; see that file for the passages each one follows).
+* ``decode_bf16_pool``: ``decode`` on a pool stored in bf16 (the step runs on
+  the stored values, the new state is rounded back to bf16 by ``round_bf16``,
+  ties to even).
 * Independent numpy restatements used only to pin the C oracle:
     - ``gating_scalar``: the gating formula evaluated with Python's ``math``.
     - ``transition_product``: the recurrence written as
@@ -79,6 +82,10 @@ def _load():
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 d, i]
             lib.oracle_decode.restype = ctypes.c_int
+            CI = ctypes.c_int
+            lib.oracle_decode_mtp.argtypes = [
+                d, d, d, d, d, ctypes.c_double, CI, d, CI, i, CI, i, i, CI, i, CI, CI, CI, CI, d, i]
+            lib.oracle_decode_mtp.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -177,6 +184,60 @@ def decode(q, k, v, g, beta, pool, ssm_indices, scale=None, use_qk_l2norm=True):
     if rc != 0:
         raise ValueError("oracle_decode: inconsistent arguments")
     return o, pool, bad.value
+
+
+def decode_mtp(q, k, v, g, beta, pool, cu_seqlens, read_idx, write_idx, num_accepted=None, scale=None,
+               use_qk_l2norm=True):
+    """Multi-token decode (see ``oracle_decode_mtp`` in gdn_oracle.c).
+    q, k [Ttot,H,K] (or [Ttot,1,H,K]); v [Ttot,HV,V]; g, beta [Ttot,HV];
+    pool [P,HV,K,V] (a copy is updated and returned); cu_seqlens [N+1];
+    read_idx / write_idx [N, ld]; num_accepted [N] or None.
+    Returns (o [Ttot,HV,V], new_pool, bad_index_flag)."""
+    q, k, v, g, beta = map(_f64, (q, k, v, g, beta))
+    q = q.reshape(q.shape[0], -1, q.shape[-1])
+    k = k.reshape(k.shape[0], -1, k.shape[-1])
+    v = v.reshape(v.shape[0], -1, v.shape[-1])
+    g = g.reshape(g.shape[0], -1)
+    beta = beta.reshape(beta.shape[0], -1)
+    Tt, H, K = q.shape
+    HV, V = v.shape[1], v.shape[2]
+    pool = _f64(pool).copy()
+    P = pool.shape[0]
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    ri = np.ascontiguousarray(np.asarray(read_idx, dtype=np.int32))
+    wi = np.ascontiguousarray(np.asarray(write_idx, dtype=np.int32))
+    N, ld = ri.shape
+    na = None if num_accepted is None else np.ascontiguousarray(np.asarray(num_accepted, dtype=np.int32))
+    o = np.zeros((Tt, HV, V))
+    bad = ctypes.c_int(0)
+    sc = float(scale) if scale is not None else -1.0
+    rc = _load().oracle_decode_mtp(_dp(q), _dp(k), _dp(v), _dp(g), _dp(beta), sc, int(bool(use_qk_l2norm)),
+                                   _dp(pool), P, _ip(cu), N, _ip(ri), _ip(wi), ld,
+                                   None if na is None else _ip(na), H, HV, K, V, _dp(o), ctypes.byref(bad))
+    if rc != 0:
+        raise ValueError("oracle_decode_mtp: inconsistent arguments")
+    return o, pool, bad.value
+
+
+def round_bf16(x):
+    """Round fp64 values to the nearest bf16 (8 significant bits, ties to even)
+    and return them as fp64: the storage rounding of a bf16 state pool."""
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)                    # x = m 2^e, 0.5 <= |m| < 1
+    return np.ldexp(np.round(m * 256.0), e - 8)
+
+
+def decode_bf16_pool(q, k, v, g, beta, pool_bf16_values, ssm_indices, scale=None, use_qk_l2norm=True):
+    """One-token decode against a pool stored in bf16: the step runs on the
+    stored values (upcast), the output uses the updated state, and the state is
+    stored back rounded to bf16.  pool_bf16_values holds the bf16 numbers as
+    floats.  Returns (o, new_pool_values, bad_index_flag)."""
+    pool = _f64(pool_bf16_values)
+    o, new, bad = decode(q, k, v, g, beta, pool, ssm_indices, scale=scale, use_qk_l2norm=use_qk_l2norm)
+    touched = sorted({int(s) for s in np.asarray(ssm_indices).ravel() if 0 <= int(s) < pool.shape[0]})
+    for s in touched:
+        new[s] = round_bf16(new[s])
+    return o, new, bad
 
 
 # --------------------------------------------------------------------------
