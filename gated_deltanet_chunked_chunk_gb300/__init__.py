@@ -23,7 +23,8 @@ import torch
 
 __all__ = ["gdn_gating", "gdn_chunk_fwd", "gdn_recurrent_decode", "chunk_fwd_workspace_size",
            "gdn_chunk_fwd_noalloc", "NOALLOC_SCRATCH_BYTES", "gdn_causal_conv1d_fwd",
-           "gdn_causal_conv1d_update", "gdn_conv_decode_pack",
+           "gdn_causal_conv1d_update", "gdn_conv_decode_pack", "gdn_recurrent_decode_bf16",
+           "gdn_recurrent_decode_mtp",
            "GDNError", "lib_path", "load_library", "status_string", "DEV_BAD_CU_SEQLENS",
            "DEV_BAD_SLOT", "DEV_WAIT_TIMEOUT", "EXPORTED_SYMBOLS"]
 
@@ -38,7 +39,8 @@ DEV_BAD_CU_SEQLENS, DEV_BAD_SLOT, DEV_WAIT_TIMEOUT = 1, 2, 4
 #: Every symbol include/gdn.h declares (checked by the tests).
 EXPORTED_SYMBOLS = ("gdn_status_string", "gdn_version", "gdn_gating", "gdn_chunk_fwd_workspace_size",
                     "gdn_chunk_fwd", "gdn_recurrent_decode", "gdn_chunk_fwd_noalloc",
-                    "gdn_causal_conv1d_fwd", "gdn_causal_conv1d_update", "gdn_conv_decode_pack")
+                    "gdn_causal_conv1d_fwd", "gdn_causal_conv1d_update", "gdn_conv_decode_pack",
+                    "gdn_recurrent_decode_bf16", "gdn_recurrent_decode_mtp")
 
 #: Size of the fixed scratch buffer behind gdn_chunk_fwd_noalloc (bytes).
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -86,6 +88,12 @@ def load_library():
         lib.gdn_causal_conv1d_update.restype = I
         lib.gdn_conv_decode_pack.argtypes = [P, P, I, I, P, P, P, I, I, I, I, I, I, I, P, P, P, P, P]
         lib.gdn_conv_decode_pack.restype = I
+        lib.gdn_recurrent_decode_bf16.argtypes = [P, P, P, P, P, P, P, P, P, F, I, P, I, P, I, I, I, I, I,
+                                                  P, P, P]
+        lib.gdn_recurrent_decode_bf16.restype = I
+        lib.gdn_recurrent_decode_mtp.argtypes = [P, P, P, P, P, P, P, P, P, F, I, P, I, P, I, I, P, P, I, P,
+                                                 I, I, I, I, P, P, P]
+        lib.gdn_recurrent_decode_mtp.restype = I
         _lib = lib
         return lib
 
@@ -402,3 +410,68 @@ def gdn_conv_decode_pack(mixed_qkv: torch.Tensor, conv_state: torch.Tensor, weig
     if rc != GDN_OK:
         raise GDNError("gdn_conv_decode_pack", rc)
     return q, k, v
+
+
+# ------------------------------------------------------- decode variants
+def _gate_args(g, beta, A_log, a, b, dt_bias, dev):
+    for t, n, dt in ((g, "g", torch.float32), (beta, "beta", torch.float32),
+                     (A_log, "A_log", torch.float32), (dt_bias, "dt_bias", torch.float32),
+                     (a, "a", torch.bfloat16), (b, "b", torch.bfloat16)):
+        _check(t, n, dt, dev)
+
+
+def gdn_recurrent_decode_bf16(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ssm_pool: torch.Tensor,
+                              ssm_indices: torch.Tensor, g=None, beta=None, A_log=None, a=None, b=None,
+                              dt_bias=None, scale=None, use_qk_l2norm: bool = True, o=None, dev_status=None):
+    """gdn_recurrent_decode against a bf16 state pool [P, HV, K, V] (updated in place)."""
+    dev = q.device
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, torch.bfloat16, dev, 4)
+    _check(ssm_pool, "ssm_pool", torch.bfloat16, dev, 4)
+    _check(ssm_indices, "ssm_indices", torch.int32, dev, 1)
+    _gate_args(g, beta, A_log, a, b, dt_bias, dev)
+    R, _, H, K = q.shape
+    HV, V = v.shape[2], v.shape[3]
+    if o is None:
+        o = torch.empty((R, 1, HV, V), dtype=torch.bfloat16, device=dev)
+    rc = load_library().gdn_recurrent_decode_bf16(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A_log), _ptr(a), _ptr(b), _ptr(dt_bias),
+        _scale_arg(scale), int(bool(use_qk_l2norm)), _ptr(ssm_pool), ssm_pool.shape[0], _ptr(ssm_indices), R,
+        H, HV, K, V, _ptr(o), _ptr(dev_status), _stream(dev))
+    if rc != GDN_OK:
+        raise GDNError("gdn_recurrent_decode_bf16", rc)
+    return o
+
+
+def gdn_recurrent_decode_mtp(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ssm_pool: torch.Tensor,
+                             cu_seqlens: torch.Tensor, read_indices: torch.Tensor, write_indices: torch.Tensor,
+                             num_accepted_tokens: Optional[torch.Tensor] = None, g=None, beta=None, A_log=None,
+                             a=None, b=None, dt_bias=None, scale=None, use_qk_l2norm: bool = True, o=None,
+                             dev_status=None):
+    """Multi-token decode; see include/gdn.h.  q, k [Ttot, H, K], v [Ttot, HV, V] bf16;
+    ssm_pool fp32 [P, HV, K, V] (in place); cu_seqlens int32 [N + 1]; read / write
+    indices int32 [N, ld]; num_accepted_tokens int32 [N] or None.  Returns o [Ttot, HV, V]."""
+    dev = q.device
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, torch.bfloat16, dev, 3)
+    _check(ssm_pool, "ssm_pool", torch.float32, dev, 4)
+    _check(cu_seqlens, "cu_seqlens", torch.int32, dev, 1)
+    _check(read_indices, "read_indices", torch.int32, dev, 2)
+    _check(write_indices, "write_indices", torch.int32, dev, 2)
+    _check(num_accepted_tokens, "num_accepted_tokens", torch.int32, dev, 1)
+    _gate_args(g, beta, A_log, a, b, dt_bias, dev)
+    if read_indices.shape != write_indices.shape:
+        raise ValueError("read_indices and write_indices must have the same shape [N, ld]")
+    Tt, H, K = q.shape
+    HV, V = v.shape[1], v.shape[2]
+    N, ld = read_indices.shape
+    if o is None:
+        o = torch.empty((Tt, HV, V), dtype=torch.bfloat16, device=dev)
+    rc = load_library().gdn_recurrent_decode_mtp(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A_log), _ptr(a), _ptr(b), _ptr(dt_bias),
+        _scale_arg(scale), int(bool(use_qk_l2norm)), _ptr(ssm_pool), ssm_pool.shape[0], _ptr(cu_seqlens), N, Tt,
+        _ptr(read_indices), _ptr(write_indices), ld, _ptr(num_accepted_tokens), H, HV, K, V, _ptr(o),
+        _ptr(dev_status), _stream(dev))
+    if rc != GDN_OK:
+        raise GDNError("gdn_recurrent_decode_mtp", rc)
+    return o

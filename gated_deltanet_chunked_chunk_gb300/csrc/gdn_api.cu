@@ -73,6 +73,29 @@ int gdn_chunk_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
   return cuda_status(gdn_host::launch_chunk(a, static_cast<cudaStream_t>(stream)));
 }
 
+namespace {
+// Shared checks of the decode entry points; fills the gate part of `d`.
+int decode_common(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *g, const float *beta,
+                  const float *A_log, const uint16_t *a, const uint16_t *b, const float *dt_bias, float scale,
+                  int use_qk_l2norm, const void *pool, int H, int HV, int K, int V, const uint16_t *o,
+                  gdn_host::DecodeArgs &d) {
+  if (H <= 0 || HV <= 0 || K <= 0 || V <= 0) return GDN_EINVAL;
+  if (HV % H != 0) return GDN_EINVAL;
+  if (!head_dim_ok(K) || !head_dim_ok(V)) return GDN_EUNSUPPORTED;
+  if (!q || !k || !v || !o || !pool) return GDN_EINVAL;
+  const bool given = g || beta;
+  const bool fused = A_log || a || b || dt_bias;
+  if (given == fused) return GDN_EINVAL;  // exactly one gate group
+  if (given && !(g && beta)) return GDN_EINVAL;
+  if (fused && !(A_log && a && b && dt_bias)) return GDN_EINVAL;
+  d.q = q; d.k = k; d.v = v; d.g = g; d.beta = beta; d.A_log = A_log; d.a = a; d.b = b; d.dt_bias = dt_bias;
+  d.scale = (scale > 0.f) ? scale : 1.f / sqrtf((float)K);  // also catches NaN
+  d.l2 = use_qk_l2norm ? 1 : 0;
+  d.H = H; d.HV = HV; d.K = K; d.V = V;
+  return GDN_OK;
+}
+}  // namespace
+
 int gdn_recurrent_decode(const uint16_t *q, const uint16_t *k,
                          const uint16_t *v, const float *g, const float *beta,
                          const float *A_log, const uint16_t *a,
@@ -81,21 +104,65 @@ int gdn_recurrent_decode(const uint16_t *q, const uint16_t *k,
                          const int32_t *ssm_indices, int R, int H, int HV,
                          int K, int V, uint16_t *o, int32_t *dev_status,
                          void *stream) {
-  if (R < 0 || P < 0 || H <= 0 || HV <= 0 || K <= 0 || V <= 0) return GDN_EINVAL;
-  if (HV % H != 0) return GDN_EINVAL;
+  if (R < 0 || P < 0) return GDN_EINVAL;
+  if (H <= 0 || HV <= 0 || K <= 0 || V <= 0 || HV % H != 0) return GDN_EINVAL;
   if (!head_dim_ok(K) || !head_dim_ok(V)) return GDN_EUNSUPPORTED;
   if (R == 0) return GDN_OK;
-  if (!q || !k || !v || !o || !ssm_indices || !ssm_pool) return GDN_EINVAL;
-  const bool given = g || beta;
-  const bool fused = A_log || a || b || dt_bias;
-  if (given == fused) return GDN_EINVAL;  // exactly one gate group
-  if (given && !(g && beta)) return GDN_EINVAL;
-  if (fused && !(A_log && a && b && dt_bias)) return GDN_EINVAL;
-  if (!(scale > 0.f)) scale = 1.f / sqrtf((float)K);
-  return cuda_status(gdn_host::launch_decode(q, k, v, g, beta, A_log, a, b, dt_bias, scale,
-                                             use_qk_l2norm ? 1 : 0, ssm_pool, P, ssm_indices,
-                                             R, H, HV, K, V, o, dev_status,
-                                             static_cast<cudaStream_t>(stream)));
+  if (!ssm_indices) return GDN_EINVAL;
+  gdn_host::DecodeArgs d{};
+  const int rc = decode_common(q, k, v, g, beta, A_log, a, b, dt_bias, scale, use_qk_l2norm, ssm_pool, H, HV,
+                               K, V, o, d);
+  if (rc != GDN_OK) return rc;
+  d.pool = ssm_pool; d.pool_bf16 = 0; d.P = P;
+  d.cu = nullptr; d.N = R; d.Ttot = R;
+  d.read_idx = ssm_indices; d.write_idx = ssm_indices; d.ld = 1; d.num_acc = nullptr;
+  d.o = o; d.dev_status = dev_status;
+  return cuda_status(gdn_host::launch_decode_general(d, static_cast<cudaStream_t>(stream)));
+}
+
+int gdn_recurrent_decode_bf16(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *g,
+                              const float *beta, const float *A_log, const uint16_t *a, const uint16_t *b,
+                              const float *dt_bias, float scale, int use_qk_l2norm, uint16_t *ssm_pool, int P,
+                              const int32_t *ssm_indices, int R, int H, int HV, int K, int V, uint16_t *o,
+                              int32_t *dev_status, void *stream) {
+  if (R < 0 || P < 0) return GDN_EINVAL;
+  if (H <= 0 || HV <= 0 || K <= 0 || V <= 0 || HV % H != 0) return GDN_EINVAL;
+  if (!head_dim_ok(K) || !head_dim_ok(V)) return GDN_EUNSUPPORTED;
+  if (R == 0) return GDN_OK;
+  if (!ssm_indices) return GDN_EINVAL;
+  gdn_host::DecodeArgs d{};
+  const int rc = decode_common(q, k, v, g, beta, A_log, a, b, dt_bias, scale, use_qk_l2norm, ssm_pool, H, HV,
+                               K, V, o, d);
+  if (rc != GDN_OK) return rc;
+  d.pool = ssm_pool; d.pool_bf16 = 1; d.P = P;
+  d.cu = nullptr; d.N = R; d.Ttot = R;
+  d.read_idx = ssm_indices; d.write_idx = ssm_indices; d.ld = 1; d.num_acc = nullptr;
+  d.o = o; d.dev_status = dev_status;
+  return cuda_status(gdn_host::launch_decode_general(d, static_cast<cudaStream_t>(stream)));
+}
+
+int gdn_recurrent_decode_mtp(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *g,
+                             const float *beta, const float *A_log, const uint16_t *a, const uint16_t *b,
+                             const float *dt_bias, float scale, int use_qk_l2norm, float *ssm_pool, int P,
+                             const int32_t *cu_seqlens, int N, int Ttot, const int32_t *read_indices,
+                             const int32_t *write_indices, int ld, const int32_t *num_accepted_tokens, int H,
+                             int HV, int K, int V, uint16_t *o, int32_t *dev_status, void *stream) {
+  if (N < 0 || P < 0 || Ttot < 0 || ld <= 0) return GDN_EINVAL;
+  if (H <= 0 || HV <= 0 || K <= 0 || V <= 0 || HV % H != 0) return GDN_EINVAL;
+  if (!head_dim_ok(K) || !head_dim_ok(V)) return GDN_EUNSUPPORTED;
+  if (N == 0) return GDN_OK;
+  if (N > 65535) return GDN_EUNSUPPORTED;
+  if (!cu_seqlens || !read_indices || !write_indices) return GDN_EINVAL;
+  if (Ttot == 0) return GDN_OK;
+  gdn_host::DecodeArgs d{};
+  const int rc = decode_common(q, k, v, g, beta, A_log, a, b, dt_bias, scale, use_qk_l2norm, ssm_pool, H, HV,
+                               K, V, o, d);
+  if (rc != GDN_OK) return rc;
+  d.pool = ssm_pool; d.pool_bf16 = 0; d.P = P;
+  d.cu = cu_seqlens; d.N = N; d.Ttot = Ttot;
+  d.read_idx = read_indices; d.write_idx = write_indices; d.ld = ld; d.num_acc = num_accepted_tokens;
+  d.o = o; d.dev_status = dev_status;
+  return cuda_status(gdn_host::launch_decode_general(d, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -47,13 +47,30 @@ cudaError_t launch_gating(const float *A_log, const uint16_t *a,
                           const uint16_t *b, const float *dt_bias,
                           int64_t Ttok, int HV, float *g, float *beta,
                           cudaStream_t s);
-cudaError_t launch_decode(const uint16_t *q, const uint16_t *k,
-                          const uint16_t *v, const float *g, const float *beta,
-                          const float *A_log, const uint16_t *a,
-                          const uint16_t *b, const float *dt_bias, float scale,
-                          int l2, float *pool, int P, const int32_t *idx, int R,
-                          int H, int HV, int K, int V, uint16_t *o,
-                          int32_t *dev_status, cudaStream_t s);
+// Recurrent decode over N requests: request n owns tokens [cu[n], cu[n+1])
+// (token n when cu is NULL), starts from pool[read_idx[n*ld + num_acc[n]-1]]
+// (column 0 when num_acc is NULL) and stores the state after its i-th token
+// into pool[write_idx[n*ld + i]].  pool is float* or bf16 (uint16_t*).
+struct DecodeArgs {
+  const uint16_t *q, *k, *v;
+  const float *g, *beta, *A_log;
+  const uint16_t *a, *b;
+  const float *dt_bias;
+  float scale;
+  int l2;
+  void *pool;
+  int pool_bf16;
+  int P;
+  const int32_t *cu;
+  int N, Ttot;
+  const int32_t *read_idx, *write_idx;
+  int ld;
+  const int32_t *num_acc;
+  int H, HV, K, V;
+  uint16_t *o;
+  int32_t *dev_status;
+};
+cudaError_t launch_decode_general(const DecodeArgs &a, cudaStream_t s);
 struct ChunkArgs {
   const uint16_t *q, *k, *v;
   const float *g, *beta;

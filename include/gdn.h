@@ -158,6 +158,56 @@ int gdn_recurrent_decode(const uint16_t *q, const uint16_t *k,
                          void *stream);
 
 /*
+ * gdn_recurrent_decode_bf16 -- gdn_recurrent_decode against a state pool
+ * stored in bf16 (ssm_pool: uint16_t bit patterns, [P, HV, K, V]), half the
+ * state bytes of the fp32 pool (the bf16 state-pool variant of the LightLLM
+ * "gdn.py" backend's ssm cache).  The step runs in fp32 on the stored values;
+ * o is computed from the updated fp32 state, which is then rounded to bf16
+ * (to nearest, ties to even) when stored.  Everything else as
+ * gdn_recurrent_decode.
+ */
+int gdn_recurrent_decode_bf16(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                              const float *g, const float *beta, const float *A_log,
+                              const uint16_t *a, const uint16_t *b, const float *dt_bias,
+                              float scale, int use_qk_l2norm, uint16_t *ssm_pool, int P,
+                              const int32_t *ssm_indices, int R, int H, int HV, int K, int V,
+                              uint16_t *o, int32_t *dev_status, void *stream);
+
+/*
+ * gdn_recurrent_decode_mtp -- multi-token (speculative / MTP) decode against
+ * the fp32 state pool.  LightLLM "gdn.py", MTP decode path: each request
+ * carries up to ld (= mtp_step + 1) tokens packed by cu_seqlens; it starts from
+ * the state in slot read_indices[n][num_accepted_tokens[n] - 1] (the state
+ * after the last token accepted in the previous step), runs the recurrence
+ * over its tokens, and stores the state after its i-th token into slot
+ * write_indices[n][i].
+ *
+ *   q, k          : bf16 [Ttot, H, K];  v : bf16 [Ttot, HV, V]
+ *   gates         : g, beta fp32 [Ttot, HV], or A_log, a, b, dt_bias as in
+ *                   gdn_recurrent_decode (a, b bf16 [Ttot, HV])
+ *   ssm_pool      : fp32 [P, HV, K, V], read and written in place
+ *   cu_seqlens    : int32 [N + 1] device offsets (0 <= cu[n] <= cu[n+1] <= Ttot,
+ *                   at most ld tokens per request; else GDN_DEV_BAD_CU_SEQLENS
+ *                   and the request is skipped)
+ *   read_indices, write_indices : int32 [N, ld]; a read slot of -1 is a PAD
+ *                   request (zero output rows, nothing stored); a write slot
+ *                   of -1 stores nothing; other values outside [0, P) set
+ *                   GDN_DEV_BAD_SLOT (read: treated as PAD; write: skipped)
+ *   num_accepted_tokens : int32 [N] in [1, ld], or NULL (read column 0)
+ *   o             : bf16 [Ttot, HV, V]
+ * The read slot is loaded before any store of the request, so it may also be
+ * one of its write slots.  Requests must not share slots.  One launch.
+ */
+int gdn_recurrent_decode_mtp(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                             const float *g, const float *beta, const float *A_log,
+                             const uint16_t *a, const uint16_t *b, const float *dt_bias,
+                             float scale, int use_qk_l2norm, float *ssm_pool, int P,
+                             const int32_t *cu_seqlens, int N, int Ttot,
+                             const int32_t *read_indices, const int32_t *write_indices, int ld,
+                             const int32_t *num_accepted_tokens, int H, int HV, int K, int V,
+                             uint16_t *o, int32_t *dev_status, void *stream);
+
+/*
  * gdn_chunk_fwd_noalloc -- gdn_chunk_fwd for callers that cannot allocate
  * device memory at call time (a serving runtime that reserves all device
  * memory for its own pool at start-up and forbids later cudaMalloc, or a hot

@@ -141,3 +141,31 @@ def test_conv_host_validation(lib):
     assert pack(q=NULL) == gdn.GDN_EINVAL
     assert pack(H=0) == gdn.GDN_EINVAL
     assert pack(S=1) == gdn.GDN_EUNSUPPORTED
+
+
+def test_decode_variants_host_validation(lib):
+    NULL = None
+    fake = ctypes.c_void_p(16)
+    F = ctypes.c_float
+
+    def bf16(pool=fake, idx=fake, R=2, K=128, g=fake):
+        return lib.gdn_recurrent_decode_bf16(fake, fake, fake, g, fake, NULL, NULL, NULL, NULL, F(-1.0), 1, pool,
+                                             4, idx, R, 2, 4, K, 128, fake, NULL, NULL)
+
+    assert bf16(R=0) == gdn.GDN_OK
+    assert bf16(pool=NULL) == gdn.GDN_EINVAL
+    assert bf16(idx=NULL) == gdn.GDN_EINVAL
+    assert bf16(K=96) == gdn.GDN_EUNSUPPORTED
+    assert bf16(g=NULL) == gdn.GDN_EINVAL                      # half a gate group
+
+    def mtp(cu=fake, rd=fake, wr=fake, N=2, Tt=6, ld=3, pool=fake):
+        return lib.gdn_recurrent_decode_mtp(fake, fake, fake, fake, fake, NULL, NULL, NULL, NULL, F(-1.0), 1,
+                                            pool, 8, cu, N, Tt, rd, wr, ld, NULL, 2, 4, 64, 64, fake, NULL, NULL)
+
+    assert mtp(N=0) == gdn.GDN_OK
+    assert mtp(cu=NULL) == gdn.GDN_EINVAL
+    assert mtp(rd=NULL) == gdn.GDN_EINVAL
+    assert mtp(wr=NULL) == gdn.GDN_EINVAL
+    assert mtp(ld=0) == gdn.GDN_EINVAL
+    assert mtp(pool=NULL) == gdn.GDN_EINVAL
+    assert mtp(N=70000) == gdn.GDN_EUNSUPPORTED
