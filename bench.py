@@ -300,6 +300,7 @@ def run_ours(args, rank, world, local_rank):
         line["decode"] = bench_decode(dev, stream, hbm, args)
         line["gating"] = bench_gating(dev, stream, hbm, args)
         line["conv1d"] = bench_conv(dev, stream, hbm, args)
+        line["decode_variants"] = bench_decode_variants(dev, stream, hbm, args)
         line["e2e"] = bench_e2e(case, dev, stream, args, world)
         if rank == 0 and world == 1:
             gg, bb = gates_for_cpu(case)
@@ -354,6 +355,66 @@ def bench_decode(dev, stream, hbm, args):
     return {"workload": "decode R=256 (valid %d) pool [512,32,128,128] fp32, fused gating" % valid,
             "ms": ms, "state_GBps": state_b / (ms / 1e3) / 1e9, "achieved_GBps": gbs, "peak": hbm,
             "frac": gbs / hbm, "requests_per_s": dc.R / (ms / 1e3), "l2_flush": "256 MB memset before each call"}
+
+
+def _timed_flush(dev, stream, call, reps):
+    import torch
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)  # 256 MB > L2
+    for _ in range(3):
+        call()
+    times = []
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(e0.elapsed_time(e1))
+    return statistics.median(times)
+
+
+def bench_decode_variants(dev, stream, hbm, args):
+    """The bf16 state pool on the batched-decode workload, and a multi-token
+    (MTP, 4 tokens per request) decode of 64 requests with the same heads."""
+    import torch
+    import gated_deltanet_chunked_chunk_gb300 as gdn
+    from gated_deltanet_chunked_chunk_gb300 import workloads as W
+    dc = W.config4()
+    d = lambda t: t.to(dev).contiguous()
+    q, k, v, idx = d(dc.q), d(dc.k), d(dc.v), d(dc.ssm_indices)
+    A_log, a, b, dt = d(dc.A_log), d(dc.a), d(dc.b), d(dc.dt_bias)
+    pool16 = d(dc.ssm_pool.to(torch.bfloat16))
+    o = torch.empty(dc.R, 1, dc.HV, dc.V, dtype=torch.bfloat16, device=dev)
+    ms16 = _timed_flush(dev, stream, lambda: gdn.gdn_recurrent_decode_bf16(
+        q, k, v, pool16, idx, A_log=A_log, a=a, b=b, dt_bias=dt, o=o), max(args.steps, 10))
+    valid = int((dc.ssm_indices >= 0).sum())
+    b16 = 2 * valid * dc.HV * dc.K * dc.V * 2 + dc.R * (2 * dc.H * dc.K * 2 + dc.HV * dc.V * 2 * 2 + dc.HV * 4)
+    del pool16
+    # MTP: 64 requests x 4 tokens, request n owns slots 4n .. 4n+3, 2 accepted last step.
+    N, ld, H, HV, K, V = 64, 4, dc.H, dc.HV, dc.K, dc.V
+    gen = torch.Generator().manual_seed(24)
+    Tt = N * ld
+    qm = d(torch.randn(Tt, H, K, generator=gen).to(torch.bfloat16))
+    km = d(torch.randn(Tt, H, K, generator=gen).to(torch.bfloat16))
+    vm = d(torch.randn(Tt, HV, V, generator=gen).to(torch.bfloat16))
+    am = d(torch.randn(Tt, HV, generator=gen).to(torch.bfloat16))
+    bm = d(torch.randn(Tt, HV, generator=gen).to(torch.bfloat16))
+    poolm = torch.randn(N * ld, HV, K, V, generator=gen, device="cpu").mul_(0.1).to(dev)
+    slots = d((torch.arange(N, dtype=torch.int32)[:, None] * ld + torch.arange(ld, dtype=torch.int32)[None, :]))
+    cu = d(torch.arange(0, Tt + 1, ld, dtype=torch.int32))
+    acc = d(torch.full((N,), 2, dtype=torch.int32))
+    om = torch.empty(Tt, HV, V, dtype=torch.bfloat16, device=dev)
+    msm = _timed_flush(dev, stream, lambda: gdn.gdn_recurrent_decode_mtp(
+        qm, km, vm, poolm, cu, slots, slots, acc, A_log=A_log, a=am, b=bm, dt_bias=dt, o=om), max(args.steps, 10))
+    bm_ = N * HV * K * V * 4 * (1 + ld) + Tt * (2 * H * K * 2 + HV * V * 2 * 2 + HV * 4)
+    return {"bf16_pool": {"workload": "decode R=256 (valid %d) pool [512,32,128,128] bf16, fused gating" % valid,
+                          "ms": ms16, "achieved_GBps": b16 / (ms16 / 1e3) / 1e9, "peak": hbm,
+                          "frac": b16 / (ms16 / 1e3) / 1e9 / hbm, "requests_per_s": dc.R / (ms16 / 1e3)},
+            "mtp": {"workload": f"MTP decode {N} requests x {ld} tokens, fp32 pool [{N * ld},32,128,128], "
+                                "state read once and stored after every token",
+                    "ms": msm, "achieved_GBps": bm_ / (msm / 1e3) / 1e9, "peak": hbm,
+                    "frac": bm_ / (msm / 1e3) / 1e9 / hbm, "tokens_per_s": Tt / (msm / 1e3)}}
 
 
 def bench_gating(dev, stream, hbm, args):
