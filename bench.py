@@ -192,6 +192,28 @@ def workload_config(case, note=""):
             "l2_flush": "inputs larger than L2 (1.6 GB vs 129 MB)", "note": note}
 
 
+# ------------------------------------------------------------ rank helpers
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The slowest rank's value (all ranks get it).  The step time of a
+    multi-GPU run is the max over ranks; every rank runs a full replica, so
+    there is no exchange on the data path, only this one reduction."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64,
+                     device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Units per second of the whole job: every rank processes units_per_rank
+    per step (weak scaling), the step lasts the slowest rank's time."""
+    return units_per_rank * world / (ms_per_step / 1e3)
+
+
 # ---------------------------------------------------------------------- ours
 
 def run_ours(args, rank, world, local_rank):
@@ -258,13 +280,10 @@ def run_ours(args, rank, world, local_rank):
     clk = clocks.stop()
     ms = t_start.elapsed_time(t_end)
     chunk_ms = [a_.elapsed_time(b_) for a_, b_ in evs]
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     ms_per_step = ms / args.steps
     tokens = B * T
-    value = tokens * world / (ms_per_step / 1e3)
+    value = whole_job_rate(tokens, world, ms_per_step)
 
     chunk_avg_ms = sum(chunk_ms) / len(chunk_ms)
     alg_b = prefill_bytes(B, T, H, HV, K, V, N)
