@@ -24,7 +24,7 @@ import torch
 __all__ = ["gdn_gating", "gdn_chunk_fwd", "gdn_recurrent_decode", "chunk_fwd_workspace_size",
            "gdn_chunk_fwd_noalloc", "NOALLOC_SCRATCH_BYTES", "gdn_causal_conv1d_fwd",
            "gdn_causal_conv1d_update", "gdn_conv_decode_pack", "gdn_recurrent_decode_bf16",
-           "gdn_recurrent_decode_mtp",
+           "gdn_recurrent_decode_mtp", "gdn_chunk_bwd", "chunk_bwd_workspace_size",
            "GDNError", "lib_path", "load_library", "status_string", "DEV_BAD_CU_SEQLENS",
            "DEV_BAD_SLOT", "DEV_WAIT_TIMEOUT", "EXPORTED_SYMBOLS"]
 
@@ -40,7 +40,8 @@ DEV_BAD_CU_SEQLENS, DEV_BAD_SLOT, DEV_WAIT_TIMEOUT = 1, 2, 4
 EXPORTED_SYMBOLS = ("gdn_status_string", "gdn_version", "gdn_gating", "gdn_chunk_fwd_workspace_size",
                     "gdn_chunk_fwd", "gdn_recurrent_decode", "gdn_chunk_fwd_noalloc",
                     "gdn_causal_conv1d_fwd", "gdn_causal_conv1d_update", "gdn_conv_decode_pack",
-                    "gdn_recurrent_decode_bf16", "gdn_recurrent_decode_mtp")
+                    "gdn_recurrent_decode_bf16", "gdn_recurrent_decode_mtp", "gdn_chunk_bwd_workspace_size",
+                    "gdn_chunk_bwd")
 
 #: Size of the fixed scratch buffer behind gdn_chunk_fwd_noalloc (bytes).
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -94,6 +95,11 @@ def load_library():
         lib.gdn_recurrent_decode_mtp.argtypes = [P, P, P, P, P, P, P, P, P, F, I, P, I, P, I, I, P, P, I, P,
                                                  I, I, I, I, P, P, P]
         lib.gdn_recurrent_decode_mtp.restype = I
+        lib.gdn_chunk_bwd_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
+        lib.gdn_chunk_bwd_workspace_size.restype = SZ
+        lib.gdn_chunk_bwd.argtypes = [P, P, P, P, P, F, P, P, I, I, I, I, I, I, I, I, P, P, P, P, P, P, P, P,
+                                      P, SZ, P, P]
+        lib.gdn_chunk_bwd.restype = I
         _lib = lib
         return lib
 
@@ -475,3 +481,46 @@ def gdn_recurrent_decode_mtp(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, 
     if rc != GDN_OK:
         raise GDNError("gdn_recurrent_decode_mtp", rc)
     return o
+
+
+# ----------------------------------------------------------------- backward
+def chunk_bwd_workspace_size(B, T, H, HV, K, V, N, varlen) -> int:
+    return int(load_library().gdn_chunk_bwd_workspace_size(B, T, H, HV, K, V, N, int(bool(varlen))))
+
+
+def gdn_chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
+                  do: torch.Tensor, scale=None, initial_state: Optional[torch.Tensor] = None,
+                  cu_seqlens: Optional[torch.Tensor] = None, dht: Optional[torch.Tensor] = None,
+                  use_qk_l2norm: bool = True, workspace: Optional[torch.Tensor] = None,
+                  dev_status: Optional[torch.Tensor] = None):
+    """Gradients of gdn_chunk_fwd; see include/gdn.h.  Returns
+    (dq, dk, dv, dg, dbeta, dh0) as fp32 tensors (dh0 None without initial_state)."""
+    dev = q.device
+    _check(q, "q", torch.bfloat16, dev, 4)
+    _check(k, "k", torch.bfloat16, dev, 4)
+    _check(v, "v", torch.bfloat16, dev, 4)
+    _check(g, "g", torch.float32, dev, 3)
+    _check(beta, "beta", torch.float32, dev, 3)
+    _check(do, "do", torch.bfloat16, dev, 4)
+    _check(initial_state, "initial_state", torch.float32, dev, 4)
+    _check(dht, "dht", torch.float32, dev, 4)
+    _check(cu_seqlens, "cu_seqlens", torch.int32, dev, 1)
+    B, T, H, K = q.shape
+    HV, V = v.shape[2], v.shape[3]
+    N = (cu_seqlens.shape[0] - 1) if cu_seqlens is not None else B
+    dq = torch.empty(B, T, H, K, dtype=torch.float32, device=dev)
+    dk = torch.empty_like(dq)
+    dv = torch.empty(B, T, HV, V, dtype=torch.float32, device=dev)
+    dg = torch.empty(B, T, HV, dtype=torch.float32, device=dev)
+    dbeta = torch.empty_like(dg)
+    dh0 = torch.empty(N, HV, K, V, dtype=torch.float32, device=dev) if initial_state is not None else None
+    need = chunk_bwd_workspace_size(B, T, H, HV, K, V, N, cu_seqlens is not None)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    rc = load_library().gdn_chunk_bwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _scale_arg(scale), _ptr(initial_state), _ptr(cu_seqlens),
+        N, B, T, H, HV, K, V, int(bool(use_qk_l2norm)), _ptr(do), _ptr(dht), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg),
+        _ptr(dbeta), _ptr(dh0), _ptr(workspace), workspace.numel(), _ptr(dev_status), _stream(dev))
+    if rc != GDN_OK:
+        raise GDNError("gdn_chunk_bwd", rc)
+    return dq, dk, dv, dg, dbeta, dh0

@@ -63,7 +63,7 @@ int gdn_chunk_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
   const size_t need = gdn_host::chunk_workspace_bytes(B, T, H, HV, K, V, N, cu_seqlens != nullptr);
   if (need > 0 && (!workspace || workspace_bytes < need)) return GDN_EWORKSPACE;
   if (!(scale > 0.f)) scale = 1.f / sqrtf((float)K);  // also catches NaN
-  gdn_host::ChunkArgs a;
+  gdn_host::ChunkArgs a{};
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.scale = scale;
   a.h0 = initial_state; a.cu = cu_seqlens;
   a.N = N; a.B = B; a.T = T; a.H = H; a.HV = HV; a.K = K; a.V = V;
@@ -71,6 +71,39 @@ int gdn_chunk_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
   a.o = o; a.ht = final_state; a.ws = workspace; a.ws_bytes = workspace_bytes;
   a.dev_status = dev_status;
   return cuda_status(gdn_host::launch_chunk(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t gdn_chunk_bwd_workspace_size(int B, int T, int H, int HV, int K, int V, int N, int varlen) {
+  if ((K != 64 && K != 128) || (V != 64 && V != 128) || B < 0 || T < 0 || HV <= 0 || N < 0) return 0;
+  return gdn_host::chunk_bwd_workspace_bytes(B, T, H, HV, K, V, N, varlen);
+}
+
+int gdn_chunk_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *g, const float *beta,
+                  float scale, const float *initial_state, const int32_t *cu_seqlens, int N, int B, int T, int H,
+                  int HV, int K, int V, int use_qk_l2norm, const uint16_t *dout, const float *dht, float *dq,
+                  float *dk, float *dv, float *dg, float *dbeta, float *dh0, void *workspace,
+                  size_t workspace_bytes, int32_t *dev_status, void *stream) {
+  if (B < 0 || T < 0 || H <= 0 || HV <= 0 || K <= 0 || V <= 0 || N < 0) return GDN_EINVAL;
+  if (HV % H != 0) return GDN_EINVAL;
+  if (cu_seqlens) {
+    if (B != 1) return GDN_EINVAL;
+  } else if (N != B) {
+    return GDN_EINVAL;
+  }
+  if (!head_dim_ok(K) || !head_dim_ok(V)) return GDN_EUNSUPPORTED;
+  const bool has_tokens = (int64_t)B * T > 0;
+  if (has_tokens && (!q || !k || !v || !g || !beta || !dout || !dq || !dk || !dv || !dg || !dbeta))
+    return GDN_EINVAL;
+  if (N == 0) return GDN_OK;
+  const size_t need = gdn_host::chunk_bwd_workspace_bytes(B, T, H, HV, K, V, N, cu_seqlens != nullptr);
+  if (!workspace || workspace_bytes < need) return GDN_EWORKSPACE;
+  if (!(scale > 0.f)) scale = 1.f / sqrtf((float)K);
+  gdn_host::ChunkBwdArgs a{};
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.scale = scale; a.h0 = initial_state; a.cu = cu_seqlens;
+  a.N = N; a.B = B; a.T = T; a.H = H; a.HV = HV; a.K = K; a.V = V; a.l2 = use_qk_l2norm ? 1 : 0;
+  a.dout = dout; a.dht = dht; a.dq = dq; a.dk = dk; a.dv = dv; a.dg = dg; a.dbeta = dbeta; a.dh0 = dh0;
+  a.ws = workspace; a.ws_bytes = workspace_bytes; a.dev_status = dev_status;
+  return cuda_status(gdn_host::launch_chunk_bwd(a, static_cast<cudaStream_t>(stream)));
 }
 
 namespace {

@@ -47,34 +47,19 @@
 
 #include <mutex>
 
+#include "gdn_chunk_shared.cuh"
 #include "gdn_common.cuh"
 #include "gdn_sm103.cuh"
 
 namespace {
 
 using namespace gdn;
+using namespace gdnc;
 
-constexpr int C = 64;
 constexpr int VT = 32;
 constexpr int NW = 8;
 constexpr int NTH = NW * 32;
-constexpr long long kWaitLimit = 2000000000LL;  // clock cycles (about 1 s) before a wait gives up
 constexpr int FROW = 68;                        // floats per padded fp32 row of 64
-constexpr float kLog2e = 1.4426950408889634f;
-
-// Per-(chunk, value head) record, byte offsets; also its shared-memory image.
-template <int K>
-struct Rec {
-  static constexpr int KA = K / 64;
-  static constexpr int W = 0;               // [64][K] bf16, 64-key SW128 atom columns
-  static constexpr int PH = KA * 8192;      // [64][64] bf16 SW128
-  static constexpr int PL = PH + 8192;
-  static constexpr int TS = PL + 8192;
-  static constexpr int SC = TS + 8192;      // og[64], sv[64], beta[64], e^{gamma_L} (fp32)
-  static constexpr int BYTES = SC + 1024;
-  static_assert(BYTES % 1024 == 0, "record alignment");
-};
-enum { RS_OG = 0, RS_SV = 64, RS_BET = 128, RS_DL = 192 };
 
 // [K; Q] tile as two TMA boxes per 64-key atom column: rows 0-63 K, 64-127 Q.
 template <int K>
@@ -90,12 +75,6 @@ __device__ __forceinline__ unsigned char *align1024(unsigned char *p) {
 // [rows][K] bf16 tile stored as 64-key SW128 atom columns of `rows` rows.
 __device__ __forceinline__ uint32_t tile_addr(uint32_t base, int rows, int row, int kc) {
   return base + (kc >> 3) * (rows * 128) + sw128(row, kc & 7);
-}
-// 2^x with the hardware approximation (relative error around 2^-22).
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
 }
 // acc (16 x 16 as two 16x8 tiles) += A (16 x 16) * B (16 x 16), fp32 row-major in
 // shared memory; fp32 bits go straight to the tf32 unit (low mantissa bits ignored).
@@ -123,32 +102,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
-}
-
-// Sequence bounds (dense or cu_seqlens); false for offsets that break the rules.
-__device__ __forceinline__ bool seq_bounds(const int32_t *cu, int n, int T, int64_t &tok0, int64_t &len) {
-  if (cu) {
-    const int32_t a0 = cu[n], a1 = cu[n + 1];
-    if (a0 < 0 || a1 < a0 || a1 > T || (n == 0 && a0 != 0)) return false;
-    tok0 = a0;
-    len = a1 - a0;
-  } else {
-    tok0 = static_cast<int64_t>(n) * T;
-    len = T;
-  }
-  return true;
-}
-__device__ __forceinline__ int chunks_of(int64_t len) { return static_cast<int>((len + C - 1) / C); }
-// Index of the first chunk of sequence n in the workspace: sum of the chunk
-// counts of the sequences before it (offsets that break the rules count 0).
-__device__ __forceinline__ int64_t chunk_base(const int32_t *cu, int n, int T) {
-  if (!cu) return static_cast<int64_t>(n) * chunks_of(T);
-  int64_t b = 0;
-  for (int m = 0; m < n; ++m) {
-    int64_t t0, l0;
-    if (seq_bounds(cu, m, T, t0, l0)) b += chunks_of(l0);
-  }
-  return b;
 }
 
 // ============================================================== prep kernel
@@ -589,7 +542,7 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, float scale, const float *__restrict__ h0,
     const int32_t *__restrict__ cu, int T, int H, int HV, int V, const unsigned char *__restrict__ ws,
-    uint16_t *__restrict__ o, float *__restrict__ ht, int32_t *dev_status) {
+    uint16_t *__restrict__ o, float *__restrict__ ht, float *__restrict__ hsave, int32_t *dev_status) {
   using Ly = WalkLay<K>;
   using R = Rec<K>;
   constexpr int KA = K / 64;
@@ -747,7 +700,7 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
         uint32_t a[16];
         tmem_ld16_issue(tl + Ly::ACC3 + 16 * hs, a);
         tmem_ld_wait16(a);
-        if (i < chunk_rows(c)) {
+        if (o && i < chunk_rows(c)) {
           const float *x = X + i * XROW + 16 * hs;
           const int64_t trow = tok0 + static_cast<int64_t>(c) * C + i;
           uint4 *dst = reinterpret_cast<uint4 *>(o + (trow * HV + hv) * V + vt0 + 16 * hs);
@@ -791,6 +744,12 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
       const uint32_t st = sb + s * Ly::STAGE;
       const unsigned char *stp = sm + s * Ly::STAGE;
       const float *rsc = reinterpret_cast<const float *>(stp + SCO);
+      if (hsave && krow) {
+        // The state entering chunk c (the backward pass reads it back).
+        float *dst = hsave + ((((cb + c) * HV + hv) * K + r) * V + vt0 + 16 * hs);
+#pragma unroll
+        for (int j = 0; j < 16; j += 4) *reinterpret_cast<float4 *>(dst + j) = make_float4(hr[j], hr[j + 1], hr[j + 2], hr[j + 3]);
+      }
       go = waitc(FULL, c) && go;  // also: the output product of chunk c - 1 is done
       // [W; Q] [h_hi | h_lo]: warp p < 4 takes k-steps [p KA, p KA + KA).
       if (warp < 4 && lane == 0 && go) {
@@ -998,11 +957,6 @@ bool make_map(CUtensorMap *m, const void *ptr, int dim, int heads, int64_t rows,
   return r == CUDA_SUCCESS;
 }
 
-int64_t total_chunk_slots(int B, int T, int N, bool varlen) {
-  const int64_t per = (static_cast<int64_t>(T) + C - 1) / C;
-  return varlen ? per + N : static_cast<int64_t>(B) * per;
-}
-
 template <int K>
 size_t ws_bytes(int B, int T, int HV, int N, bool varlen) {
   return static_cast<size_t>(total_chunk_slots(B, T, N, varlen)) * HV * Rec<K>::BYTES;
@@ -1036,7 +990,8 @@ cudaError_t launch_k(const gdn_host::ChunkArgs &a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   dim3 grid(a.V / VT, a.HV, a.N);
   chunk_walk_kernel<K><<<grid, WALK_THREADS, wsmem, s>>>(mq, mk, mv, a.scale, a.h0, a.cu, a.T, a.H, a.HV, a.V,
-                                                static_cast<const unsigned char *>(a.ws), a.o, a.ht, a.dev_status);
+                                                static_cast<const unsigned char *>(a.ws), a.o, a.ht, a.hsave,
+                                                a.dev_status);
   return cudaGetLastError();
 }
 

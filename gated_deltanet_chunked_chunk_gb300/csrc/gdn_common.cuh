@@ -78,8 +78,9 @@ struct ChunkArgs {
   const float *h0;
   const int32_t *cu;
   int N, B, T, H, HV, K, V, l2;
-  uint16_t *o;
+  uint16_t *o;   // may be NULL (no output written)
   float *ht;
+  float *hsave;  // NULL, or [chunk slots][HV][K][V]: the state entering every chunk
   void *ws;
   size_t ws_bytes;
   int32_t *dev_status;
@@ -87,4 +88,20 @@ struct ChunkArgs {
 size_t chunk_workspace_bytes(int B, int T, int H, int HV, int K, int V, int N,
                              int varlen);
 cudaError_t launch_chunk(const ChunkArgs &a, cudaStream_t s);
+struct ChunkBwdArgs {
+  const uint16_t *q, *k, *v;
+  const float *g, *beta;
+  float scale;
+  const float *h0;
+  const int32_t *cu;
+  int N, B, T, H, HV, K, V, l2;
+  const uint16_t *dout;
+  const float *dht;
+  float *dq, *dk, *dv, *dg, *dbeta, *dh0;
+  void *ws;
+  size_t ws_bytes;
+  int32_t *dev_status;
+};
+size_t chunk_bwd_workspace_bytes(int B, int T, int H, int HV, int K, int V, int N, int varlen);
+cudaError_t launch_chunk_bwd(const ChunkBwdArgs &a, cudaStream_t s);
 }  // namespace gdn_host

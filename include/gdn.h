@@ -158,6 +158,39 @@ int gdn_recurrent_decode(const uint16_t *q, const uint16_t *k,
                          void *stream);
 
 /*
+ * gdn_chunk_bwd_workspace_size -- bytes of device workspace gdn_chunk_bwd
+ * needs (the forward's records plus two fp32 states per chunk and value head).
+ */
+size_t gdn_chunk_bwd_workspace_size(int B, int T, int H, int HV, int K, int V,
+                                    int N, int varlen);
+
+/*
+ * gdn_chunk_bwd -- gradients of gdn_chunk_fwd for training ("NPU Training
+ * Operators - GDN" pairs the chunked forward with a backward returning the
+ * gradients of q, k, v, beta, g and the initial state).  Reverse-mode
+ * differentiation of the same operation as gdn_chunk_fwd: given the gradient
+ * of the output do and (optionally) of the final state dht, it returns
+ *   dq, dk        : fp32 [B, T, H, K]   (summed over the value heads of a group)
+ *   dv            : fp32 [B, T, HV, V]
+ *   dg, dbeta     : fp32 [B, T, HV]
+ *   dh0           : fp32 [N, HV, K, V], or NULL to skip
+ * Inputs as gdn_chunk_fwd (same shapes, scale, initial_state, cu_seqlens,
+ * use_qk_l2norm); do: bf16 [B, T, HV, V]; dht: fp32 [N, HV, K, V] or NULL
+ * (zero).  The forward is recomputed inside (the call saves the state
+ * entering every chunk in the workspace), then the state gradients run last
+ * chunk first, then the per-chunk gradients in parallel: four launches plus
+ * two memsets of dq, dk on `stream`.  Errors as gdn_chunk_fwd; the workspace
+ * must hold gdn_chunk_bwd_workspace_size() bytes.
+ */
+int gdn_chunk_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                  const float *g, const float *beta, float scale,
+                  const float *initial_state, const int32_t *cu_seqlens, int N,
+                  int B, int T, int H, int HV, int K, int V, int use_qk_l2norm,
+                  const uint16_t *dout, const float *dht, float *dq, float *dk,
+                  float *dv, float *dg, float *dbeta, float *dh0, void *workspace,
+                  size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/*
  * gdn_recurrent_decode_bf16 -- gdn_recurrent_decode against a state pool
  * stored in bf16 (ssm_pool: uint16_t bit patterns, [P, HV, K, V]), half the
  * state bytes of the fp32 pool (the bf16 state-pool variant of the LightLLM
