@@ -320,6 +320,7 @@ def run_ours(args, rank, world, local_rank):
         line["gating"] = bench_gating(dev, stream, hbm, args)
         line["conv1d"] = bench_conv(dev, stream, hbm, args)
         line["decode_variants"] = bench_decode_variants(dev, stream, hbm, args)
+        line["backward"] = bench_backward(dev, stream, args)
         line["e2e"] = bench_e2e(case, dev, stream, args, world)
         if rank == 0 and world == 1:
             gg, bb = gates_for_cpu(case)
@@ -508,6 +509,44 @@ def bench_conv(dev, stream, hbm, args):
             "decode": {"workload": f"conv1d update R={R} (valid {valid}) x {dimd} channels, pool "
                                    f"{tuple(sd.shape)} bf16", "us": ms_d * 1e3,
                        "achieved_GBps": bytes_d / (ms_d / 1e3) / 1e9}}
+
+
+def bench_backward(dev, stream, args):
+    """gdn_chunk_bwd on the dense prefill (B=2, T=4096, H=16, HV=32, K=V=128,
+    initial state and final-state gradient): forward recompute, state-gradient
+    walk and per-chunk gradients, timed together."""
+    import torch
+    import gated_deltanet_chunked_chunk_gb300 as gdn
+    from gated_deltanet_chunked_chunk_gb300 import workloads as W
+    case = W.config1()
+    d = lambda t: t.to(dev).contiguous()
+    g, beta = gdn.gdn_gating(d(case.A_log), d(case.a), d(case.b), d(case.dt_bias))
+    g = g.view(case.B, case.T, case.HV)
+    beta = beta.view(case.B, case.T, case.HV)
+    gen = torch.Generator().manual_seed(31)
+    do = d(torch.randn(case.B, case.T, case.HV, case.V, generator=gen).to(torch.bfloat16))
+    dht = d(torch.randn(case.N, case.HV, case.K, case.V, generator=gen))
+    q, k, v, h0 = d(case.q), d(case.k), d(case.v), d(case.initial_state)
+    need = gdn.chunk_bwd_workspace_size(case.B, case.T, case.H, case.HV, case.K, case.V, case.N, False)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+
+    def call():
+        gdn.gdn_chunk_bwd(q, k, v, g, beta, do, initial_state=h0, dht=dht, workspace=ws)
+    for _ in range(3):
+        call()
+    times = []
+    for _ in range(max(args.steps, 5)):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(e0.elapsed_time(e1))
+    ms = statistics.median(times)
+    tokens = case.B * case.T
+    return {"workload": f"backward B={case.B} T={case.T} H={case.H} HV={case.HV} K={case.K} V={case.V}, "
+                        "initial state, final-state gradient, forward recomputed inside",
+            "ms": ms, "tokens_per_s": tokens / (ms / 1e3)}
 
 
 def bench_e2e(case, dev, stream, args, world):

@@ -77,3 +77,29 @@ def test_bwd_varlen_with_empty_sequence():
     case = W.prefill_case("bwd_var", 44, 1, sum(lengths), 2, 4, 128, 64, init="all",
                           cu_seqlens=W.cu_from_lengths(lengths))
     _run(case, seed=4)
+
+
+def test_bwd_qwen_heads_sampled_group():
+    # H=16, HV=32, K=V=128, T=1024 with initial and final-state gradients; the
+    # oracle runs on one key-head group (key head 5, value heads 10 and 11),
+    # whose gradients do not depend on the other heads.
+    import gated_deltanet_chunked_chunk_gb300 as gdn
+    case = W.prefill_case("bwd_qwen", 45, 1, 1024, 16, 32, 128, 128, init="all")
+    g, beta = P.oracle_gates(case)
+    gen = torch.Generator().manual_seed(1045)
+    do = torch.randn(1, 1024, 32, 128, generator=gen).to(torch.bfloat16)
+    dht = torch.randn(1, 32, 128, 128, generator=gen)
+    d = lambda t: t.to(DEV).contiguous()
+    out = gdn.gdn_chunk_bwd(d(case.q), d(case.k), d(case.v), d(g), d(beta), d(do), initial_state=d(case.initial_state),
+                            dht=d(dht))
+    torch.cuda.synchronize()
+    h, hv = 5, slice(10, 12)
+    ref = BO.backward(case.q[:, :, h:h + 1].float().numpy(), case.k[:, :, h:h + 1].float().numpy(),
+                      case.v[:, :, hv].float().numpy(), g[:, :, hv].numpy(), beta[:, :, hv].numpy(),
+                      do[:, :, hv].float().numpy(), initial_state=case.initial_state[:, hv].numpy(),
+                      dht=dht[:, hv].numpy(), use_qk_l2norm=True, scale=1.0 / np.sqrt(128))
+    gpu = [out[0][:, :, h:h + 1], out[1][:, :, h:h + 1], out[2][:, :, hv], out[3][:, :, hv], out[4][:, :, hv],
+           out[5][:, hv]]
+    for name, x, r in zip(["dq", "dk", "dv", "dg", "dbeta", "dh0"], gpu, ref):
+        err = P.rel_l2(x.cpu().numpy().astype(np.float64), r)
+        assert err <= BWD_REL_L2, f"{name}: rel-L2 {err:.3e}"
