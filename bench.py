@@ -321,6 +321,8 @@ def run_ours(args, rank, world, local_rank):
         line["conv1d"] = bench_conv(dev, stream, hbm, args)
         line["decode_variants"] = bench_decode_variants(dev, stream, hbm, args)
         line["backward"] = bench_backward(dev, stream, args)
+        line["fused_gating"] = bench_fused_gating(dev, stream, args,
+                                                  (q, k, v, A_log, a, b, dt_bias, h0, o, ht, ws, B, T, HV))
         line["e2e"] = bench_e2e(case, dev, stream, args, world)
         if rank == 0 and world == 1:
             gg, bb = gates_for_cpu(case)
@@ -547,6 +549,33 @@ def bench_backward(dev, stream, args):
     return {"workload": f"backward B={case.B} T={case.T} H={case.H} HV={case.HV} K={case.K} V={case.V}, "
                         "initial state, final-state gradient, forward recomputed inside",
             "ms": ms, "tokens_per_s": tokens / (ms / 1e3)}
+
+
+def bench_fused_gating(dev, stream, args, bufs):
+    """The same long-context prefill with the gating fused into the prefill's
+    first kernel (gdn_chunk_fwd_gated: two launches, no g / beta arrays),
+    timed beside the headline's gdn_gating + gdn_chunk_fwd."""
+    import torch
+    import gated_deltanet_chunked_chunk_gb300 as gdn
+    q, k, v, A_log, a, b, dt_bias, h0, o, ht, ws, B, T, HV = bufs
+    a3, b3 = a.view(B, T, HV), b.view(B, T, HV)
+
+    def call():
+        gdn.gdn_chunk_fwd_gated(q, k, v, A_log, a3, b3, dt_bias, initial_state=h0, o=o, final_state=ht,
+                                workspace=ws)
+    for _ in range(3):
+        call()
+    times = []
+    for _ in range(max(args.steps, 5)):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(e0.elapsed_time(e1))
+    ms = statistics.median(times)
+    return {"workload": f"long-context prefill B={B} T={T}, gating fused (gdn_chunk_fwd_gated)",
+            "ms": ms, "tokens_per_s": B * T / (ms / 1e3), "launches": 2}
 
 
 def bench_e2e(case, dev, stream, args, world):

@@ -25,7 +25,7 @@ __all__ = ["gdn_gating", "gdn_chunk_fwd", "gdn_recurrent_decode", "chunk_fwd_wor
            "gdn_chunk_fwd_noalloc", "NOALLOC_SCRATCH_BYTES", "gdn_causal_conv1d_fwd",
            "gdn_causal_conv1d_update", "gdn_conv_decode_pack", "gdn_recurrent_decode_bf16",
            "gdn_recurrent_decode_mtp", "gdn_chunk_bwd", "chunk_bwd_workspace_size",
-           "GDNError", "lib_path", "load_library", "status_string", "DEV_BAD_CU_SEQLENS",
+           "gdn_chunk_fwd_gated", "GDNError", "lib_path", "load_library", "status_string", "DEV_BAD_CU_SEQLENS",
            "DEV_BAD_SLOT", "DEV_WAIT_TIMEOUT", "EXPORTED_SYMBOLS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -41,7 +41,7 @@ EXPORTED_SYMBOLS = ("gdn_status_string", "gdn_version", "gdn_gating", "gdn_chunk
                     "gdn_chunk_fwd", "gdn_recurrent_decode", "gdn_chunk_fwd_noalloc",
                     "gdn_causal_conv1d_fwd", "gdn_causal_conv1d_update", "gdn_conv_decode_pack",
                     "gdn_recurrent_decode_bf16", "gdn_recurrent_decode_mtp", "gdn_chunk_bwd_workspace_size",
-                    "gdn_chunk_bwd")
+                    "gdn_chunk_bwd", "gdn_chunk_fwd_gated")
 
 #: Size of the fixed scratch buffer behind gdn_chunk_fwd_noalloc (bytes).
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -78,6 +78,9 @@ def load_library():
         lib.gdn_chunk_fwd_workspace_size.restype = SZ
         lib.gdn_chunk_fwd.argtypes = [P, P, P, P, P, F, P, P, I, I, I, I, I, I, I, I, P, P, P, SZ, P, P]
         lib.gdn_chunk_fwd.restype = I
+        lib.gdn_chunk_fwd_gated.argtypes = [P, P, P, P, P, P, P, F, P, P, I, I, I, I, I, I, I, I, P, P, P, P,
+                                            P, SZ, P, P]
+        lib.gdn_chunk_fwd_gated.restype = I
         lib.gdn_recurrent_decode.argtypes = [P, P, P, P, P, P, P, P, P, F, I, P, I, P, I, I, I, I, I,
                                              P, P, P]
         lib.gdn_recurrent_decode.restype = I
@@ -170,29 +173,16 @@ def chunk_fwd_workspace_size(B, T, H, HV, K, V, N, varlen) -> int:
     return int(load_library().gdn_chunk_fwd_workspace_size(B, T, H, HV, K, V, N, int(bool(varlen))))
 
 
-def gdn_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
-                  beta: torch.Tensor, scale: Optional[float] = None,
-                  initial_state: Optional[torch.Tensor] = None, output_final_state: bool = True,
-                  cu_seqlens: Optional[torch.Tensor] = None, use_qk_l2norm: bool = True,
-                  num_seqs: Optional[int] = None, dev_status: Optional[torch.Tensor] = None,
-                  o: Optional[torch.Tensor] = None, final_state: Optional[torch.Tensor] = None,
-                  workspace: Optional[torch.Tensor] = None
-                  ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
-    """Chunked prefill.  q, k bf16 [B,T,H,K]; v bf16 [B,T,HV,V]; g, beta fp32
-    [B,T,HV]; initial_state fp32 [N,HV,K,V] or None; cu_seqlens int32 [N+1]
-    (device) with B = 1, or None.  Returns (o bf16 [B,T,HV,V], final_state fp32
-    [N,HV,K,V] or None).  ``num_seqs`` gives N for varlen input without a
-    device-to-host read (default: cu_seqlens.numel() - 1, a host-side size)."""
+def _prefill_args(fn, q, k, v, initial_state, output_final_state, cu_seqlens, num_seqs, dev_status, o,
+                  final_state, workspace):
+    """Checks and output allocation shared by the prefill entry points."""
     dev = q.device
-    for t, n, dt in ((q, "q", torch.bfloat16), (k, "k", torch.bfloat16), (v, "v", torch.bfloat16),
-                     (g, "g", torch.float32), (beta, "beta", torch.float32)):
-        _check(t, n, dt, dev)
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, torch.bfloat16, dev)
     if q.dim() != 4 or k.shape != q.shape or v.dim() != 4 or v.shape[:2] != q.shape[:2]:
-        raise ValueError("gdn_chunk_fwd: q, k must be [B,T,H,K] and v [B,T,HV,V]")
+        raise ValueError(f"{fn}: q, k must be [B,T,H,K] and v [B,T,HV,V]")
     B, T, H, K = q.shape
     HV, V = v.shape[2], v.shape[3]
-    if tuple(g.shape) != (B, T, HV) or tuple(beta.shape) != (B, T, HV):
-        raise ValueError(f"gdn_chunk_fwd: g and beta must be [B,T,HV] = {(B, T, HV)}")
     if cu_seqlens is not None:
         _check(cu_seqlens, "cu_seqlens", torch.int32, dev, ndim=1)
         N = int(num_seqs) if num_seqs is not None else cu_seqlens.numel() - 1
@@ -214,13 +204,75 @@ def gdn_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
     ws_bytes = chunk_fwd_workspace_size(B, T, H, HV, K, V, N, cu_seqlens is not None)
     if ws_bytes > 0 and workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    return (B, T, H, K, HV, V, N), o, final_state, workspace
+
+
+def gdn_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                  beta: torch.Tensor, scale: Optional[float] = None,
+                  initial_state: Optional[torch.Tensor] = None, output_final_state: bool = True,
+                  cu_seqlens: Optional[torch.Tensor] = None, use_qk_l2norm: bool = True,
+                  num_seqs: Optional[int] = None, dev_status: Optional[torch.Tensor] = None,
+                  o: Optional[torch.Tensor] = None, final_state: Optional[torch.Tensor] = None,
+                  workspace: Optional[torch.Tensor] = None
+                  ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Chunked prefill.  q, k bf16 [B,T,H,K]; v bf16 [B,T,HV,V]; g, beta fp32
+    [B,T,HV]; initial_state fp32 [N,HV,K,V] or None; cu_seqlens int32 [N+1]
+    (device) with B = 1, or None.  Returns (o bf16 [B,T,HV,V], final_state fp32
+    [N,HV,K,V] or None).  ``num_seqs`` gives N for varlen input without a
+    device-to-host read (default: cu_seqlens.numel() - 1, a host-side size)."""
+    dims, o, final_state, workspace = _prefill_args("gdn_chunk_fwd", q, k, v, initial_state, output_final_state,
+                                                    cu_seqlens, num_seqs, dev_status, o, final_state, workspace)
+    B, T, H, K, HV, V, N = dims
+    for t, n in ((g, "g"), (beta, "beta")):
+        _check(t, n, torch.float32, q.device)
+    if tuple(g.shape) != (B, T, HV) or tuple(beta.shape) != (B, T, HV):
+        raise ValueError(f"gdn_chunk_fwd: g and beta must be [B,T,HV] = {(B, T, HV)}")
     rc = load_library().gdn_chunk_fwd(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _scale_arg(scale), _ptr(initial_state),
         _ptr(cu_seqlens), N, B, T, H, HV, K, V, int(bool(use_qk_l2norm)), _ptr(o),
         _ptr(final_state), _ptr(workspace), 0 if workspace is None else workspace.numel(),
-        _ptr(dev_status), _stream(dev))
+        _ptr(dev_status), _stream(q.device))
     if rc != GDN_OK:
         raise GDNError("gdn_chunk_fwd", rc)
+    return o, final_state
+
+
+def gdn_chunk_fwd_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, A_log: torch.Tensor,
+                        a: torch.Tensor, b: torch.Tensor, dt_bias: torch.Tensor, scale: Optional[float] = None,
+                        initial_state: Optional[torch.Tensor] = None, output_final_state: bool = True,
+                        cu_seqlens: Optional[torch.Tensor] = None, use_qk_l2norm: bool = True,
+                        num_seqs: Optional[int] = None, return_gates: bool = False,
+                        dev_status: Optional[torch.Tensor] = None, o: Optional[torch.Tensor] = None,
+                        final_state: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None):
+    """Chunked prefill with the gating fused in: A_log, dt_bias fp32 [HV]; a, b
+    bf16 [B,T,HV] (the raw gate projections).  Returns (o, final_state), or
+    (o, final_state, g, beta) with ``return_gates`` (fp32 [B,T,HV], e.g. for
+    the backward).  Other arguments as in ``gdn_chunk_fwd``."""
+    dims, o, final_state, workspace = _prefill_args("gdn_chunk_fwd_gated", q, k, v, initial_state,
+                                                    output_final_state, cu_seqlens, num_seqs, dev_status, o,
+                                                    final_state, workspace)
+    B, T, H, K, HV, V, N = dims
+    dev = q.device
+    for t, n, dt in ((A_log, "A_log", torch.float32), (dt_bias, "dt_bias", torch.float32),
+                     (a, "a", torch.bfloat16), (b, "b", torch.bfloat16)):
+        _check(t, n, dt, dev)
+    if tuple(A_log.shape) != (HV,) or tuple(dt_bias.shape) != (HV,):
+        raise ValueError(f"gdn_chunk_fwd_gated: A_log and dt_bias must be [HV] = {(HV,)}")
+    if tuple(a.shape) != (B, T, HV) or tuple(b.shape) != (B, T, HV):
+        raise ValueError(f"gdn_chunk_fwd_gated: a and b must be [B,T,HV] = {(B, T, HV)}")
+    g_out = beta_out = None
+    if return_gates:
+        g_out = torch.zeros((B, T, HV), dtype=torch.float32, device=dev)
+        beta_out = torch.zeros((B, T, HV), dtype=torch.float32, device=dev)
+    rc = load_library().gdn_chunk_fwd_gated(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(A_log), _ptr(a), _ptr(b), _ptr(dt_bias), _scale_arg(scale),
+        _ptr(initial_state), _ptr(cu_seqlens), N, B, T, H, HV, K, V, int(bool(use_qk_l2norm)), _ptr(o),
+        _ptr(final_state), _ptr(g_out), _ptr(beta_out), _ptr(workspace),
+        0 if workspace is None else workspace.numel(), _ptr(dev_status), _stream(dev))
+    if rc != GDN_OK:
+        raise GDNError("gdn_chunk_fwd_gated", rc)
+    if return_gates:
+        return o, final_state, g_out, beta_out
     return o, final_state
 
 

@@ -43,12 +43,13 @@ size_t gdn_chunk_fwd_workspace_size(int B, int T, int H, int HV, int K, int V,
   return gdn_host::chunk_workspace_bytes(B, T, H, HV, K, V, N, varlen);
 }
 
-int gdn_chunk_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                  const float *g, const float *beta, float scale,
-                  const float *initial_state, const int32_t *cu_seqlens, int N,
-                  int B, int T, int H, int HV, int K, int V, int use_qk_l2norm,
-                  uint16_t *o, float *final_state, void *workspace,
-                  size_t workspace_bytes, int32_t *dev_status, void *stream) {
+namespace {
+// Shared checks and launch of the two prefill entry points; `a` arrives with
+// its gate fields set.
+int chunk_fwd_common(gdn_host::ChunkArgs &a, const uint16_t *q, const uint16_t *k, const uint16_t *v, float scale,
+                     const float *initial_state, const int32_t *cu_seqlens, int N, int B, int T, int H, int HV,
+                     int K, int V, int use_qk_l2norm, uint16_t *o, float *final_state, void *workspace,
+                     size_t workspace_bytes, int32_t *dev_status, void *stream) {
   if (B < 0 || T < 0 || H <= 0 || HV <= 0 || K <= 0 || V <= 0 || N < 0) return GDN_EINVAL;
   if (HV % H != 0) return GDN_EINVAL;
   if (cu_seqlens) {
@@ -58,19 +59,45 @@ int gdn_chunk_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
   }
   if (!head_dim_ok(K) || !head_dim_ok(V)) return GDN_EUNSUPPORTED;
   const bool has_tokens = (int64_t)B * T > 0;
-  if (has_tokens && (!q || !k || !v || !g || !beta || !o)) return GDN_EINVAL;
+  const bool gates = a.A_log ? (a.ga && a.gb && a.dt_bias) : (a.g && a.beta);
+  if (has_tokens && (!q || !k || !v || !gates || !o)) return GDN_EINVAL;
   if (N == 0) return GDN_OK;
   const size_t need = gdn_host::chunk_workspace_bytes(B, T, H, HV, K, V, N, cu_seqlens != nullptr);
   if (need > 0 && (!workspace || workspace_bytes < need)) return GDN_EWORKSPACE;
   if (!(scale > 0.f)) scale = 1.f / sqrtf((float)K);  // also catches NaN
-  gdn_host::ChunkArgs a{};
-  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.scale = scale;
+  a.q = q; a.k = k; a.v = v; a.scale = scale;
   a.h0 = initial_state; a.cu = cu_seqlens;
   a.N = N; a.B = B; a.T = T; a.H = H; a.HV = HV; a.K = K; a.V = V;
   a.l2 = use_qk_l2norm ? 1 : 0;
   a.o = o; a.ht = final_state; a.ws = workspace; a.ws_bytes = workspace_bytes;
   a.dev_status = dev_status;
   return cuda_status(gdn_host::launch_chunk(a, static_cast<cudaStream_t>(stream)));
+}
+}  // namespace
+
+int gdn_chunk_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                  const float *g, const float *beta, float scale,
+                  const float *initial_state, const int32_t *cu_seqlens, int N,
+                  int B, int T, int H, int HV, int K, int V, int use_qk_l2norm,
+                  uint16_t *o, float *final_state, void *workspace,
+                  size_t workspace_bytes, int32_t *dev_status, void *stream) {
+  gdn_host::ChunkArgs a{};
+  a.g = g; a.beta = beta;
+  return chunk_fwd_common(a, q, k, v, scale, initial_state, cu_seqlens, N, B, T, H, HV, K, V, use_qk_l2norm, o,
+                          final_state, workspace, workspace_bytes, dev_status, stream);
+}
+
+int gdn_chunk_fwd_gated(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *A_log,
+                        const uint16_t *a_raw, const uint16_t *b_raw, const float *dt_bias, float scale,
+                        const float *initial_state, const int32_t *cu_seqlens, int N, int B, int T, int H,
+                        int HV, int K, int V, int use_qk_l2norm, uint16_t *o, float *final_state, float *g_out,
+                        float *beta_out, void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                        void *stream) {
+  if ((g_out == nullptr) != (beta_out == nullptr)) return GDN_EINVAL;  // both or neither
+  gdn_host::ChunkArgs a{};
+  a.A_log = A_log; a.ga = a_raw; a.gb = b_raw; a.dt_bias = dt_bias; a.g_out = g_out; a.beta_out = beta_out;
+  return chunk_fwd_common(a, q, k, v, scale, initial_state, cu_seqlens, N, B, T, H, HV, K, V, use_qk_l2norm, o,
+                          final_state, workspace, workspace_bytes, dev_status, stream);
 }
 
 size_t gdn_chunk_bwd_workspace_size(int B, int T, int H, int HV, int K, int V, int N, int varlen) {

@@ -21,7 +21,7 @@
 //   o     = scale (e^gamma rq (Q h) + P v_new)
 //   h    <- e^{gamma_L} h + K^T diag(e^{gamma_L-gamma} rk) v_new
 //
-// gdn_chunk_prep (one CTA per (chunk, value head), two CTAs per SM): TMA loads
+// gdn_chunk_prep (one CTA per (chunk, value head), four CTAs per SM): TMA loads
 // K and Q; one thread issues tcgen05.mma for [K;Q][K;Q]^T (M = N = 128,
 // 128B-swizzled smem operands, fp32 accumulator in TMEM), whose diagonal gives
 // the row norms; A and P are built from TMEM; T by 16x16 diagonal-block
@@ -107,23 +107,37 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
 // ============================================================== prep kernel
 template <int K>
 struct PrepLay {
+  // The Q rows of the [K;Q] tile are dead once [K;Q][K;Q]^T has completed: the
+  // bf16 T diag(beta e^g rk) tile and the fp32 scratch of the solve reuse them,
+  // which keeps a CTA small enough for four per SM.
   static constexpr int OFF_KQ = 0;                              // [K;Q] tile
+  static constexpr int OFF_TP = 8192;                           // T diag(beta e^g rk), bf16 SW128 (Q rows, atom 0)
   static constexpr int OFF_AT = KQ<K>::BYTES;                   // A then T, fp32 [64][FROW], in place
-  static constexpr int OFF_TP = OFF_AT + 64 * FROW * 4;         // T diag(beta e^g rk), bf16 SW128
-  static constexpr int OFF_X = OFF_TP + 8192;                   // 4 x [16][17] fp32
-  static constexpr int OFF_SC = OFF_X + 4352;                   // gl, bet, rk, rq, rowA, rowP, colf, ftp
+  static constexpr int OFF_X = K >= 128 ? 16384 + 8192          // 4 x [16][17] fp32 (Q rows, atom 1)
+                                        : OFF_AT + 64 * FROW * 4;
+  static constexpr int OFF_SC = K >= 128 ? OFF_AT + 64 * FROW * 4 : OFF_X + 4352;  // gl, bet, rk, rq, rowA, rowP, colf, ftp
   static constexpr int OFF_BAR = OFF_SC + 8 * 256;
   static constexpr int OFF_MISC = OFF_BAR + 16;
   static constexpr int BYTES = OFF_MISC + 16;
   static_assert(OFF_TP % 1024 == 0, "swizzled tile alignment");
+  static_assert(4 * (BYTES + 1024 + 1024) <= 228 * 1024, "four CTAs per SM");
 };
 enum { PS_GL = 0, PS_BET = 1, PS_RK = 2, PS_RQ = 3, PS_RA = 4, PS_RP = 5, PS_CF = 6, PS_FTP = 7 };
 
+// Raw gate inputs when the gating is fused into the prep (A_log == NULL: g and
+// beta are given instead).
+struct PrepGates {
+  const float *A_log;
+  const uint16_t *a, *b;
+  const float *dt_bias;
+  float *g_out, *beta_out;  // optional copies of the computed gates
+};
+
 template <int K>
-__global__ void __launch_bounds__(NTH, 3) chunk_prep_kernel(
+__global__ void __launch_bounds__(NTH, 4) chunk_prep_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k, const float *__restrict__ g,
-    const float *__restrict__ beta, const int32_t *__restrict__ cu, int N, int T, int H, int HV, int l2,
-    unsigned char *__restrict__ ws, int32_t *dev_status) {
+    const float *__restrict__ beta, const PrepGates gt, const int32_t *__restrict__ cu, int N, int T, int H,
+    int HV, int l2, unsigned char *__restrict__ ws, int32_t *dev_status) {
   using Ly = PrepLay<K>;
   using R = Rec<K>;
   constexpr int KA = K / 64;
@@ -193,13 +207,31 @@ __global__ void __launch_bounds__(NTH, 3) chunk_prep_kernel(
     }
   }
   // Gates (rows >= L read as 0) and their chunk-local cumsum in base 2 (warp 4).
+  // Fused gating follows FastDeploy PR "support fla triton kernel for qwen3.5",
+  // Usage section 5: g = -e^{A_log} softplus(a + dt_bias), beta = sigmoid(b).
   if (warp == 4) {
     float x[2], bb[2];
+    const float na = gt.A_log ? -expf(gt.A_log[hv]) : 0.f;
+    const float db = gt.A_log ? gt.dt_bias[hv] : 0.f;
 #pragma unroll
     for (int u2 = 0; u2 < 2; ++u2) {
       const int r = 2 * lane + u2;
-      x[u2] = r < L ? g[(trow0 + r) * HV + hv] : 0.f;
-      bb[u2] = r < L ? beta[(trow0 + r) * HV + hv] : 0.f;
+      const int64_t gi = (trow0 + r) * HV + hv;
+      x[u2] = 0.f;
+      bb[u2] = 0.f;
+      if (r < L) {
+        if (gt.A_log) {
+          x[u2] = na * softplus_fast(bf2f(gt.a[gi]) + db);  // as gdn_gating computes them
+          bb[u2] = sigmoid_fast(bf2f(gt.b[gi]));
+          if (gt.g_out) {
+            gt.g_out[gi] = x[u2];
+            gt.beta_out[gi] = bb[u2];
+          }
+        } else {
+          x[u2] = g[gi];
+          bb[u2] = beta[gi];
+        }
+      }
     }
     bet[2 * lane] = bb[0];
     bet[2 * lane + 1] = bb[1];
@@ -250,11 +282,21 @@ __global__ void __launch_bounds__(NTH, 3) chunk_prep_kernel(
       const bool kdiag = (quad < 2) && (half == quad);
       const bool qdiag = (warp == 2) || (warp == 7);
       if (kdiag || qdiag) {
-        float dv[32];
-        if (qdiag) tmem_ld32(tl + 64 + 32 * (quad - 2), dv);
-        float d = kdiag ? vals[0] : dv[0];
+        float d = vals[0];
+        if (kdiag) {
 #pragma unroll
-        for (int m = 1; m < 32; ++m) d = (lane == m) ? (kdiag ? vals[m] : dv[m]) : d;
+          for (int m = 1; m < 32; ++m) d = (lane == m) ? vals[m] : d;
+        } else {
+          // The Q Q^T diagonal, 16 columns at a time (fewer live registers).
+#pragma unroll
+          for (int p = 0; p < 2; ++p) {
+            uint32_t dv[16];
+            tmem_ld16_issue(tl + 64 + 32 * (quad - 2) + 16 * p, dv);
+            tmem_ld_wait16(dv);
+#pragma unroll
+            for (int m = 0; m < 16; ++m) d = (lane == 16 * p + m) ? __uint_as_float(dv[m]) : d;
+          }
+        }
         const float rn = rsqrtf(d + GDN_L2_EPS);
         if (kdiag) rk[row] = rn; else rq[row - 64] = rn;
       }
@@ -452,36 +494,40 @@ __global__ void __launch_bounds__(NTH, 3) chunk_prep_kernel(
   }
   __syncthreads();
 
-  // W = Tp K (64 x K): warp -> 16 rows (mi) x half of the keys (nh).
+  // W = Tp K (64 x K): warp -> 16 rows (mi) x half of the keys (nh), in two
+  // passes of a quarter of the keys each (fewer live accumulators).
   {
     const int mi = warp & 3, nh = warp >> 2;
-    constexpr int WN = K / 16;
-    float acc[WN][4];
+    constexpr int WN = K / 16, WQ = WN / 2;
 #pragma unroll
-    for (int j = 0; j < WN; ++j)
+    for (int pass = 0; pass < 2; ++pass) {
+      float acc[WQ][4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
+      for (int j = 0; j < WQ; ++j)
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      uint32_t a[4];
-      ldsm_x4(sb + Ly::OFF_TP + sw128(16 * mi + (lane & 15), 2 * kk + (lane >> 4)), a);
-      const int mq = lane >> 3;
-      const int trow = 16 * kk + (lane & 7) + 8 * (mq & 1);
+        for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
 #pragma unroll
-      for (int j = 0; j < WN; j += 2) {
-        uint32_t b[4];
-        ldsm_x4_t(tile_addr(kq, 128, trow, nh * WN + j + (mq >> 1)), b);
-        mma_bf16(acc[j], a, b[0], b[1]);
-        mma_bf16(acc[j + 1], a, b[2], b[3]);
+      for (int kk = 0; kk < 4; ++kk) {
+        uint32_t a[4];
+        ldsm_x4(sb + Ly::OFF_TP + sw128(16 * mi + (lane & 15), 2 * kk + (lane >> 4)), a);
+        const int mq = lane >> 3;
+        const int trow = 16 * kk + (lane & 7) + 8 * (mq & 1);
+#pragma unroll
+        for (int j = 0; j < WQ; j += 2) {
+          uint32_t b[4];
+          ldsm_x4_t(tile_addr(kq, 128, trow, nh * WN + pass * WQ + j + (mq >> 1)), b);
+          mma_bf16(acc[j], a, b[0], b[1]);
+          mma_bf16(acc[j + 1], a, b[2], b[3]);
+        }
       }
-    }
 #pragma unroll
-    for (int j = 0; j < WN; ++j) {
-      const int key = 8 * (nh * WN + j) + 2 * t4;
-      const int r0 = 16 * mi + g4;
-      unsigned char *base = rec + R::W + (key >> 6) * 8192 + (key & 7) * 2;
-      *reinterpret_cast<uint32_t *>(base + sw128(r0, (key & 63) >> 3)) = pack_bf16(acc[j][0], acc[j][1]);
-      *reinterpret_cast<uint32_t *>(base + sw128(r0 + 8, (key & 63) >> 3)) = pack_bf16(acc[j][2], acc[j][3]);
+      for (int j = 0; j < WQ; ++j) {
+        const int key = 8 * (nh * WN + pass * WQ + j) + 2 * t4;
+        const int r0 = 16 * mi + g4;
+        unsigned char *base = rec + R::W + (key >> 6) * 8192 + (key & 7) * 2;
+        *reinterpret_cast<uint32_t *>(base + sw128(r0, (key & 63) >> 3)) = pack_bf16(acc[j][0], acc[j][1]);
+        *reinterpret_cast<uint32_t *>(base + sw128(r0 + 8, (key & 63) >> 3)) = pack_bf16(acc[j][2], acc[j][3]);
+      }
     }
   }
 }
@@ -980,7 +1026,8 @@ cudaError_t launch_k(const gdn_host::ChunkArgs &a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, psmem);
     if (e != cudaSuccess) return e;
     dim3 pgrid(static_cast<unsigned>(slots), a.HV);
-    chunk_prep_kernel<K><<<pgrid, NTH, psmem, s>>>(mq, mk, a.g, a.beta, a.cu, a.N, a.T, a.H, a.HV, a.l2,
+    const PrepGates gt{a.A_log, a.ga, a.gb, a.dt_bias, a.g_out, a.beta_out};
+    chunk_prep_kernel<K><<<pgrid, NTH, psmem, s>>>(mq, mk, a.g, a.beta, gt, a.cu, a.N, a.T, a.H, a.HV, a.l2,
                                                    static_cast<unsigned char *>(a.ws), a.dev_status);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -35,6 +35,13 @@ __device__ __forceinline__ float softplus_f(float x) {
 
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + expf(-x)); }
 
+// The same two functions with the hardware exponential (a relative error of a
+// few ulp in e^x moves log1p(e^x) and 1 / (1 + e^-x) by less than that, far
+// inside the 1e-5 relative budget of the gates).  gdn_gating and the fused
+// gating of the prefill both use these, so their gates agree bit for bit.
+__device__ __forceinline__ float softplus_fast(float x) { return x > 20.f ? x : log1pf(__expf(x)); }
+__device__ __forceinline__ float sigmoid_fast(float x) { return 1.f / (1.f + __expf(-x)); }
+
 __device__ __forceinline__ void set_status(int32_t *st, int bits) {
   if (st) atomicOr(st, bits);
 }
@@ -81,6 +88,13 @@ struct ChunkArgs {
   uint16_t *o;   // may be NULL (no output written)
   float *ht;
   float *hsave;  // NULL, or [chunk slots][HV][K][V]: the state entering every chunk
+  // Fused gating (A_log != NULL; g, beta then NULL): the prep kernel computes
+  // g = -e^{A_log} softplus(a + dt_bias), beta = sigmoid(b) itself and, when
+  // g_out / beta_out are set, stores them ([B, T, HV] fp32).
+  const float *A_log;
+  const uint16_t *ga, *gb;
+  const float *dt_bias;
+  float *g_out, *beta_out;
   void *ws;
   size_t ws_bytes;
   int32_t *dev_status;

@@ -126,6 +126,35 @@ int gdn_chunk_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                   size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /*
+ * gdn_chunk_fwd_gated -- gdn_chunk_fwd with the gating fused into its first
+ * kernel.  FastDeploy PR "support fla triton kernel for qwen3.5", Usage
+ * section 5 ("Fused GDN Gating": g = -exp(A_log) * softplus(a + dt_bias),
+ * beta = sigmoid(b)) feeding Usage section 1; LightLLM "gdn.py" computes the
+ * same gates right before its prefill call.  The per-chunk kernel computes
+ * g and beta from the raw inputs as it loads them, so no [B, T, HV] gate
+ * arrays pass through memory unless asked for.
+ *
+ *   A_log, dt_bias : fp32 [HV]
+ *   a, b           : bf16 [B, T, HV]
+ *   g_out, beta_out: fp32 [B, T, HV] copies of the computed gates (for a
+ *                    later backward), or both NULL; exactly one NULL is
+ *                    GDN_EINVAL.  Rows of every chunk are written; rows past
+ *                    cu_seqlens[N] are not.
+ * Every other argument, the workspace and the errors are as in gdn_chunk_fwd.
+ * The gates are bit-identical to gdn_gating's, and so are o and final_state
+ * to those of gdn_chunk_fwd given those gates.
+ */
+int gdn_chunk_fwd_gated(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                        const float *A_log, const uint16_t *a,
+                        const uint16_t *b, const float *dt_bias, float scale,
+                        const float *initial_state, const int32_t *cu_seqlens,
+                        int N, int B, int T, int H, int HV, int K, int V,
+                        int use_qk_l2norm, uint16_t *o, float *final_state,
+                        float *g_out, float *beta_out, void *workspace,
+                        size_t workspace_bytes, int32_t *dev_status,
+                        void *stream);
+
+/*
  * gdn_recurrent_decode -- one token per request against a state pool,
  * updated in place.  FastDeploy PR "support fla triton kernel for qwen3.5",
  * Usage section 2 ("Decode (fused recurrent, pool-index)") and its file table

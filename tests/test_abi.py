@@ -66,6 +66,29 @@ def test_chunk_fwd_host_validation(lib):
     assert _chunk(lib, N=0, B=0, T=0) == gdn.GDN_OK           # nothing to do, nothing launched
 
 
+def test_chunk_fwd_gated_host_validation(lib):
+    fake = ctypes.c_void_p(16)
+
+    def call(**kw):
+        a = dict(q=fake, k=fake, v=fake, A_log=fake, a=fake, b=fake, dt=fake, scale=-1.0, h0=NULL, cu=NULL,
+                 N=1, B=1, T=8, H=2, HV=4, K=128, V=128, l2=1, o=fake, ht=NULL, gout=NULL, bout=NULL,
+                 ws=NULL, wsb=0, st=NULL, stream=NULL)
+        a.update(kw)
+        return lib.gdn_chunk_fwd_gated(a["q"], a["k"], a["v"], a["A_log"], a["a"], a["b"], a["dt"], a["scale"],
+                                       a["h0"], a["cu"], a["N"], a["B"], a["T"], a["H"], a["HV"], a["K"],
+                                       a["V"], a["l2"], a["o"], a["ht"], a["gout"], a["bout"], a["ws"],
+                                       a["wsb"], a["st"], a["stream"])
+    assert call(A_log=NULL) == gdn.GDN_EINVAL                 # no gate inputs at all
+    assert call(b=NULL) == gdn.GDN_EINVAL                     # part of the gate group
+    assert call(dt=NULL) == gdn.GDN_EINVAL
+    assert call(gout=fake) == gdn.GDN_EINVAL                  # g copy without the beta copy
+    assert call(bout=fake) == gdn.GDN_EINVAL
+    assert call(HV=3) == gdn.GDN_EINVAL
+    assert call(K=96) == gdn.GDN_EUNSUPPORTED
+    assert call() == gdn.GDN_EWORKSPACE                       # T = 8 needs the record workspace
+    assert call(N=0, B=0, T=0, A_log=NULL, a=NULL, b=NULL, dt=NULL) == gdn.GDN_OK
+
+
 def test_decode_host_validation(lib):
     fake = ctypes.c_void_p(16)
 
