@@ -21,7 +21,8 @@
 //
 // The forward is re-run first (prep + walk kernels of gdn_chunk.cu) with the
 // walk saving the state entering every chunk; the dh walk saves dh' of every
-// chunk.  Both kernels here compute in fp32 on the CUDA cores.
+// chunk (fp32, CUDA cores).  The per-chunk gradients run their products on the
+// tensor cores (mma.sync tf32, operands split hi + lo for fp32 accuracy).
 #include <math.h>
 #include <string.h>
 
@@ -212,38 +213,104 @@ __global__ void __launch_bounds__(BT, 1) chunk_dh_kernel(
 }
 
 // ---------------------------------------------------------- chunk gradients
-// One CTA per (chunk, value head), fp32 throughout.  Thread t owns row
-// i = t / 4 of every 64-row result and a quarter of its columns.
-constexpr int VS = 16;  // V columns per slice
+// One CTA per (chunk, value head).  Every product runs on the tensor cores as
+// warp-level mma.sync m16n8k8 in tf32 with fp32 accumulation.  A computed fp32
+// operand is split into tf32 hi + lo parts and the product takes hi*hi + hi*lo
+// + lo*hi, which keeps fp32-level accuracy; an operand holding raw bf16 inputs
+// (q, k, v, do) is exact in tf32 and has no low part.  Warp w owns the 16-row
+// tile mt = w & 3 of a 64-row result and, where the result is wider than one
+// warp's share, the column half hf = w >> 2.
+
+__device__ __forceinline__ uint32_t tf32_rna(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// c (16 x 8 NT) += A (16 x [k0, k1)) B ([k0, k1) x 8 NT) for one warp, with
+// fa(r, k) = A[r][k] (r < 16) and fb(k, n) = B[k][n]; k0, k1 multiples of 8.
+// AX / BX: that operand is exact in tf32.
+template <int NT, bool AX, bool BX, class FA, class FB>
+__device__ __forceinline__ void wgemm(float (&c)[NT][4], int k0, int k1, FA fa, FB fb) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  for (int k = k0; k < k1; k += 8) {
+    const float av[4] = {fa(g, k + t), fa(g + 8, k + t), fa(g, k + t + 4), fa(g + 8, k + t + 4)};
+    uint32_t ah[4], al[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      ah[e] = AX ? __float_as_uint(av[e]) : tf32_rna(av[e]);
+      al[e] = AX ? 0u : tf32_rna(av[e] - __uint_as_float(ah[e]));
+    }
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      const float b0 = fb(k + t, 8 * n + g), b1 = fb(k + t + 4, 8 * n + g);
+      const uint32_t bh0 = BX ? __float_as_uint(b0) : tf32_rna(b0);
+      const uint32_t bh1 = BX ? __float_as_uint(b1) : tf32_rna(b1);
+      mma_tf32(c[n], ah, bh0, bh1);
+      if (!BX) mma_tf32(c[n], ah, tf32_rna(b0 - __uint_as_float(bh0)), tf32_rna(b1 - __uint_as_float(bh1)));
+      if (!AX) mma_tf32(c[n], al, bh0, bh1);
+    }
+  }
+}
+// f(rh, r, n, x) for every accumulator element: row r = g + 8 rh, column n.
+template <int NT, class F>
+__device__ __forceinline__ void cvisit(float (&c)[NT][4], F f) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int n = 0; n < NT; ++n)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) f(e >> 1, g + 8 * (e >> 1), 8 * n + 2 * t + (e & 1), c[n][e]);
+}
+__device__ __forceinline__ float quad_sum(float x) {
+  x += __shfl_xor_sync(0xffffffffu, x, 1);
+  return x + __shfl_xor_sync(0xffffffffu, x, 2);
+}
+
+constexpr int VS = 32;  // V columns per slice
+constexpr int MS = 68;  // fp32 row stride of a 64 x 64 tile
+constexpr int SS = 36;  // fp32 row stride of a 32-column slice
 
 template <int K>
 struct GradLay {
-  static constexpr int QROW = K + 4;                        // padded fp32 rows
-  static constexpr int OFF_Q = 0;                           // q^ [64][QROW]
-  static constexpr int OFF_K = OFF_Q + 64 * QROW * 4;       // k^ [64][QROW]
-  static constexpr int M64 = 64 * 65 * 4;                   // a padded 64 x 64 fp32 tile
-  static constexpr int OFF_KK = OFF_K + 64 * QROW * 4;      // k^ k^T
-  static constexpr int OFF_QK = OFF_KK + M64;               // q^ k^T
-  static constexpr int OFF_T = OFF_QK + M64;                // T
-  static constexpr int OFF_DT = OFF_T + M64;                // dT
-  static constexpr int OFF_DP = OFF_DT + M64;               // dP
-  static constexpr int OFF_X = OFF_DP + M64;                // scratch 64 x 64
-  static constexpr int SROW = VS + 1;
-  static constexpr int OFF_H = OFF_X + M64;                 // h slice [K][SROW]
-  static constexpr int OFF_DH = OFF_H + K * SROW * 4;       // dh' slice [K][SROW]
-  static constexpr int OFF_V = OFF_DH + K * SROW * 4;       // v slice [64][SROW]
-  static constexpr int OFF_DO = OFF_V + 64 * SROW * 4;      // do slice
-  static constexpr int OFF_KH = OFF_DO + 64 * SROW * 4;     // k^ h
-  static constexpr int OFF_QH = OFF_KH + 64 * SROW * 4;     // q^ h
-  static constexpr int OFF_KDH = OFF_QH + 64 * SROW * 4;    // k^ dh'
-  static constexpr int OFF_VN = OFF_KDH + 64 * SROW * 4;    // v_new
-  static constexpr int OFF_DVN = OFF_VN + 64 * SROW * 4;    // dv_new
-  static constexpr int OFF_TU = OFF_DVN + 64 * SROW * 4;    // T^T dv_new
-  static constexpr int OFF_VEC = OFF_TU + 64 * SROW * 4;    // per-row vectors
-  static constexpr int NVEC = 12;
-  static constexpr int BYTES = OFF_VEC + NVEC * 64 * 4 + 16;
+  static constexpr int BROW = K + 8;                     // bf16 row stride of raw q, k
+  static constexpr int M64 = 64 * MS * 4;
+  static constexpr int HS = K * SS * 4, RS = 64 * SS * 4;
+  static constexpr int OFF_QB = 0;                       // raw q [64][BROW] bf16
+  static constexpr int OFF_KB = OFF_QB + 64 * BROW * 2;  // raw k
+  static constexpr int OFF_T = OFF_KB + 64 * BROW * 2;   // A, then T = (I + A)^-1
+  static constexpr int OFF_P = OFF_T + M64;              // P_ij = e^{gamma_i-gamma_j} q^_i.k^_j (j <= i)
+  static constexpr int OFF_EK = OFF_P + M64;             // e^{gamma_i-gamma_j} k^_i.k^_j (j < i)
+  static constexpr int OFF_SL = OFF_EK + M64;            // V-slice buffers, reused afterwards
+  static constexpr int OFF_H = OFF_SL;                   // h slice [K][SS]
+  static constexpr int OFF_DH = OFF_H + HS;              // dh' slice
+  static constexpr int OFF_V = OFF_DH + HS;              // v slice [64][SS]
+  static constexpr int OFF_DO = OFF_V + RS;              // do slice
+  static constexpr int OFF_KH = OFF_DO + RS;             // k^ h
+  static constexpr int OFF_KDH = OFF_KH + RS;            // k^ dh'
+  static constexpr int OFF_MV = OFF_KDH + RS;            // diag(beta) (v - diag(og) k^ h)
+  static constexpr int OFF_VN = OFF_MV + RS;             // v_new
+  static constexpr int OFF_DVN = OFF_VN + RS;            // dv_new
+  static constexpr int OFF_TU = OFF_DVN + RS;            // T^T dv_new
+  static constexpr int SL_END = OFF_TU + RS;
+  static constexpr int OFF_DT = OFF_SL;                  // after the slices: dT, then dA
+  static constexpr int OFF_DP = OFF_DT + M64;            // scale dP
+  static constexpr int OFF_X = OFF_DP + M64;             // dT T^T
+  static constexpr int OFF_S1 = OFF_X + M64;             // (A-bar + A-bar^T) diag(rk)
+  static constexpr int OFF_S2 = OFF_S1 + M64;            // P-bar^T diag(rq)
+  static constexpr int OFF_S3 = OFF_S2 + M64;            // P-bar diag(rk)
+  static constexpr int END_END = OFF_S3 + M64;
+  static constexpr int OFF_VEC = SL_END > END_END ? SL_END : END_END;
+  static constexpr int NVEC = 14;
+  static constexpr int BYTES = OFF_VEC + NVEC * 64 * 4;
+  static_assert(BYTES <= 227 * 1024, "one CTA per SM");
 };
-enum { GV_GAM = 0, GV_BET, GV_RQ, GV_RK, GV_OG, GV_SV, GV_DB, GV_DG, GV_DGL, GV_TMP, GV_TMP2, GV_L };
+enum { GV_GAM = 0, GV_OG, GV_SV, GV_BET, GV_RQ, GV_RK, GV_DB, GV_DG, GV_SQ, GV_SG, GV_SL, GV_PQ, GV_PK, GV_MISC };
 
 template <int K>
 __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
@@ -253,40 +320,46 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
     int N, int T, int H, int HV, int V, int l2, float *__restrict__ dq, float *__restrict__ dk,
     float *__restrict__ dv, float *__restrict__ dg, float *__restrict__ dbeta, int32_t *dev_status) {
   using Ly = GradLay<K>;
-  constexpr int QR = Ly::QROW, SR = Ly::SROW;
+  constexpr int BR = Ly::BROW;
+  constexpr int NH = K / 16;  // n-tiles of a warp's half of K columns
   extern __shared__ __align__(16) unsigned char smem[];
-  float *Qh = reinterpret_cast<float *>(smem + Ly::OFF_Q);
-  float *Kh = reinterpret_cast<float *>(smem + Ly::OFF_K);
-  float *KK = reinterpret_cast<float *>(smem + Ly::OFF_KK);
-  float *QK = reinterpret_cast<float *>(smem + Ly::OFF_QK);
+  uint16_t *Qb = reinterpret_cast<uint16_t *>(smem + Ly::OFF_QB);
+  uint16_t *Kb = reinterpret_cast<uint16_t *>(smem + Ly::OFF_KB);
   float *Tm = reinterpret_cast<float *>(smem + Ly::OFF_T);
-  float *dT = reinterpret_cast<float *>(smem + Ly::OFF_DT);
-  float *dP = reinterpret_cast<float *>(smem + Ly::OFF_DP);
-  float *X = reinterpret_cast<float *>(smem + Ly::OFF_X);
+  float *Pm = reinterpret_cast<float *>(smem + Ly::OFF_P);
+  float *EK = reinterpret_cast<float *>(smem + Ly::OFF_EK);
   float *hS = reinterpret_cast<float *>(smem + Ly::OFF_H);
   float *dhS = reinterpret_cast<float *>(smem + Ly::OFF_DH);
   float *vS = reinterpret_cast<float *>(smem + Ly::OFF_V);
   float *doS = reinterpret_cast<float *>(smem + Ly::OFF_DO);
   float *KhS = reinterpret_cast<float *>(smem + Ly::OFF_KH);
-  float *QhS = reinterpret_cast<float *>(smem + Ly::OFF_QH);
   float *KdhS = reinterpret_cast<float *>(smem + Ly::OFF_KDH);
+  float *MvS = reinterpret_cast<float *>(smem + Ly::OFF_MV);
   float *vnS = reinterpret_cast<float *>(smem + Ly::OFF_VN);
   float *dvnS = reinterpret_cast<float *>(smem + Ly::OFF_DVN);
   float *TuS = reinterpret_cast<float *>(smem + Ly::OFF_TU);
+  float *DT = reinterpret_cast<float *>(smem + Ly::OFF_DT);
+  float *DP = reinterpret_cast<float *>(smem + Ly::OFF_DP);
+  float *Xm = reinterpret_cast<float *>(smem + Ly::OFF_X);
+  float *S1 = reinterpret_cast<float *>(smem + Ly::OFF_S1);
+  float *S2 = reinterpret_cast<float *>(smem + Ly::OFF_S2);
+  float *S3 = reinterpret_cast<float *>(smem + Ly::OFF_S3);
   float *vec = reinterpret_cast<float *>(smem + Ly::OFF_VEC);
-  float *gam = vec + GV_GAM * 64, *bet = vec + GV_BET * 64, *rq = vec + GV_RQ * 64, *rk = vec + GV_RK * 64;
-  float *og = vec + GV_OG * 64, *sv = vec + GV_SV * 64, *dbv = vec + GV_DB * 64, *dgam = vec + GV_DG * 64;
-  float *tmp = vec + GV_TMP * 64;
-  constexpr int M = 65;  // padded 64 x 64 stride
+  float *gam = vec + GV_GAM * 64, *og = vec + GV_OG * 64, *sv = vec + GV_SV * 64, *bet = vec + GV_BET * 64;
+  float *rq = vec + GV_RQ * 64, *rk = vec + GV_RK * 64, *DB = vec + GV_DB * 64, *DG = vec + GV_DG * 64;
+  float *SQ = vec + GV_SQ * 64, *SG = vec + GV_SG * 64, *SLv = vec + GV_SL * 64;
+  float *PQ = vec + GV_PQ * 64, *PK = vec + GV_PK * 64, *misc = vec + GV_MISC * 64;
 
   const int gc = blockIdx.x, hv = blockIdx.y;
   const int h = hv / (HV / H);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int ri = tid >> 2, qd = tid & 3;  // row and column quarter of 64-row results
+  const int g8 = lane >> 2, t4 = lane & 3;
+  const int mt = warp & 3, hf = warp >> 2, r0 = 16 * mt;
 
   // Which sequence / chunk?
   int c = 0;
-  int64_t tok0 = 0, len = 0, slot = gc;
+  int64_t tok0 = 0, len = 0;
+  const int64_t slot = gc;
   {
     int64_t base = 0;
     bool found = false;
@@ -307,13 +380,20 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
   const int64_t rem = len - (int64_t)c * C;
   const int L = rem < C ? (int)rem : C;
   const int64_t trow0 = tok0 + (int64_t)c * C;
+  auto qv = [&](int i, int x) { return bf2f(Qb[i * BR + x]); };
+  auto kv = [&](int i, int x) { return bf2f(Kb[i * BR + x]); };
 
-  // ---- q^, k^, gates, decays
-  for (int e = tid; e < 64 * K; e += BT) {
-    const int i = e / K, x = e % K;
-    const bool live = i < L;
-    Qh[i * QR + x] = live ? bf2f(q[((trow0 + i) * H + h) * K + x]) : 0.f;
-    Kh[i * QR + x] = live ? bf2f(k[((trow0 + i) * H + h) * K + x]) : 0.f;
+  // ---- raw q, k rows (zero past L), gates and their cumsum
+  for (int e = tid; e < 64 * (K / 8); e += BT) {
+    const int i = e / (K / 8), ch = e % (K / 8);
+    uint4 a = make_uint4(0, 0, 0, 0), b = a;
+    if (i < L) {
+      const int64_t off = ((trow0 + i) * H + h) * K + ch * 8;
+      a = *reinterpret_cast<const uint4 *>(q + off);
+      b = *reinterpret_cast<const uint4 *>(k + off);
+    }
+    *reinterpret_cast<uint4 *>(Qb + i * BR + ch * 8) = a;
+    *reinterpret_cast<uint4 *>(Kb + i * BR + ch * 8) = b;
   }
   if (warp == 0) {
     float x[2];
@@ -332,323 +412,365 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
     gam[2 * lane] = sum - x[1];
     gam[2 * lane + 1] = sum;
   }
+  for (int e = tid; e < 64 * (GV_MISC - GV_DB + 1); e += BT) vec[GV_DB * 64 + e] = 0.f;
   __syncthreads();
-  if (tid < 128) {  // norms: 2 threads per row (q for tid < 64, k otherwise)
-    const int i = tid & 63;
-    const float *row = (tid < 64 ? Qh : Kh) + i * QR;
-    float s2 = 0.f;
-    for (int x = 0; x < K; ++x) s2 = fmaf(row[x], row[x], s2);
-    const float rn = l2 ? rsqrtf(s2 + GDN_L2_EPS) : 1.f;
-    (tid < 64 ? rq : rk)[i] = rn;
-  }
-  __syncthreads();
-  for (int e = tid; e < 64 * K; e += BT) {
-    const int i = e / K, x = e % K;
-    Qh[i * QR + x] *= rq[i];
-    Kh[i * QR + x] *= rk[i];
-  }
-  if (tid < 64) {
-    og[tid] = expf(gam[tid]);
-    sv[tid] = expf(gam[63] - gam[tid]);
-    dbv[tid] = 0.f;
-    dgam[tid] = 0.f;
-  }
-  __syncthreads();
-  // ---- KK = k^ k^T, QK = q^ k^T (full 64 x 64)
-  for (int e = tid; e < 64 * 64; e += BT) {
-    const int i = e >> 6, j = e & 63;
-    float a = 0.f, b = 0.f;
-    for (int x = 0; x < K; ++x) {
-      a = fmaf(Kh[i * QR + x], Kh[j * QR + x], a);
-      b = fmaf(Qh[i * QR + x], Kh[j * QR + x], b);
+  {  // norms: four threads per row
+    const int i = tid >> 2, p = tid & 3;
+    float sq = 0.f, sk = 0.f;
+    for (int x = p * (K / 4); x < (p + 1) * (K / 4); ++x) {
+      const float a = qv(i, x), b = kv(i, x);
+      sq = fmaf(a, a, sq);
+      sk = fmaf(b, b, sk);
     }
-    KK[i * M + j] = a;
-    QK[i * M + j] = b;
-  }
-  __syncthreads();
-  // ---- T = (I + A)^-1: column j by forward substitution (64 threads)
-  if (tid < 64) {
-    const int j = tid;
-    for (int i = 0; i < 64; ++i) {
-      float x = (i == j) ? 1.f : 0.f;
-      if (i > j) {
-        const float ci = bet[i];
-        float s = 0.f;
-        for (int m = j; m < i; ++m) s = fmaf(ci * expf(gam[i] - gam[m]) * KK[i * M + m], Tm[m * M + j], s);
-        x = -s;
-      }
-      Tm[i * M + j] = (i >= j) ? x : 0.f;
+    sq = quad_sum(sq);
+    sk = quad_sum(sk);
+    if (p == 0) {
+      rq[i] = l2 ? rsqrtf(sq + GDN_L2_EPS) : 1.f;
+      rk[i] = l2 ? rsqrtf(sk + GDN_L2_EPS) : 1.f;
+    }
+    if (tid < 64) {
+      og[tid] = expf(gam[tid]);
+      sv[tid] = expf(gam[63] - gam[tid]);
     }
   }
-  for (int e = tid; e < 64 * 64; e += BT) {
-    const int i = e >> 6, j = e & 63;
-    dT[i * M + j] = 0.f;
-    dP[i * M + j] = 0.f;
+  __syncthreads();
+
+  // ---- k k^T and q k^T (exact bf16 operands): EK, A (into Tm), P
+  {
+    float ck[4][4] = {}, cq[4][4] = {};
+    auto fk = [&](int r, int x) { return kv(r0 + r, x); };
+    auto fq = [&](int r, int x) { return qv(r0 + r, x); };
+    auto fkt = [&](int x, int n) { return kv(32 * hf + n, x); };
+    wgemm<4, true, true>(ck, 0, K, fk, fkt);
+    wgemm<4, true, true>(cq, 0, K, fq, fkt);
+    cvisit(ck, [&](int, int r, int n, float x) {
+      const int i = r0 + r, j = 32 * hf + n;
+      const float ek = (j < i) ? expf(gam[i] - gam[j]) * x * rk[i] * rk[j] : 0.f;
+      EK[i * MS + j] = ek;
+      Tm[i * MS + j] = bet[i] * ek;
+    });
+    cvisit(cq, [&](int, int r, int n, float x) {
+      const int i = r0 + r, j = 32 * hf + n;
+      Pm[i * MS + j] = (j <= i) ? expf(gam[i] - gam[j]) * x * rq[i] * rk[j] : 0.f;
+    });
   }
-  float dQa[K / 4], dKa[K / 4];  // this thread's quarter of row ri of dq^, dk^
+  __syncthreads();
+
+  // ---- T = (I + A)^-1 in place: 16 x 16 diagonal blocks by substitution
+  // (thread = one column of one block), then block rows 1..3:
+  // T_ij = -D_i sum_{m=j}^{i-1} A_im T_mj.
+  if (tid < 64) {
+    const int b0 = 16 * (tid >> 4), col = tid & 15;
+    float x[16];
 #pragma unroll
-  for (int x = 0; x < K / 4; ++x) dQa[x] = dKa[x] = 0.f;
-  float dgl = 0.f;  // this thread's part of d gamma_L
+    for (int i = 0; i < 16; ++i) x[i] = (i == col) ? 1.f : 0.f;
+#pragma unroll
+    for (int j = 0; j < 15; ++j)
+#pragma unroll
+      for (int i = j + 1; i < 16; ++i) x[i] = fmaf(-Tm[(b0 + i) * MS + b0 + j], x[j], x[i]);
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) Tm[(b0 + i) * MS + b0 + col] = x[i];
+  }
   __syncthreads();
+  for (int bi = 1; bi < 4; ++bi) {
+    float *Xs = DT + warp * 16 * 17;  // the slice area is free here
+    if (warp < bi) {
+      float cs[2][4] = {};
+      auto fa = [&](int r, int m) { return Tm[(16 * bi + r) * MS + m]; };
+      auto fb = [&](int m, int n) { return Tm[m * MS + 16 * warp + n]; };
+      wgemm<2, false, false>(cs, 16 * warp, 16 * bi, fa, fb);
+      cvisit(cs, [&](int, int r, int n, float x) { Xs[r * 17 + n] = x; });
+    }
+    __syncthreads();
+    if (warp < bi) {
+      float ct[2][4] = {};
+      auto fa = [&](int r, int m) { return Tm[(16 * bi + r) * MS + 16 * bi + m]; };
+      auto fb = [&](int m, int n) { return Xs[m * 17 + n]; };
+      wgemm<2, false, false>(ct, 0, 16, fa, fb);
+      cvisit(ct, [&](int, int r, int n, float x) { Tm[(16 * bi + r) * MS + 16 * warp + n] = -x; });
+    }
+    __syncthreads();
+  }
 
   // ---- V slices
+  float accK[NH][4] = {}, accQ[NH][4] = {};  // dk^, and do h^T (dq^ before its row scale)
+  float accT[4][4] = {}, accP[4][4] = {};    // dT, dP (rows r0.., columns 32 hf..)
+  const int x0 = hf * (K / 2);
   for (int v0 = 0; v0 < V; v0 += VS) {
-    const int64_t hb = ((int64_t)(slot * HV + hv) * K) * V + v0;
-    for (int e = tid; e < K * VS; e += BT) {
-      const int x = e / VS, cc = e % VS;
-      hS[x * SR + cc] = Hs[hb + (int64_t)x * V + cc];
-      dhS[x * SR + cc] = DH[hb + (int64_t)x * V + cc];
+    const int64_t hb = ((slot * HV + hv) * K) * (int64_t)V + v0;
+    for (int e = tid; e < K * (VS / 4); e += BT) {
+      const int x = e / (VS / 4), c4 = e % (VS / 4);
+      *reinterpret_cast<float4 *>(hS + x * SS + 4 * c4) =
+          *reinterpret_cast<const float4 *>(Hs + hb + (int64_t)x * V + 4 * c4);
+      *reinterpret_cast<float4 *>(dhS + x * SS + 4 * c4) =
+          *reinterpret_cast<const float4 *>(DH + hb + (int64_t)x * V + 4 * c4);
     }
-    for (int e = tid; e < 64 * VS; e += BT) {
-      const int i = e / VS, cc = e % VS;
-      const bool live = i < L;
-      vS[i * SR + cc] = live ? bf2f(v[((trow0 + i) * HV + hv) * V + v0 + cc]) : 0.f;
-      doS[i * SR + cc] = live ? bf2f(dout[((trow0 + i) * HV + hv) * V + v0 + cc]) : 0.f;
-    }
-    __syncthreads();
-    // k^ h, q^ h, k^ dh' (64 x VS): thread (ri, 4 columns)
-    {
-      float a[4] = {0, 0, 0, 0}, b[4] = {0, 0, 0, 0}, d[4] = {0, 0, 0, 0};
-      for (int x = 0; x < K; ++x) {
-        const float kv = Kh[ri * QR + x], qv = Qh[ri * QR + x];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float hv_ = hS[x * SR + qd * 4 + u], dv_ = dhS[x * SR + qd * 4 + u];
-          a[u] = fmaf(kv, hv_, a[u]);
-          b[u] = fmaf(qv, hv_, b[u]);
-          d[u] = fmaf(kv, dv_, d[u]);
-        }
+    for (int e = tid; e < 64 * (VS / 8); e += BT) {
+      const int i = e / (VS / 8), c8 = e % (VS / 8);
+      uint4 a = make_uint4(0, 0, 0, 0), b = a;
+      if (i < L) {
+        const int64_t off = ((trow0 + i) * HV + hv) * V + v0 + 8 * c8;
+        a = *reinterpret_cast<const uint4 *>(v + off);
+        b = *reinterpret_cast<const uint4 *>(dout + off);
       }
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+      float *vd = vS + i * SS + 8 * c8, *dd = doS + i * SS + 8 * c8;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        KhS[ri * SR + qd * 4 + u] = a[u];
-        QhS[ri * SR + qd * 4 + u] = b[u];
-        KdhS[ri * SR + qd * 4 + u] = d[u];
+        vd[2 * u] = bf16lo_f(aw[u]);
+        vd[2 * u + 1] = bf16hi_f(aw[u]);
+        dd[2 * u] = bf16lo_f(bw[u]);
+        dd[2 * u + 1] = bf16hi_f(bw[u]);
       }
     }
     __syncthreads();
-    // v_new = T (diag(beta) V - diag(beta og) K^h);  dv_new = diag(sv) K^dh' + scale P^T do
+    // k^ h, q^ h, k^ dh' (columns 16 hf ..): k, q exact, h, dh' split
     {
-      float a[4] = {0, 0, 0, 0}, b[4] = {0, 0, 0, 0};
-      for (int m = 0; m <= ri; ++m) {
-        const float t = Tm[ri * M + m] * bet[m];
-        const float tg = t * og[m];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) a[u] = fmaf(t, vS[m * SR + qd * 4 + u], fmaf(-tg, KhS[m * SR + qd * 4 + u], a[u]));
-      }
-      for (int i = ri; i < 64; ++i) {
-        const float p = expf(gam[i] - gam[ri]) * QK[i * M + ri];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) b[u] = fmaf(p, doS[i * SR + qd * 4 + u], b[u]);
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        vnS[ri * SR + qd * 4 + u] = a[u];
-        dvnS[ri * SR + qd * 4 + u] = fmaf(sv[ri], KdhS[ri * SR + qd * 4 + u], scale * b[u]);
+      float ckh[2][4] = {}, cqh[2][4] = {}, ckd[2][4] = {};
+      const int n0 = 16 * hf;
+      auto fk = [&](int r, int x) { return kv(r0 + r, x); };
+      auto fq = [&](int r, int x) { return qv(r0 + r, x); };
+      auto fh = [&](int x, int n) { return hS[x * SS + n0 + n]; };
+      auto fd = [&](int x, int n) { return dhS[x * SS + n0 + n]; };
+      wgemm<2, true, false>(ckh, 0, K, fk, fh);
+      wgemm<2, true, false>(cqh, 0, K, fq, fh);
+      wgemm<2, true, false>(ckd, 0, K, fk, fd);
+      cvisit(ckh, [&](int, int r, int n, float x) {
+        const int i = r0 + r, cc = n0 + n;
+        const float kh = x * rk[i];
+        KhS[i * SS + cc] = kh;
+        MvS[i * SS + cc] = bet[i] * (vS[i * SS + cc] - og[i] * kh);
+      });
+      cvisit(ckd, [&](int, int r, int n, float x) { KdhS[(r0 + r) * SS + n0 + n] = x * rk[r0 + r]; });
+      float sq[2] = {0.f, 0.f};
+      cvisit(cqh, [&](int rh, int r, int n, float x) {
+        const int i = r0 + r;
+        sq[rh] = fmaf(x * rq[i], doS[i * SS + n0 + n], sq[rh]);
+      });
+      sq[0] = quad_sum(sq[0]);
+      sq[1] = quad_sum(sq[1]);
+      if (t4 == 0) {
+        atomicAdd(&SQ[r0 + g8], sq[0]);
+        atomicAdd(&SQ[r0 + g8 + 8], sq[1]);
       }
     }
     __syncthreads();
-    // T^T dv_new; dv = diag(beta) T^T dv_new (output)
-    {
-      float a[4] = {0, 0, 0, 0};
-      for (int m = ri; m < 64; ++m) {
-        const float t = Tm[m * M + ri];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) a[u] = fmaf(t, dvnS[m * SR + qd * 4 + u], a[u]);
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) TuS[ri * SR + qd * 4 + u] = a[u];
-      if (ri < L) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u) dv[((trow0 + ri) * HV + hv) * V + v0 + qd * 4 + u] = bet[ri] * a[u];
-      }
+    if (warp < 4) {
+      // v_new = T Mv (T lower)
+      float cc[4][4] = {};
+      auto fa = [&](int r, int m) { return Tm[(r0 + r) * MS + m]; };
+      auto fb = [&](int m, int n) { return MvS[m * SS + n]; };
+      wgemm<4, false, false>(cc, 0, r0 + 16, fa, fb);
+      cvisit(cc, [&](int, int r, int n, float x) { vnS[(r0 + r) * SS + n] = x; });
+    } else {
+      // dv_new = diag(sv) k^ dh' + scale P^T do (P^T upper)
+      float cc[4][4] = {};
+      auto fa = [&](int r, int m) { return Pm[m * MS + r0 + r]; };
+      auto fb = [&](int m, int n) { return doS[m * SS + n]; };
+      wgemm<4, false, true>(cc, r0, 64, fa, fb);
+      cvisit(cc, [&](int, int r, int n, float x) {
+        const int i = r0 + r;
+        dvnS[i * SS + n] = fmaf(sv[i], KdhS[i * SS + n], scale * x);
+      });
     }
     __syncthreads();
-    // dT += dv_new (diag(beta) V - diag(beta og) K^h)^T ;  dP += scale do v_new^T (j <= i)
-    for (int e = tid; e < 64 * 64; e += BT) {
-      const int i = e >> 6, j = e & 63;
-      float a = 0.f, b = 0.f;
+    if (warp < 4) {
+      // Tu = T^T dv_new (T^T upper); dv = diag(beta) Tu; d beta, d gamma row sums
+      float cc[4][4] = {};
+      auto fa = [&](int r, int m) { return Tm[m * MS + r0 + r]; };
+      auto fb = [&](int m, int n) { return dvnS[m * SS + n]; };
+      wgemm<4, false, false>(cc, r0, 64, fa, fb);
+      float sb[2] = {0.f, 0.f}, sg[2] = {0.f, 0.f};
+      cvisit(cc, [&](int rh, int r, int n, float x) {
+        const int i = r0 + r;
+        TuS[i * SS + n] = x;
+        if (i < L) dv[((trow0 + i) * HV + hv) * V + v0 + n] = bet[i] * x;
+        const float kh = KhS[i * SS + n];
+        sb[rh] = fmaf(x, vS[i * SS + n] - og[i] * kh, sb[rh]);
+        sg[rh] = fmaf(x, kh, sg[rh]);
+      });
 #pragma unroll
-      for (int u = 0; u < VS; ++u) {
-        a = fmaf(dvnS[i * SR + u], bet[j] * (vS[j * SR + u] - og[j] * KhS[j * SR + u]), a);
-        b = fmaf(doS[i * SR + u], vnS[j * SR + u], b);
+      for (int u = 0; u < 2; ++u) {
+        sb[u] = quad_sum(sb[u]);
+        sg[u] = quad_sum(sg[u]);
       }
-      dT[i * M + j] += a;
-      if (j <= i) dP[i * M + j] += scale * b;
-    }
-    // per-row sums (thread ri, columns of its quarter, reduced over the 4 threads of the row)
-    {
-      float sb = 0.f, sg = 0.f, sq = 0.f, sl = 0.f;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int cc = qd * 4 + u;
-        const float tu = TuS[ri * SR + cc], khv = KhS[ri * SR + cc];
-        sb = fmaf(tu, vS[ri * SR + cc] - og[ri] * khv, sb);   // d beta
-        sg = fmaf(tu, khv, sg);                                // -> d gamma (W term)
-        sq = fmaf(QhS[ri * SR + cc], doS[ri * SR + cc], sq);   // og term
-        sl = fmaf(KdhS[ri * SR + cc], vnS[ri * SR + cc], sl);  // state term
+      if (t4 == 0) {
+        DB[r0 + g8] += sb[0];
+        DB[r0 + g8 + 8] += sb[1];
+        SG[r0 + g8] += sg[0];
+        SG[r0 + g8 + 8] += sg[1];
       }
-#pragma unroll
-      for (int off = 1; off < 4; off <<= 1) {
-        sb += __shfl_xor_sync(0xffffffffu, sb, off);
-        sg += __shfl_xor_sync(0xffffffffu, sg, off);
-        sq += __shfl_xor_sync(0xffffffffu, sq, off);
-        sl += __shfl_xor_sync(0xffffffffu, sl, off);
-      }
-      if (qd == 0) {
-        dbv[ri] += sb;
-        dgam[ri] += -bet[ri] * og[ri] * sg + scale * og[ri] * sq - sv[ri] * sl;
-      }
-      if (qd == 0) dgl += sv[ri] * sl;
-    }
-    // e^{gamma_L} <dh', h> for this slice
-    {
+    } else {
+      // state terms: sum_c k^dh'_ic v_new_ic per row, and <dh', h> for d gamma_L
+      const int tt = tid - 128, i = tt >> 1, cb = (tt & 1) * (VS / 2);
       float s = 0.f;
-      for (int e = tid; e < K * VS; e += BT) s = fmaf(dhS[(e / VS) * SR + e % VS], hS[(e / VS) * SR + e % VS], s);
-      if (tid < 64) tmp[tid] = 0.f;
-      s = warp_sum(s);
-      __syncthreads();
-      if (lane == 0) atomicAdd(&tmp[0], s);
-      __syncthreads();
-      if (tid == 0) dgl += og[63] * tmp[0];
+#pragma unroll 4
+      for (int u = 0; u < VS / 2; ++u) s = fmaf(KdhS[i * SS + cb + u], vnS[i * SS + cb + u], s);
+      s += __shfl_xor_sync(0xffffffffu, s, 1);
+      if ((tt & 1) == 0) SLv[i] += s;
+      float hh = 0.f;
+      for (int e = tt; e < K * VS; e += 128) hh = fmaf(dhS[(e / VS) * SS + e % VS], hS[(e / VS) * SS + e % VS], hh);
+      hh = warp_sum(hh);
+      if (lane == 0) atomicAdd(&misc[0], hh);
     }
-    // dk^ += -diag(beta og) T^T dv_new h^T + diag(sv) v_new dh'^T ;  dq^ += scale diag(og) do h^T
-#pragma unroll
-    for (int xq = 0; xq < K / 4; ++xq) {
-      const int x = qd * (K / 4) + xq;
-      float a = 0.f, b = 0.f, d = 0.f;
-#pragma unroll
-      for (int u = 0; u < VS; ++u) {
-        a = fmaf(TuS[ri * SR + u], hS[x * SR + u], a);
-        b = fmaf(vnS[ri * SR + u], dhS[x * SR + u], b);
-        d = fmaf(doS[ri * SR + u], hS[x * SR + u], d);
+    __syncthreads();
+    {
+      // dT += dv_new Mv^T ; dP += do v_new^T (j <= i)
+      auto fa1 = [&](int r, int u) { return dvnS[(r0 + r) * SS + u]; };
+      auto fb1 = [&](int u, int n) { return MvS[(32 * hf + n) * SS + u]; };
+      wgemm<4, false, false>(accT, 0, VS, fa1, fb1);
+      if (!(hf == 1 && mt < 2)) {
+        auto fa2 = [&](int r, int u) { return doS[(r0 + r) * SS + u]; };
+        auto fb2 = [&](int u, int n) { return vnS[(32 * hf + n) * SS + u]; };
+        wgemm<4, true, false>(accP, 0, VS, fa2, fb2);
       }
-      dKa[xq] += -bet[ri] * og[ri] * a + sv[ri] * b;
-      dQa[xq] += scale * og[ri] * d;
+      // dk^ += [-diag(beta og) Tu | diag(sv) v_new] [h | dh']^T ; do h^T
+      auto fa3 = [&](int r, int u) {
+        const int i = r0 + r;
+        return u < VS ? -bet[i] * og[i] * TuS[i * SS + u] : sv[i] * vnS[i * SS + u - VS];
+      };
+      auto fb3 = [&](int u, int n) { return u < VS ? hS[(x0 + n) * SS + u] : dhS[(x0 + n) * SS + u - VS]; };
+      wgemm<NH, false, false>(accK, 0, 2 * VS, fa3, fb3);
+      auto fa4 = [&](int r, int u) { return doS[(r0 + r) * SS + u]; };
+      auto fb4 = [&](int u, int n) { return hS[(x0 + n) * SS + u]; };
+      wgemm<NH, true, false>(accQ, 0, VS, fa4, fb4);
     }
     __syncthreads();
   }
 
-  // ---- dA = -(T^T dT T^T), strictly lower.  X = dT T^T, then dA = -T^T X.
-  for (int e = tid; e < 64 * 64; e += BT) {
-    const int i = e >> 6, j = e & 63;
-    float a = 0.f;
-    for (int m = 0; m <= j; ++m) a = fmaf(dT[i * M + m], Tm[j * M + m], a);  // (T^T)_{mj} = T_{jm}, m <= j
-    X[i * M + j] = a;
-  }
+  // ---- dA = -T^T (dT T^T) (strictly lower)
+  cvisit(accT, [&](int, int r, int n, float x) { DT[(r0 + r) * MS + 32 * hf + n] = x; });
+  cvisit(accP, [&](int, int r, int n, float x) {
+    const int i = r0 + r, j = 32 * hf + n;
+    DP[i * MS + j] = (j <= i) ? scale * x : 0.f;
+  });
   __syncthreads();
-  for (int e = tid; e < 64 * 64; e += BT) {
-    const int i = e >> 6, j = e & 63;
-    float a = 0.f;
-    if (j < i)
-      for (int m = i; m < 64; ++m) a = fmaf(Tm[m * M + i], X[m * M + j], a);
-    dT[i * M + j] = -a;  // dT now holds dA (zero outside j < i)
-  }
-  __syncthreads();
-  // ---- from A_ij = beta_i e^{gamma_i-gamma_j} KK_ij (j < i) and P_ij = e^{gamma_i-gamma_j} QK_ij (j <= i)
-  // row terms (thread ri): d beta_i, d gamma_i (+), dk^_i, dq^_i
   {
-    float sb = 0.f, sgr = 0.f;
-    for (int j = qd; j < 64; j += 4) {
-      const float e = expf(gam[ri] - gam[j]);
-      if (j < ri) {
-        const float da = dT[ri * M + j];
-        sb = fmaf(da, e * KK[ri * M + j], sb);
-        sgr = fmaf(da, bet[ri] * e * KK[ri * M + j], sgr);
+    float cc[4][4] = {};
+    auto fa = [&](int r, int m) { return DT[(r0 + r) * MS + m]; };
+    auto fb = [&](int m, int n) { return Tm[(32 * hf + n) * MS + m]; };
+    wgemm<4, false, false>(cc, 0, 32 * hf + 32, fa, fb);
+    cvisit(cc, [&](int, int r, int n, float x) { Xm[(r0 + r) * MS + 32 * hf + n] = x; });
+  }
+  __syncthreads();
+  {
+    float cc[4][4] = {};
+    if (!(hf == 1 && mt < 2)) {
+      auto fa = [&](int r, int m) { return Tm[m * MS + r0 + r]; };
+      auto fb = [&](int m, int n) { return Xm[m * MS + 32 * hf + n]; };
+      wgemm<4, false, false>(cc, r0, 64, fa, fb);
+    }
+    cvisit(cc, [&](int, int r, int n, float x) {
+      const int i = r0 + r, j = 32 * hf + n;
+      DT[i * MS + j] = (j < i) ? -x : 0.f;
+    });
+  }
+  __syncthreads();
+  // ---- through A_ij = beta_i EK_ij and P_ij: d beta, d gamma (row +, column -),
+  // and the coefficient tiles of the last products.
+  {
+    const int i = tid >> 2, q4 = tid & 3;
+    float sb = 0.f, sr = 0.f;
+    for (int m = 0; m < 16; ++m) {
+      const int j = q4 + 4 * m;
+      const float da = DT[i * MS + j], dp = DP[i * MS + j];
+      const float term = fmaf(da * bet[i], EK[i * MS + j], dp * Pm[i * MS + j]);
+      sb = fmaf(da, EK[i * MS + j], sb);
+      sr += term;
+      atomicAdd(&DG[j], -term);
+      float s1 = 0.f, s2 = 0.f, s3 = 0.f;
+      if (j < i) {
+        const float e = expf(gam[i] - gam[j]);
+        s1 = da * bet[i] * e * rk[j];
+        s3 = dp * e * rk[j];
+      } else if (j > i) {
+        const float e = expf(gam[j] - gam[i]);
+        s1 = DT[j * MS + i] * bet[j] * e * rk[j];
+        s2 = DP[j * MS + i] * e * rq[j];
+      } else {
+        s2 = dp * rq[j];
+        s3 = dp * rk[j];
       }
-      if (j <= ri) sgr = fmaf(dP[ri * M + j], e * QK[ri * M + j], sgr);
+      S1[i * MS + j] = s1;
+      S2[i * MS + j] = s2;
+      S3[i * MS + j] = s3;
     }
+    sb = quad_sum(sb);
+    sr = quad_sum(sr);
+    if (q4 == 0) {
+      DB[i] += sb;
+      atomicAdd(&DG[i], sr);
+    }
+  }
+  __syncthreads();
+  // ---- dk^ += [S1 | S2] [k; q] ; dq^ = scale og (do h^T) + S3 k
+  {
+    auto fa = [&](int r, int m) { return m < 64 ? S1[(r0 + r) * MS + m] : S2[(r0 + r) * MS + m - 64]; };
+    auto fb = [&](int m, int n) { return m < 64 ? kv(m, x0 + n) : qv(m - 64, x0 + n); };
+    wgemm<NH, false, true>(accK, 0, 128, fa, fb);
+    cvisit(accQ, [&](int, int r, int, float &x) { x *= scale * og[r0 + r]; });
+    auto fa2 = [&](int r, int m) { return S3[(r0 + r) * MS + m]; };
+    auto fb2 = [&](int m, int n) { return kv(m, x0 + n); };
+    wgemm<NH, false, true>(accQ, 0, r0 + 16, fa2, fb2);
+  }
+  // ---- through the L2 norms (dx = r (dx^ - x^ (x^ . dx^))), summed over the group's value heads
+  {
+    float pq[2] = {0.f, 0.f}, pk[2] = {0.f, 0.f};
+    cvisit(accQ, [&](int rh, int r, int n, float x) { pq[rh] = fmaf(qv(r0 + r, x0 + n), x, pq[rh]); });
+    cvisit(accK, [&](int rh, int r, int n, float x) { pk[rh] = fmaf(kv(r0 + r, x0 + n), x, pk[rh]); });
 #pragma unroll
-    for (int off = 1; off < 4; off <<= 1) {
-      sb += __shfl_xor_sync(0xffffffffu, sb, off);
-      sgr += __shfl_xor_sync(0xffffffffu, sgr, off);
+    for (int u = 0; u < 2; ++u) {
+      pq[u] = quad_sum(pq[u]);
+      pk[u] = quad_sum(pk[u]);
     }
-    if (qd == 0) {
-      dbv[ri] += sb;
-      dgam[ri] += sgr;
-    }
-  }
-  __syncthreads();
-  // column terms: d gamma_j (-)
-  if (tid < 64) {
-    const int j = tid;
-    float s = 0.f;
-    for (int i = j; i < 64; ++i) {
-      const float e = expf(gam[i] - gam[j]);
-      if (j < i) s = fmaf(dT[i * M + j], bet[i] * e * KK[i * M + j], s);
-      s = fmaf(dP[i * M + j], e * QK[i * M + j], s);
-    }
-    dgam[j] -= s;
-  }
-  // dk^_i += sum_{j<i} dA_ij beta_i e_ij k^_j + sum_{m>i} dA_mi beta_m e_mi k^_m + sum_{m>=i} dP_mi e_mi q^_m
-  // dq^_i += sum_{j<=i} dP_ij e_ij k^_j
-  for (int j = 0; j < 64; ++j) {
-    const float eij = expf(gam[ri] - gam[j]);
-    const float cA = (j < ri) ? dT[ri * M + j] * bet[ri] * eij : 0.f;
-    const float cP = (j <= ri) ? dP[ri * M + j] * eij : 0.f;
-    const float eji = expf(gam[j] - gam[ri]);
-    const float cA2 = (j > ri) ? dT[j * M + ri] * bet[j] * eji : 0.f;
-    const float cP2 = (j >= ri) ? dP[j * M + ri] * eji : 0.f;
-#pragma unroll
-    for (int xq = 0; xq < K / 4; ++xq) {
-      const int x = qd * (K / 4) + xq;
-      dKa[xq] = fmaf(cA, Kh[j * QR + x], fmaf(cA2, Kh[j * QR + x], fmaf(cP2, Qh[j * QR + x], dKa[xq])));
-      dQa[xq] = fmaf(cP, Kh[j * QR + x], dQa[xq]);
+    if (t4 == 0) {
+      atomicAdd(&PQ[r0 + g8], pq[0]);
+      atomicAdd(&PQ[r0 + g8 + 8], pq[1]);
+      atomicAdd(&PK[r0 + g8], pk[0]);
+      atomicAdd(&PK[r0 + g8 + 8], pk[1]);
     }
   }
   __syncthreads();
-  // ---- d gamma_L, then dg = reverse cumsum of d gamma over the chunk
-  dgl = warp_sum(dgl);
-  if (tid < 64) tmp[tid] = 0.f;
-  __syncthreads();
-  if (lane == 0) atomicAdd(&tmp[0], dgl);
-  __syncthreads();
-  if (tid == 0) dgam[63] += tmp[0];
-  __syncthreads();
+  cvisit(accQ, [&](int, int r, int n, float x) {
+    const int i = r0 + r, xx = x0 + n;
+    if (i < L) {
+      const float gq = l2 ? rq[i] * (x - rq[i] * rq[i] * qv(i, xx) * PQ[i]) : x;
+      atomicAdd(dq + ((trow0 + i) * H + h) * K + xx, gq);
+    }
+  });
+  cvisit(accK, [&](int, int r, int n, float x) {
+    const int i = r0 + r, xx = x0 + n;
+    if (i < L) {
+      const float gk = l2 ? rk[i] * (x - rk[i] * rk[i] * kv(i, xx) * PK[i]) : x;
+      atomicAdd(dk + ((trow0 + i) * H + h) * K + xx, gk);
+    }
+  });
+  // ---- d gamma, then dg = reverse cumsum over the chunk; d beta
   if (warp == 0) {
-    // reverse inclusive scan over 64 rows, two per lane
-    const float x0 = dgam[2 * lane], x1 = dgam[2 * lane + 1];
-    float s = x0 + x1;
+    float d[2], dl = 0.f;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int i = 2 * lane + u;
+      d[u] = DG[i] - bet[i] * og[i] * SG[i] + scale * og[i] * SQ[i] - sv[i] * SLv[i];
+      dl = fmaf(sv[i], SLv[i], dl);
+    }
+    dl = warp_sum(dl) + og[63] * misc[0];  // d gamma_L
+    if (lane == 31) d[1] += dl;
+    float s = d[0] + d[1];
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const float y = __shfl_down_sync(0xffffffffu, s, off);
       if (lane + off < 32) s += y;
     }
-    const float r1 = s - x0;  // sum over rows >= 2 lane + 1
+    const float s1 = s - d[0];  // rows >= 2 lane + 1
     if (2 * lane < L) {
       dg[(trow0 + 2 * lane) * HV + hv] = s;
-      dbeta[(trow0 + 2 * lane) * HV + hv] = dbv[2 * lane];
+      dbeta[(trow0 + 2 * lane) * HV + hv] = DB[2 * lane];
     }
     if (2 * lane + 1 < L) {
-      dg[(trow0 + 2 * lane + 1) * HV + hv] = r1;
-      dbeta[(trow0 + 2 * lane + 1) * HV + hv] = dbv[2 * lane + 1];
-    }
-  }
-  // ---- through the L2 norms: dx = r (dx^ - x^ (x^ . dx^)); summed over the group's value heads
-  {
-    float pq = 0.f, pk = 0.f;
-#pragma unroll
-    for (int xq = 0; xq < K / 4; ++xq) {
-      const int x = qd * (K / 4) + xq;
-      pq = fmaf(Qh[ri * QR + x], dQa[xq], pq);
-      pk = fmaf(Kh[ri * QR + x], dKa[xq], pk);
-    }
-#pragma unroll
-    for (int off = 1; off < 4; off <<= 1) {
-      pq += __shfl_xor_sync(0xffffffffu, pq, off);
-      pk += __shfl_xor_sync(0xffffffffu, pk, off);
-    }
-    if (ri < L) {
-      float *dqr = dq + ((trow0 + ri) * H + h) * K + qd * (K / 4);
-      float *dkr = dk + ((trow0 + ri) * H + h) * K + qd * (K / 4);
-#pragma unroll
-      for (int xq = 0; xq < K / 4; ++xq) {
-        const int x = qd * (K / 4) + xq;
-        const float gq = l2 ? rq[ri] * (dQa[xq] - Qh[ri * QR + x] * pq) : dQa[xq];
-        const float gk = l2 ? rk[ri] * (dKa[xq] - Kh[ri * QR + x] * pk) : dKa[xq];
-        atomicAdd(dqr + xq, gq);
-        atomicAdd(dkr + xq, gk);
-      }
+      dg[(trow0 + 2 * lane + 1) * HV + hv] = s1;
+      dbeta[(trow0 + 2 * lane + 1) * HV + hv] = DB[2 * lane + 1];
     }
   }
 }
