@@ -57,170 +57,11 @@ __device__ __forceinline__ float tile64(const unsigned char *t, int i, int j) {
   return bf2f(*reinterpret_cast<const uint16_t *>(t + sw128(i, j >> 3) + (j & 7) * 2));
 }
 
-// ------------------------------------------------------------------ dh walk
-// One CTA per (32-column slice of V, value head, sequence): dh (K x 32 fp32)
-// lives in registers, thread (row r, columns c0 .. c0 + CPT); per chunk, last
-// first, K, Q, W, P, the scalars and the do slice are staged in shared memory
-// (cp.async, double buffered).
-template <int K>
-struct DhLay {
-  static constexpr int KROW = K * 2 + 16;             // padded bf16 row of K keys
-  static constexpr int OFF_K = 0;                     // raw K [64][KROW]
-  static constexpr int OFF_Q = OFF_K + 64 * KROW;     // raw Q [64][KROW]
-  static constexpr int OFF_REC = OFF_Q + 64 * KROW;   // record bytes W | PH | PL (contiguous in the record)
-  static constexpr int REC_BYTES = Rec<K>::TS;        // W + PH + PL
-  static constexpr int OFF_SC = OFF_REC + REC_BYTES;  // record scalars (1 KB)
-  static constexpr int OFF_DO = OFF_SC + 1024;        // do slice [64][32] bf16
-  static constexpr int STAGE = OFF_DO + 64 * 64;
-  static constexpr int OFF_DHS = 2 * STAGE;           // dh' [K][32] fp32
-  static constexpr int OFF_DVN = OFF_DHS + K * 32 * 4;  // dv_new [64][32] fp32
-  static constexpr int BYTES = OFF_DVN + 64 * 32 * 4;
-  static_assert(STAGE % 16 == 0, "16-byte copies");
-};
-
-template <int K>
-__global__ void __launch_bounds__(BT, 1) chunk_dh_kernel(
-    const uint16_t *__restrict__ q, const uint16_t *__restrict__ k, const uint16_t *__restrict__ dout,
-    const unsigned char *__restrict__ ws, float *__restrict__ DH, const float *__restrict__ dht,
-    float *__restrict__ dh0, float scale, const int32_t *__restrict__ cu, int T, int H, int HV, int V,
-    int32_t *dev_status) {
-  using Ly = DhLay<K>;
-  using R = Rec<K>;
-  constexpr int TPR = BT / K;   // threads per state row
-  constexpr int CPT = 32 / TPR; // columns per thread
-  extern __shared__ __align__(16) unsigned char smem[];
-  const int vt0 = blockIdx.x * 32, hv = blockIdx.y, n = blockIdx.z;
-  const int h = hv / (HV / H);
-  const int tid = threadIdx.x;
-  const int r = tid / TPR, c0 = (tid % TPR) * CPT;
-
-  int64_t tok0, len;
-  if (!seq_bounds(cu, n, T, tok0, len)) {
-    if (tid == 0) set_status(dev_status, GDN_DEV_BAD_CU_SEQLENS);
-    return;
-  }
-  const int NC = chunks_of(len);
-  const int64_t cb = chunk_base(cu, n, T);
-  const int64_t sidx = ((int64_t)n * HV + hv) * K + r;
-  float dh[CPT];
-#pragma unroll
-  for (int j = 0; j < CPT; ++j) dh[j] = dht ? dht[sidx * V + vt0 + c0 + j] : 0.f;
-
-  auto issue = [&](int c, int st) {
-    unsigned char *S = smem + st * Ly::STAGE;
-    const int64_t trow = tok0 + (int64_t)c * C;
-    const int64_t rem = len - (int64_t)c * C;
-    const int L = rem < C ? (int)rem : C;
-    // K and Q rows: K * 2 bytes = K / 8 chunks of 16 bytes each
-    for (int e = tid; e < 64 * (K / 8); e += BT) {
-      const int row = e / (K / 8), ch = e % (K / 8);
-      const bool ok = row < L;
-      const int64_t g = ok ? ((trow + row) * H + h) * K + ch * 8 : 0;
-      cp_async16(S + Ly::OFF_K + row * Ly::KROW + ch * 16, k + g, ok);
-      cp_async16(S + Ly::OFF_Q + row * Ly::KROW + ch * 16, q + g, ok);
-    }
-    const unsigned char *rec = ws + ((size_t)(cb + c) * HV + hv) * R::BYTES;
-    for (int e = tid; e < Ly::REC_BYTES / 16; e += BT) cp_async16(S + Ly::OFF_REC + e * 16, rec + e * 16, true);
-    for (int e = tid; e < 1024 / 16; e += BT) cp_async16(S + Ly::OFF_SC + e * 16, rec + R::SC + e * 16, true);
-    for (int e = tid; e < 64 * 4; e += BT) {
-      const int row = e >> 2, ch = e & 3;
-      const bool ok = row < L;
-      const int64_t g = ok ? ((trow + row) * HV + hv) * V + vt0 + ch * 8 : 0;
-      cp_async16(S + Ly::OFF_DO + row * 64 + ch * 16, dout + g, ok);
-    }
-    cp_async_commit();
-  };
-
-  float *dhs = reinterpret_cast<float *>(smem + Ly::OFF_DHS);
-  float *dvn = reinterpret_cast<float *>(smem + Ly::OFF_DVN);
-  if (NC > 0) issue(NC - 1, 0);
-  for (int c = NC - 1; c >= 0; --c) {
-    const int st = (NC - 1 - c) & 1;
-    if (c > 0) {
-      issue(c - 1, st ^ 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    // dh' of this chunk: to the workspace and to shared memory.
-    {
-      float *dst = DH + (((cb + c) * HV + hv) * K + r) * (int64_t)V + vt0 + c0;
-#pragma unroll
-      for (int j = 0; j < CPT; ++j) {
-        dst[j] = dh[j];
-        dhs[r * 32 + c0 + j] = dh[j];
-      }
-    }
-    __syncthreads();
-    const unsigned char *S = smem + st * Ly::STAGE;
-    const float *sc = reinterpret_cast<const float *>(S + Ly::OFF_SC);
-    const uint16_t *Ks = reinterpret_cast<const uint16_t *>(S + Ly::OFF_K);
-    const uint16_t *Qs = reinterpret_cast<const uint16_t *>(S + Ly::OFF_Q);
-    const uint16_t *Ds = reinterpret_cast<const uint16_t *>(S + Ly::OFF_DO);
-    const unsigned char *PH = S + Ly::OFF_REC + (R::PH - R::W);
-    const unsigned char *PL = S + Ly::OFF_REC + (R::PL - R::W);
-    // dv_new[j][8 columns] = sv_j (k_j . dh'[:, c]) + scale sum_{i >= j} P_ij do_i[c]
-    {
-      const int j = tid >> 2, cq = (tid & 3) * 8;
-      float a[8], b[8];
-#pragma unroll
-      for (int x = 0; x < 8; ++x) a[x] = b[x] = 0.f;
-      const uint16_t *kr = Ks + j * (Ly::KROW / 2);
-      for (int key = 0; key < K; ++key) {
-        const float kv = bf2f(kr[key]);
-        const float *dr = dhs + key * 32 + cq;
-#pragma unroll
-        for (int x = 0; x < 8; ++x) a[x] = fmaf(kv, dr[x], a[x]);
-      }
-      for (int i = j; i < 64; ++i) {
-        const float p = tile64(PH, i, j) + tile64(PL, i, j);
-        const uint16_t *dr = Ds + i * 32 + cq;
-#pragma unroll
-        for (int x = 0; x < 8; ++x) b[x] = fmaf(p, bf2f(dr[x]), b[x]);
-      }
-      const float sv = sc[RS_SV + j];
-#pragma unroll
-      for (int x = 0; x < 8; ++x) dvn[j * 32 + cq + x] = fmaf(sv, a[x], scale * b[x]);
-    }
-    __syncthreads();
-    // dh = e^{gamma_L} dh' + scale sum_i og_i q_i[r] do_i - sum_j W_j[r] dv_new_j
-    {
-      float a[CPT], b[CPT];
-#pragma unroll
-      for (int x = 0; x < CPT; ++x) a[x] = b[x] = 0.f;
-      const unsigned char *Wt = S + Ly::OFF_REC;
-      for (int i = 0; i < 64; ++i) {
-        const float qo = sc[RS_OG + i] * bf2f(Qs[i * (Ly::KROW / 2) + r]);
-        const float wv = rec_w(Wt, i, r);
-        const uint16_t *dr = Ds + i * 32 + c0;
-        const float *vr = dvn + i * 32 + c0;
-#pragma unroll
-        for (int x = 0; x < CPT; ++x) {
-          a[x] = fmaf(qo, bf2f(dr[x]), a[x]);
-          b[x] = fmaf(wv, vr[x], b[x]);
-        }
-      }
-      const float dL = sc[RS_DL];
-#pragma unroll
-      for (int x = 0; x < CPT; ++x) dh[x] = fmaf(dL, dh[x], fmaf(scale, a[x], -b[x]));
-    }
-    __syncthreads();  // this stage is refilled by the next issue
-  }
-  if (dh0) {
-#pragma unroll
-    for (int j = 0; j < CPT; ++j) dh0[sidx * V + vt0 + c0 + j] = dh[j];
-  }
-}
-
-// ---------------------------------------------------------- chunk gradients
-// One CTA per (chunk, value head).  Every product runs on the tensor cores as
-// warp-level mma.sync m16n8k8 in tf32 with fp32 accumulation.  A computed fp32
+// ------------------------------------------------------------- mma helpers
+// Warp-level mma.sync m16n8k8 in tf32 with fp32 accumulation.  A computed fp32
 // operand is split into tf32 hi + lo parts and the product takes hi*hi + hi*lo
-// + lo*hi, which keeps fp32-level accuracy; an operand holding raw bf16 inputs
-// (q, k, v, do) is exact in tf32 and has no low part.  Warp w owns the 16-row
-// tile mt = w & 3 of a 64-row result and, where the result is wider than one
-// warp's share, the column half hf = w >> 2.
-
+// + lo*hi, which keeps fp32-level accuracy; an operand holding raw bf16 values
+// is exact in tf32 and has no low part.
 __device__ __forceinline__ uint32_t tf32_rna(float x) {
   uint32_t r;
   asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
@@ -275,6 +116,161 @@ __device__ __forceinline__ float quad_sum(float x) {
 constexpr int VS = 32;  // V columns per slice
 constexpr int MS = 68;  // fp32 row stride of a 64 x 64 tile
 constexpr int SS = 36;  // fp32 row stride of a 32-column slice
+
+// ------------------------------------------------------------------ dh walk
+// One CTA per (32-column slice of V, value head, sequence), last chunk first.
+// dh (K x 32 fp32) lives in the mma accumulators of the eight warps (warp w:
+// rows of tile w % (K / 16), a share of the columns); per chunk K, Q, W, P,
+// the scalars and the do slice are staged in shared memory (cp.async, double
+// buffered).  Both products of a chunk run on mma.sync tf32: the raw bf16 k,
+// q, W, P hi / lo and do are exact in tf32, the computed dh' and dv_new are
+// split hi + lo.
+template <int K>
+struct DhLay {
+  static constexpr int KROW = K * 2 + 16;             // padded bf16 row of K keys
+  static constexpr int OFF_K = 0;                     // raw K [64][KROW]
+  static constexpr int OFF_Q = OFF_K + 64 * KROW;     // raw Q [64][KROW]
+  static constexpr int OFF_REC = OFF_Q + 64 * KROW;   // record bytes W | PH | PL (contiguous in the record)
+  static constexpr int REC_BYTES = Rec<K>::TS;        // W + PH + PL
+  static constexpr int OFF_SC = OFF_REC + REC_BYTES;  // record scalars (1 KB)
+  static constexpr int OFF_DO = OFF_SC + 1024;        // do slice [64][32] bf16
+  static constexpr int STAGE = OFF_DO + 64 * 64;
+  static constexpr int OFF_DHS = 2 * STAGE;           // dh' [K][SS] fp32
+  static constexpr int OFF_DVN = OFF_DHS + K * SS * 4;  // dv_new [64][SS] fp32
+  static constexpr int BYTES = OFF_DVN + 64 * SS * 4;
+  static_assert(STAGE % 16 == 0, "16-byte copies");
+};
+
+template <int K>
+__global__ void __launch_bounds__(BT, 1) chunk_dh_kernel(
+    const uint16_t *__restrict__ q, const uint16_t *__restrict__ k, const uint16_t *__restrict__ dout,
+    const unsigned char *__restrict__ ws, float *__restrict__ DH, const float *__restrict__ dht,
+    float *__restrict__ dh0, float scale, const int32_t *__restrict__ cu, int T, int H, int HV, int V,
+    int32_t *dev_status) {
+  using Ly = DhLay<K>;
+  using R = Rec<K>;
+  constexpr int KE = Ly::KROW / 2;  // bf16 elements per staged K / Q row
+  constexpr int MTK = K / 16;       // row tiles of dh
+  constexpr int WPM = 8 / MTK;      // warps per row tile
+  constexpr int NTD = 4 / WPM;      // n-tiles (8 columns) per warp
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int vt0 = blockIdx.x * 32, hv = blockIdx.y, n = blockIdx.z;
+  const int h = hv / (HV / H);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int dm0 = 16 * (warp % MTK), dc0 = 8 * NTD * (warp / MTK);  // this warp's block of dh
+  const int mt = warp & 3, r0 = 16 * mt, hf = warp >> 2;              // its block of dv_new
+
+  int64_t tok0, len;
+  if (!seq_bounds(cu, n, T, tok0, len)) {
+    if (tid == 0) set_status(dev_status, GDN_DEV_BAD_CU_SEQLENS);
+    return;
+  }
+  const int NC = chunks_of(len);
+  const int64_t cb = chunk_base(cu, n, T);
+  const int64_t sbase = ((int64_t)n * HV + hv) * K;
+  float dh[NTD][4];
+  cvisit(dh, [&](int, int r, int c, float &x) {
+    x = dht ? dht[(sbase + dm0 + r) * V + vt0 + dc0 + c] : 0.f;
+  });
+
+  auto issue = [&](int c, int st) {
+    unsigned char *S = smem + st * Ly::STAGE;
+    const int64_t trow = tok0 + (int64_t)c * C;
+    const int64_t rem = len - (int64_t)c * C;
+    const int L = rem < C ? (int)rem : C;
+    for (int e = tid; e < 64 * (K / 8); e += BT) {
+      const int row = e / (K / 8), ch = e % (K / 8);
+      const bool ok = row < L;
+      const int64_t g = ok ? ((trow + row) * H + h) * K + ch * 8 : 0;
+      cp_async16(S + Ly::OFF_K + row * Ly::KROW + ch * 16, k + g, ok);
+      cp_async16(S + Ly::OFF_Q + row * Ly::KROW + ch * 16, q + g, ok);
+    }
+    const unsigned char *rec = ws + ((size_t)(cb + c) * HV + hv) * R::BYTES;
+    for (int e = tid; e < Ly::REC_BYTES / 16; e += BT) cp_async16(S + Ly::OFF_REC + e * 16, rec + e * 16, true);
+    for (int e = tid; e < 1024 / 16; e += BT) cp_async16(S + Ly::OFF_SC + e * 16, rec + R::SC + e * 16, true);
+    for (int e = tid; e < 64 * 4; e += BT) {
+      const int row = e >> 2, ch = e & 3;
+      const bool ok = row < L;
+      const int64_t g = ok ? ((trow + row) * HV + hv) * V + vt0 + ch * 8 : 0;
+      cp_async16(S + Ly::OFF_DO + row * 64 + ch * 16, dout + g, ok);
+    }
+    cp_async_commit();
+  };
+
+  float *dhs = reinterpret_cast<float *>(smem + Ly::OFF_DHS);
+  float *dvn = reinterpret_cast<float *>(smem + Ly::OFF_DVN);
+  if (NC > 0) issue(NC - 1, 0);
+  for (int c = NC - 1; c >= 0; --c) {
+    const int st = (NC - 1 - c) & 1;
+    if (c > 0) {
+      issue(c - 1, st ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    // dh' of this chunk: to the workspace and to shared memory.
+    {
+      float *dst = DH + (((cb + c) * HV + hv) * K) * (int64_t)V + vt0;
+      cvisit(dh, [&](int, int r, int cc, float x) {
+        const int row = dm0 + r, col = dc0 + cc;
+        dst[(int64_t)row * V + col] = x;
+        dhs[row * SS + col] = x;
+      });
+    }
+    __syncthreads();
+    const unsigned char *S = smem + st * Ly::STAGE;
+    const float *sc = reinterpret_cast<const float *>(S + Ly::OFF_SC);
+    const uint16_t *Ks = reinterpret_cast<const uint16_t *>(S + Ly::OFF_K);
+    const uint16_t *Qs = reinterpret_cast<const uint16_t *>(S + Ly::OFF_Q);
+    const uint16_t *Ds = reinterpret_cast<const uint16_t *>(S + Ly::OFF_DO);
+    const unsigned char *Wt = S + Ly::OFF_REC;
+    const unsigned char *PH = S + Ly::OFF_REC + (R::PH - R::W);
+    const unsigned char *PL = S + Ly::OFF_REC + (R::PL - R::W);
+    // dv_new = diag(sv) K dh' + scale (P_hi + P_lo)^T do   (sv carries 1/||k||)
+    {
+      float ca[2][4] = {}, cp[2][4] = {};
+      const int n0 = 16 * hf;
+      auto fk = [&](int r, int x) { return bf2f(Ks[(r0 + r) * KE + x]); };
+      auto fd = [&](int x, int nn) { return dhs[x * SS + n0 + nn]; };
+      wgemm<2, true, false>(ca, 0, K, fk, fd);
+      auto fph = [&](int r, int i) { return tile64(PH, i, r0 + r); };
+      auto fpl = [&](int r, int i) { return tile64(PL, i, r0 + r); };
+      auto fo = [&](int i, int nn) { return bf2f(Ds[i * 32 + n0 + nn]); };
+      wgemm<2, true, true>(cp, r0, 64, fph, fo);
+      wgemm<2, true, true>(cp, r0, 64, fpl, fo);
+      const int g = (tid & 31) >> 2, t = tid & 3;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j = r0 + g + 8 * (e >> 1);
+          dvn[j * SS + n0 + 8 * nt + 2 * t + (e & 1)] = fmaf(sc[RS_SV + j], ca[nt][e], scale * cp[nt][e]);
+        }
+    }
+    __syncthreads();
+    // dh = e^{gamma_L} dh' + Q^T diag(scale og) do - W^T dv_new   (og carries 1/||q||)
+    {
+      const float dL = sc[RS_DL];
+      cvisit(dh, [&](int, int, int, float &x) { x *= dL; });
+      auto fq = [&](int r, int i) { return bf2f(Qs[i * KE + dm0 + r]); };
+      auto fo = [&](int i, int cc) { return scale * sc[RS_OG + i] * bf2f(Ds[i * 32 + dc0 + cc]); };
+      wgemm<NTD, true, false>(dh, 0, 64, fq, fo);
+      auto fw = [&](int r, int j) { return rec_w(Wt, j, dm0 + r); };
+      auto fv = [&](int j, int cc) { return -dvn[j * SS + dc0 + cc]; };
+      wgemm<NTD, true, false>(dh, 0, 64, fw, fv);
+    }
+    __syncthreads();  // this stage is refilled by the next issue
+  }
+  if (dh0) {
+    cvisit(dh, [&](int, int r, int cc, float x) { dh0[(sbase + dm0 + r) * V + vt0 + dc0 + cc] = x; });
+  }
+}
+
+// ---------------------------------------------------------- chunk gradients
+// One CTA per (chunk, value head); every product on the tensor cores with the
+// helpers above (raw q, k, v, do exact, computed operands split).  Warp w owns
+// the 16-row tile mt = w & 3 of a 64-row result and, where the result is wider
+// than one warp's share, the column half hf = w >> 2.
 
 template <int K>
 struct GradLay {
