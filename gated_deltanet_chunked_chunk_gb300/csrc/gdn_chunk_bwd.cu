@@ -80,6 +80,7 @@ __device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], 
 template <int NT, bool AX, bool BX, class FA, class FB>
 __device__ __forceinline__ void wgemm(float (&c)[NT][4], int k0, int k1, FA fa, FB fb) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll 2
   for (int k = k0; k < k1; k += 8) {
     const float av[4] = {fa(g, k + t), fa(g + 8, k + t), fa(g, k + t + 4), fa(g + 8, k + t + 4)};
     uint32_t ah[4], al[4];
@@ -88,14 +89,25 @@ __device__ __forceinline__ void wgemm(float (&c)[NT][4], int k0, int k1, FA fa, 
       ah[e] = AX ? __float_as_uint(av[e]) : tf32_rna(av[e]);
       al[e] = AX ? 0u : tf32_rna(av[e] - __uint_as_float(ah[e]));
     }
+    uint32_t bh[NT][2], bl[NT][2];
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
       const float b0 = fb(k + t, 8 * n + g), b1 = fb(k + t + 4, 8 * n + g);
-      const uint32_t bh0 = BX ? __float_as_uint(b0) : tf32_rna(b0);
-      const uint32_t bh1 = BX ? __float_as_uint(b1) : tf32_rna(b1);
-      mma_tf32(c[n], ah, bh0, bh1);
-      if (!BX) mma_tf32(c[n], ah, tf32_rna(b0 - __uint_as_float(bh0)), tf32_rna(b1 - __uint_as_float(bh1)));
-      if (!AX) mma_tf32(c[n], al, bh0, bh1);
+      bh[n][0] = BX ? __float_as_uint(b0) : tf32_rna(b0);
+      bh[n][1] = BX ? __float_as_uint(b1) : tf32_rna(b1);
+      bl[n][0] = BX ? 0u : tf32_rna(b0 - __uint_as_float(bh[n][0]));
+      bl[n][1] = BX ? 0u : tf32_rna(b1 - __uint_as_float(bh[n][1]));
+    }
+    // passes outermost, so that consecutive products go to different accumulators
+#pragma unroll
+    for (int n = 0; n < NT; ++n) mma_tf32(c[n], ah, bh[n][0], bh[n][1]);
+    if (!BX) {
+#pragma unroll
+      for (int n = 0; n < NT; ++n) mma_tf32(c[n], ah, bl[n][0], bl[n][1]);
+    }
+    if (!AX) {
+#pragma unroll
+      for (int n = 0; n < NT; ++n) mma_tf32(c[n], al, bh[n][0], bh[n][1]);
     }
   }
 }
@@ -133,11 +145,15 @@ struct DhLay {
   static constexpr int OFF_REC = OFF_Q + 64 * KROW;   // record bytes W | PH | PL (contiguous in the record)
   static constexpr int REC_BYTES = Rec<K>::TS;        // W + PH + PL
   static constexpr int OFF_SC = OFF_REC + REC_BYTES;  // record scalars (1 KB)
-  static constexpr int OFF_DO = OFF_SC + 1024;        // do slice [64][32] bf16
-  static constexpr int STAGE = OFF_DO + 64 * 64;
-  static constexpr int OFF_DHS = 2 * STAGE;           // dh' [K][SS] fp32
-  static constexpr int OFF_DVN = OFF_DHS + K * SS * 4;  // dv_new [64][SS] fp32
-  static constexpr int BYTES = OFF_DVN + 64 * SS * 4;
+  static constexpr int DOROW = 96;                    // padded bf16 row of the 32-column do slice
+  static constexpr int OFF_DO = OFF_SC + 1024;        // do slice [64][DOROW bytes]
+  static constexpr int STAGE = OFF_DO + 64 * DOROW;
+  // dh' and dv_new are read as B operands (row k + t, column g of a fragment):
+  // a row stride of 8 (mod 32) words keeps those reads free of bank conflicts.
+  static constexpr int BS = 40;
+  static constexpr int OFF_DHS = 2 * STAGE;           // dh' [K][BS] fp32
+  static constexpr int OFF_DVN = OFF_DHS + K * BS * 4;  // dv_new [64][BS] fp32
+  static constexpr int BYTES = OFF_DVN + 64 * BS * 4;
   static_assert(STAGE % 16 == 0, "16-byte copies");
 };
 
@@ -192,7 +208,7 @@ __global__ void __launch_bounds__(BT, 1) chunk_dh_kernel(
       const int row = e >> 2, ch = e & 3;
       const bool ok = row < L;
       const int64_t g = ok ? ((trow + row) * HV + hv) * V + vt0 + ch * 8 : 0;
-      cp_async16(S + Ly::OFF_DO + row * 64 + ch * 16, dout + g, ok);
+      cp_async16(S + Ly::OFF_DO + row * Ly::DOROW + ch * 16, dout + g, ok);
     }
     cp_async_commit();
   };
@@ -214,7 +230,7 @@ __global__ void __launch_bounds__(BT, 1) chunk_dh_kernel(
       cvisit(dh, [&](int, int r, int cc, float x) {
         const int row = dm0 + r, col = dc0 + cc;
         dst[(int64_t)row * V + col] = x;
-        dhs[row * SS + col] = x;
+        dhs[row * Ly::BS + col] = x;
       });
     }
     __syncthreads();
@@ -231,11 +247,11 @@ __global__ void __launch_bounds__(BT, 1) chunk_dh_kernel(
       float ca[2][4] = {}, cp[2][4] = {};
       const int n0 = 16 * hf;
       auto fk = [&](int r, int x) { return bf2f(Ks[(r0 + r) * KE + x]); };
-      auto fd = [&](int x, int nn) { return dhs[x * SS + n0 + nn]; };
+      auto fd = [&](int x, int nn) { return dhs[x * Ly::BS + n0 + nn]; };
       wgemm<2, true, false>(ca, 0, K, fk, fd);
       auto fph = [&](int r, int i) { return tile64(PH, i, r0 + r); };
       auto fpl = [&](int r, int i) { return tile64(PL, i, r0 + r); };
-      auto fo = [&](int i, int nn) { return bf2f(Ds[i * 32 + n0 + nn]); };
+      auto fo = [&](int i, int nn) { return bf2f(Ds[i * (Ly::DOROW / 2) + n0 + nn]); };
       wgemm<2, true, true>(cp, r0, 64, fph, fo);
       wgemm<2, true, true>(cp, r0, 64, fpl, fo);
       const int g = (tid & 31) >> 2, t = tid & 3;
@@ -244,20 +260,24 @@ __global__ void __launch_bounds__(BT, 1) chunk_dh_kernel(
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int j = r0 + g + 8 * (e >> 1);
-          dvn[j * SS + n0 + 8 * nt + 2 * t + (e & 1)] = fmaf(sc[RS_SV + j], ca[nt][e], scale * cp[nt][e]);
+          dvn[j * Ly::BS + n0 + 8 * nt + 2 * t + (e & 1)] = fmaf(sc[RS_SV + j], ca[nt][e], scale * cp[nt][e]);
         }
     }
     __syncthreads();
     // dh = e^{gamma_L} dh' + Q^T diag(scale og) do - W^T dv_new   (og carries 1/||q||)
     {
       const float dL = sc[RS_DL];
-      cvisit(dh, [&](int, int, int, float &x) { x *= dL; });
+      float t1[NTD][4] = {}, t2[NTD][4] = {};  // separate accumulators: independent mma chains
       auto fq = [&](int r, int i) { return bf2f(Qs[i * KE + dm0 + r]); };
-      auto fo = [&](int i, int cc) { return scale * sc[RS_OG + i] * bf2f(Ds[i * 32 + dc0 + cc]); };
-      wgemm<NTD, true, false>(dh, 0, 64, fq, fo);
+      auto fo = [&](int i, int cc) { return scale * sc[RS_OG + i] * bf2f(Ds[i * (Ly::DOROW / 2) + dc0 + cc]); };
+      wgemm<NTD, true, false>(t1, 0, 64, fq, fo);
       auto fw = [&](int r, int j) { return rec_w(Wt, j, dm0 + r); };
-      auto fv = [&](int j, int cc) { return -dvn[j * SS + dc0 + cc]; };
-      wgemm<NTD, true, false>(dh, 0, 64, fw, fv);
+      auto fv = [&](int j, int cc) { return dvn[j * Ly::BS + dc0 + cc]; };
+      wgemm<NTD, true, false>(t2, 0, 64, fw, fv);
+#pragma unroll
+      for (int nt = 0; nt < NTD; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dh[nt][e] = fmaf(dL, dh[nt][e], t1[nt][e] - t2[nt][e]);
     }
     __syncthreads();  // this stage is refilled by the next issue
   }
@@ -529,9 +549,45 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
       auto fq = [&](int r, int x) { return qv(r0 + r, x); };
       auto fh = [&](int x, int n) { return hS[x * SS + n0 + n]; };
       auto fd = [&](int x, int n) { return dhS[x * SS + n0 + n]; };
-      wgemm<2, true, false>(ckh, 0, K, fk, fh);
-      wgemm<2, true, false>(cqh, 0, K, fq, fh);
-      wgemm<2, true, false>(ckd, 0, K, fk, fd);
+      // one pass over K for the three products (shared fragments, six accumulators)
+      {
+        const int fr = lane >> 2, ft = lane & 3;
+#pragma unroll 2
+        for (int kk = 0; kk < K; kk += 8) {
+          uint32_t ak[4], aq[4];
+          ak[0] = __float_as_uint(fk(fr, kk + ft));
+          ak[1] = __float_as_uint(fk(fr + 8, kk + ft));
+          ak[2] = __float_as_uint(fk(fr, kk + ft + 4));
+          ak[3] = __float_as_uint(fk(fr + 8, kk + ft + 4));
+          aq[0] = __float_as_uint(fq(fr, kk + ft));
+          aq[1] = __float_as_uint(fq(fr + 8, kk + ft));
+          aq[2] = __float_as_uint(fq(fr, kk + ft + 4));
+          aq[3] = __float_as_uint(fq(fr + 8, kk + ft + 4));
+          uint32_t hh[2][2], hl[2][2], dh_[2][2], dl[2][2];
+#pragma unroll
+          for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const float x = fh(kk + ft + 4 * u, 8 * n + fr), y = fd(kk + ft + 4 * u, 8 * n + fr);
+              hh[n][u] = tf32_rna(x);
+              hl[n][u] = tf32_rna(x - __uint_as_float(hh[n][u]));
+              dh_[n][u] = tf32_rna(y);
+              dl[n][u] = tf32_rna(y - __uint_as_float(dh_[n][u]));
+            }
+#pragma unroll
+          for (int n = 0; n < 2; ++n) {
+            mma_tf32(ckh[n], ak, hh[n][0], hh[n][1]);
+            mma_tf32(cqh[n], aq, hh[n][0], hh[n][1]);
+            mma_tf32(ckd[n], ak, dh_[n][0], dh_[n][1]);
+          }
+#pragma unroll
+          for (int n = 0; n < 2; ++n) {
+            mma_tf32(ckh[n], ak, hl[n][0], hl[n][1]);
+            mma_tf32(cqh[n], aq, hl[n][0], hl[n][1]);
+            mma_tf32(ckd[n], ak, dl[n][0], dl[n][1]);
+          }
+        }
+      }
       cvisit(ckh, [&](int, int r, int n, float x) {
         const int i = r0 + r, cc = n0 + n;
         const float kh = x * rk[i];

@@ -8,6 +8,7 @@ Cases:
   chunk_long  : B=1, T=65536, H=16, HV=32, K=V=128 (the benchmark workload)
   decode      : 256 requests against a [512, 32, 128, 128] fp32 pool, fused gating
   gating      : 524288 x 32 gates
+  bwd_dense   : gdn_chunk_bwd on the chunk_dense workload (initial state, final-state gradient)
 """
 from __future__ import annotations
 
@@ -23,7 +24,7 @@ from gated_deltanet_chunked_chunk_gb300 import workloads as W
 def main():
     p = argparse.ArgumentParser()
     p.add_argument("--case", default="chunk_dense",
-                   choices=["chunk_dense", "chunk_long", "decode", "gating"])
+                   choices=["chunk_dense", "chunk_long", "decode", "gating", "bwd_dense"])
     p.add_argument("--reps", type=int, default=3)
     args = p.parse_args()
     gbuild.build()
@@ -37,6 +38,17 @@ def main():
         beta = beta.view(case.B, case.T, case.HV)
         for _ in range(args.reps):
             gdn.gdn_chunk_fwd(q, k, v, g, beta, initial_state=h0)
+    elif args.case == "bwd_dense":
+        case = W.config1()
+        g, beta = gdn.gdn_gating(d(case.A_log), d(case.a), d(case.b), d(case.dt_bias))
+        g = g.view(case.B, case.T, case.HV)
+        beta = beta.view(case.B, case.T, case.HV)
+        gen = torch.Generator().manual_seed(31)
+        do = d(torch.randn(case.B, case.T, case.HV, case.V, generator=gen).to(torch.bfloat16))
+        dht = d(torch.randn(case.N, case.HV, case.K, case.V, generator=gen))
+        q, k, v, h0 = d(case.q), d(case.k), d(case.v), d(case.initial_state)
+        for _ in range(args.reps):
+            gdn.gdn_chunk_bwd(q, k, v, g, beta, do, initial_state=h0, dht=dht)
     elif args.case == "decode":
         dc = W.config4()
         pool = d(dc.ssm_pool)
