@@ -25,7 +25,7 @@ __all__ = ["gdn_gating", "gdn_chunk_fwd", "gdn_recurrent_decode", "chunk_fwd_wor
            "gdn_chunk_fwd_noalloc", "NOALLOC_SCRATCH_BYTES", "gdn_causal_conv1d_fwd",
            "gdn_causal_conv1d_update", "gdn_conv_decode_pack", "gdn_recurrent_decode_bf16",
            "gdn_recurrent_decode_mtp", "gdn_chunk_bwd", "chunk_bwd_workspace_size",
-           "gdn_chunk_fwd_gated", "GDNError", "lib_path", "load_library", "status_string", "DEV_BAD_CU_SEQLENS",
+           "gdn_chunk_fwd_gated", "chunk_gated_delta_rule", "GDNError", "lib_path", "load_library", "status_string", "DEV_BAD_CU_SEQLENS",
            "DEV_BAD_SLOT", "DEV_WAIT_TIMEOUT", "EXPORTED_SYMBOLS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -576,3 +576,47 @@ def gdn_chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
     if rc != GDN_OK:
         raise GDNError("gdn_chunk_bwd", rc)
     return dq, dk, dv, dg, dbeta, dh0
+
+
+class _ChunkGatedDeltaRule(torch.autograd.Function):
+    """gdn_chunk_fwd forward, gdn_chunk_bwd backward (marshalling only)."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, g, beta, initial_state, scale, output_final_state, cu_seqlens, use_qk_l2norm,
+                num_seqs):
+        o, ht = gdn_chunk_fwd(q, k, v, g, beta, scale=scale, initial_state=initial_state,
+                              output_final_state=output_final_state, cu_seqlens=cu_seqlens,
+                              use_qk_l2norm=use_qk_l2norm, num_seqs=num_seqs)
+        ctx.save_for_backward(q, k, v, g, beta, initial_state, cu_seqlens)
+        ctx.scale, ctx.l2 = scale, use_qk_l2norm
+        if ht is None:
+            return o
+        return o, ht
+
+    @staticmethod
+    def backward(ctx, do, dht=None):
+        q, k, v, g, beta, h0, cu = ctx.saved_tensors
+        do = do.to(torch.bfloat16).contiguous()
+        dht = None if dht is None else dht.float().contiguous()
+        dq, dk, dv, dg, dbeta, dh0 = gdn_chunk_bwd(q, k, v, g, beta, do, scale=ctx.scale, initial_state=h0,
+                                                   cu_seqlens=cu, dht=dht, use_qk_l2norm=ctx.l2)
+        return (dq.to(q.dtype), dk.to(k.dtype), dv.to(v.dtype), dg, dbeta,
+                None if dh0 is None else dh0, None, None, None, None, None)
+
+
+def chunk_gated_delta_rule(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                           beta: torch.Tensor, scale: Optional[float] = None,
+                           initial_state: Optional[torch.Tensor] = None, output_final_state: bool = True,
+                           cu_seqlens: Optional[torch.Tensor] = None, use_qk_l2norm_in_kernel: bool = True,
+                           num_seqs: Optional[int] = None):
+    """Differentiable chunked prefill with the argument names of the pages'
+    chunk_gated_delta_rule (FastDeploy PR "support fla triton kernel for
+    qwen3.5", Usage section 1).  Returns (o, final_state) (final_state None
+    unless ``output_final_state``); autograd runs gdn_chunk_bwd and yields
+    gradients for q, k, v (in their bf16 dtype), g, beta and initial_state
+    (fp32)."""
+    out = _ChunkGatedDeltaRule.apply(q, k, v, g, beta, initial_state, scale, output_final_state, cu_seqlens,
+                                     use_qk_l2norm_in_kernel, num_seqs)
+    if isinstance(out, tuple):
+        return out
+    return out, None
