@@ -144,7 +144,9 @@ __global__ void __launch_bounds__(NTH, 4) chunk_prep_kernel(
   extern __shared__ unsigned char smem_raw[];
   unsigned char *sm = align1024(smem_raw);
   const uint32_t sb = smem_u32(sm);
-  const int gc = blockIdx.x, hv = blockIdx.y;
+  // Value head fastest: the G value heads of a key head run side by side and
+  // share the K, Q tile through L2.
+  const int gc = static_cast<int>(blockIdx.x / HV), hv = static_cast<int>(blockIdx.x % HV);
   const int h = hv / (HV / H);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g4 = lane >> 2, t4 = lane & 3;
@@ -1025,7 +1027,7 @@ cudaError_t launch_k(const gdn_host::ChunkArgs &a, cudaStream_t s) {
     const int psmem = PrepLay<K>::BYTES + 1024;
     cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, psmem);
     if (e != cudaSuccess) return e;
-    dim3 pgrid(static_cast<unsigned>(slots), a.HV);
+    dim3 pgrid(static_cast<unsigned>(slots * a.HV));
     const PrepGates gt{a.A_log, a.ga, a.gb, a.dt_bias, a.g_out, a.beta_out};
     chunk_prep_kernel<K><<<pgrid, NTH, psmem, s>>>(mq, mk, a.g, a.beta, gt, a.cu, a.N, a.T, a.H, a.HV, a.l2,
                                                    static_cast<unsigned char *>(a.ws), a.dev_status);

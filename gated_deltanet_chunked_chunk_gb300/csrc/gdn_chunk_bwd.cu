@@ -366,7 +366,8 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
   float *SQ = vec + GV_SQ * 64, *SG = vec + GV_SG * 64, *SLv = vec + GV_SL * 64;
   float *PQ = vec + GV_PQ * 64, *PK = vec + GV_PK * 64, *misc = vec + GV_MISC * 64;
 
-  const int gc = blockIdx.x, hv = blockIdx.y;
+  // Value head fastest, so that the value heads of a key head share q, k through L2.
+  const int gc = static_cast<int>(blockIdx.x / HV), hv = static_cast<int>(blockIdx.x % HV);
   const int h = hv / (HV / H);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g8 = lane >> 2, t4 = lane & 3;
@@ -866,7 +867,7 @@ cudaError_t launch_bwd_k(const gdn_host::ChunkBwdArgs &a, cudaStream_t s) {
     const int smem = GradLay<K>::BYTES;
     e = cudaFuncSetAttribute(chunk_grad_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    chunk_grad_kernel<K><<<dim3((unsigned)slots, a.HV), BT, smem, s>>>(
+    chunk_grad_kernel<K><<<dim3((unsigned)(slots * a.HV)), BT, smem, s>>>(
         a.q, a.k, a.v, a.g, a.beta, a.dout, Hs, DH, a.scale, a.cu, a.N, a.T, a.H, a.HV, a.V, a.l2, a.dq, a.dk,
         a.dv, a.dg, a.dbeta, a.dev_status);
     e = cudaGetLastError();
