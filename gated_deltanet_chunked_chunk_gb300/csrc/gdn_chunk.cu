@@ -98,11 +98,6 @@ __device__ __forceinline__ void mm16_tf32(const float *A, int lda, const float *
     }
   }
 }
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
 
 // ============================================================== prep kernel
 template <int K>
