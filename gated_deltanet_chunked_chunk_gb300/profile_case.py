@@ -7,6 +7,7 @@ Cases:
                 (about 230 MB of inputs and outputs, above the 129 MB L2)
   chunk_long  : B=1, T=65536, H=16, HV=32, K=V=128 (the benchmark workload)
   decode      : 256 requests against a [512, 32, 128, 128] fp32 pool, fused gating
+  decode_bf16 : the same against a bf16 pool
   gating      : 524288 x 32 gates
   bwd_dense   : gdn_chunk_bwd on the chunk_dense workload (initial state, final-state gradient)
 """
@@ -24,7 +25,7 @@ from gated_deltanet_chunked_chunk_gb300 import workloads as W
 def main():
     p = argparse.ArgumentParser()
     p.add_argument("--case", default="chunk_dense",
-                   choices=["chunk_dense", "chunk_long", "decode", "gating", "bwd_dense"])
+                   choices=["chunk_dense", "chunk_long", "decode", "decode_bf16", "gating", "bwd_dense"])
     p.add_argument("--reps", type=int, default=3)
     args = p.parse_args()
     gbuild.build()
@@ -49,12 +50,17 @@ def main():
         q, k, v, h0 = d(case.q), d(case.k), d(case.v), d(case.initial_state)
         for _ in range(args.reps):
             gdn.gdn_chunk_bwd(q, k, v, g, beta, do, initial_state=h0, dht=dht)
-    elif args.case == "decode":
+    elif args.case in ("decode", "decode_bf16"):
         dc = W.config4()
-        pool = d(dc.ssm_pool)
+        if args.case == "decode":
+            pool = d(dc.ssm_pool)
+            fn = gdn.gdn_recurrent_decode
+        else:
+            pool = d(dc.ssm_pool.to(torch.bfloat16))
+            fn = gdn.gdn_recurrent_decode_bf16
         for _ in range(args.reps):
-            gdn.gdn_recurrent_decode(d(dc.q), d(dc.k), d(dc.v), pool, d(dc.ssm_indices),
-                                     A_log=d(dc.A_log), a=d(dc.a), b=d(dc.b), dt_bias=d(dc.dt_bias))
+            fn(d(dc.q), d(dc.k), d(dc.v), pool, d(dc.ssm_indices),
+               A_log=d(dc.A_log), a=d(dc.a), b=d(dc.b), dt_bias=d(dc.dt_bias))
     else:
         n, HV = 65536 * 8, 32
         gen = torch.Generator().manual_seed(5)
