@@ -15,7 +15,7 @@
 //
 // All three ops are memory-bound (a few multiply-adds per element).
 //  * conv_prefill_kernel: x is channel-first [dim, total]; a CTA takes one
-//    channel and 8192 tokens, a thread 8 consecutive tokens per step with
+//    channel and 32768 tokens, a thread 8 consecutive tokens per step with
 //    16-byte loads and stores (the general per-token path, with a binary
 //    search in query_start_loc, serves sequence starts and unaligned rows).
 //  * conv_state_kernel (same stream, after the prefill kernel, so every read
@@ -33,9 +33,12 @@ namespace {
 
 constexpr int kConvMaxW = 8;
 constexpr int kConvMaxS = 64;
-constexpr int kPrefillTile = 8192;
+constexpr int kPrefillTile = 32768;
 
-__device__ __forceinline__ float conv_act(float x, int act) { return act ? x / (1.f + expf(-x)) : x; }
+// SiLU with the hardware exponential and a fast divide: a few ulp of fp32,
+// far below the bf16 rounding of the output (for x < -87 the divisor is huge
+// and the result is 0, as SiLU underflows there anyway).
+__device__ __forceinline__ float conv_act(float x, int act) { return act ? __fdividef(x, 1.f + __expf(-x)) : x; }
 
 // Largest n in [0, N] with qsl[n] <= t (qsl non-decreasing), or -1.
 __device__ __forceinline__ int seq_of(const int32_t *qsl, int N, int64_t t) {
@@ -81,7 +84,7 @@ __device__ __forceinline__ float conv_prefill_one(const uint16_t *__restrict__ x
   return acc;
 }
 
-// One CTA per (channel, 2048-token tile).  Vector path (rows 16-byte aligned):
+// One CTA per (channel, 32768-token tile).  Vector path (rows 16-byte aligned):
 // a thread takes 8 consecutive tokens, loads them and the 8 before them with
 // two 16-byte loads (the second mostly an L1 hit) and stores 16 bytes; tokens
 // within W - 1 of a sequence start, or sharing the 8 with a boundary, take the
@@ -113,12 +116,25 @@ __global__ void __launch_bounds__(256) conv_prefill_kernel(
     }
     return;
   }
+  // The sequence [s_lo, s_hi) holding the last group looked up: the thread's
+  // groups are 8 blockDim tokens apart, so the binary search runs only when a
+  // group leaves it.
+  int64_t s_lo = 1, s_hi = 0;
   for (int64_t t0 = tile0 + 8 * threadIdx.x; t0 < t_end; t0 += 8 * blockDim.x) {
   // Fast path: all 8 tokens in one sequence, at least W - 1 tokens past its start.
   bool fast = t0 + 8 <= t_end;
   if (fast) {
-    const int n = seq_of(qsl, N, t0);
-    fast = n >= 0 && n < N && qsl[n] >= 0 && t0 - qsl[n] >= W - 1 && qsl[n + 1] >= t0 + 8;
+    if (t0 < s_lo || t0 >= s_hi) {
+      const int n = seq_of(qsl, N, t0);
+      if (n >= 0 && n < N && qsl[n] >= 0) {
+        s_lo = qsl[n];
+        s_hi = qsl[n + 1];
+      } else {
+        s_lo = 1;
+        s_hi = 0;
+      }
+    }
+    fast = t0 >= s_lo && t0 - s_lo >= W - 1 && s_hi >= t0 + 8;
   }
   if (fast) {
     const uint4 cur = *reinterpret_cast<const uint4 *>(xr + t0);
