@@ -131,8 +131,9 @@ struct PrepGates {
 template <int K>
 __global__ void __launch_bounds__(NTH, 4) chunk_prep_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k, const float *__restrict__ g,
-    const float *__restrict__ beta, const PrepGates gt, const int32_t *__restrict__ cu, int N, int T, int H,
-    int HV, int l2, unsigned char *__restrict__ ws, int32_t *dev_status) {
+    const float *__restrict__ beta, const PrepGates gt, const int32_t *__restrict__ cu,
+    const int32_t *__restrict__ cs, int N, int T, int H, int HV, int l2, unsigned char *__restrict__ ws,
+    int32_t *dev_status) {
   using Ly = PrepLay<K>;
   using R = Rec<K>;
   constexpr int KA = K / 64;
@@ -149,25 +150,8 @@ __global__ void __launch_bounds__(NTH, 4) chunk_prep_kernel(
   // Which sequence / chunk is this?
   int n = 0, c = 0;
   int64_t tok0 = 0, len = 0;
-  {
-    int64_t base = 0;
-    bool found = false;
-    for (int m = 0; m < N && !found; ++m) {
-      int64_t t0, l0;
-      if (!seq_bounds(cu, m, T, t0, l0)) continue;
-      const int nc = chunks_of(l0);
-      if (gc < base + nc) {
-        found = true;
-        n = m;
-        c = static_cast<int>(gc - base);
-        tok0 = t0;
-        len = l0;
-      }
-      base += nc;
-    }
-    if (!found) return;  // past the last chunk (the grid is an upper bound)
-  }
-  (void)n;
+  if (!slot_chunk(cs, N, T, gc, n, c) || !seq_bounds(cu, n, T, tok0, len))
+    return;  // past the last chunk (the grid is an upper bound)
   const int64_t rem = len - static_cast<int64_t>(c) * C;
   const int L = static_cast<int>(rem < C ? rem : C);
   const int64_t trow0 = tok0 + static_cast<int64_t>(c) * C;
@@ -585,7 +569,8 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, float scale, const float *__restrict__ h0,
     const int32_t *__restrict__ cu, int T, int H, int HV, int V, const unsigned char *__restrict__ ws,
-    uint16_t *__restrict__ o, float *__restrict__ ht, float *__restrict__ hsave, int32_t *dev_status) {
+    uint16_t *__restrict__ o, float *__restrict__ ht, float *__restrict__ hsave, const int32_t *__restrict__ cs,
+    int32_t *dev_status) {
   using Ly = WalkLay<K>;
   using R = Rec<K>;
   constexpr int KA = K / 64;
@@ -607,7 +592,7 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
     return;
   }
   const int NC = chunks_of(len);
-  const int64_t cb = chunk_base(cu, n, T);
+  const int64_t cb = chunk_base(cs, n, T);
   uint32_t *misc = reinterpret_cast<uint32_t *>(sm + Ly::OFF_MISC);
   volatile uint32_t *abort_flag = misc + 1;
   // Two-slot barriers, slot c & 1 serving chunk c:
@@ -968,6 +953,38 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
   if (tid == 0 && *abort_flag) set_status(dev_status, GDN_DEV_WAIT_TIMEOUT);
 }
 
+// ------------------------------------------------------------- chunk starts
+// cs[n] = number of chunks of the sequences before n (cu_seqlens input; a
+// sequence whose offsets break the rules has none), cs[N] = the total: one
+// block, each thread summing a contiguous run of sequences, then a block scan.
+__global__ void __launch_bounds__(1024) chunk_starts_kernel(const int32_t *__restrict__ cu, int N, int T,
+                                                            int32_t *__restrict__ cs) {
+  __shared__ int32_t part[1024];
+  const int tid = threadIdx.x;
+  const int per = (N + 1023) / 1024;
+  const int n0 = min(N, tid * per), n1 = min(N, n0 + per);
+  int32_t sum = 0;
+  for (int n = n0; n < n1; ++n) {
+    int64_t t0, l0;
+    if (seq_bounds(cu, n, T, t0, l0)) sum += chunks_of(l0);
+  }
+  part[tid] = sum;
+  __syncthreads();
+  for (int off = 1; off < 1024; off <<= 1) {  // inclusive scan
+    const int32_t y = tid >= off ? part[tid - off] : 0;
+    __syncthreads();
+    part[tid] += y;
+    __syncthreads();
+  }
+  int32_t run = part[tid] - sum;  // exclusive
+  for (int n = n0; n < n1; ++n) {
+    cs[n] = run;
+    int64_t t0, l0;
+    if (seq_bounds(cu, n, T, t0, l0)) run += chunks_of(l0);
+  }
+  if (tid == 1023) cs[N] = part[1023];
+}
+
 // ---------------------------------------------------------------- host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
@@ -1001,8 +1018,12 @@ bool make_map(CUtensorMap *m, const void *ptr, int dim, int heads, int64_t rows,
 }
 
 template <int K>
-size_t ws_bytes(int B, int T, int HV, int N, bool varlen) {
+size_t records_bytes(int B, int T, int HV, int N, bool varlen) {
   return static_cast<size_t>(total_chunk_slots(B, T, N, varlen)) * HV * Rec<K>::BYTES;
+}
+template <int K>
+size_t ws_bytes(int B, int T, int HV, int N, bool varlen) {
+  return records_bytes<K>(B, T, HV, N, varlen) + chunk_starts_bytes(N, varlen);
 }
 
 template <int K>
@@ -1018,13 +1039,23 @@ cudaError_t launch_k(const gdn_host::ChunkArgs &a, cudaStream_t s) {
                    !make_map(&mv, a.v, a.V, a.HV, rows, 64, true)))
     return cudaErrorInvalidValue;
   const int64_t slots = total_chunk_slots(a.B, a.T, a.N, a.cu != nullptr);
+  // cu_seqlens: the chunk starts of the sequences, after the records.
+  const int32_t *cs = nullptr;
+  if (a.cu) {
+    int32_t *csw = reinterpret_cast<int32_t *>(static_cast<unsigned char *>(a.ws) +
+                                               records_bytes<K>(a.B, a.T, a.HV, a.N, true));
+    chunk_starts_kernel<<<1, 1024, 0, s>>>(a.cu, a.N, a.T, csw);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    cs = csw;
+  }
   if (rows > 0 && slots > 0) {
     const int psmem = PrepLay<K>::BYTES + 1024;
     cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, psmem);
     if (e != cudaSuccess) return e;
     dim3 pgrid(static_cast<unsigned>(slots * a.HV));
     const PrepGates gt{a.A_log, a.ga, a.gb, a.dt_bias, a.g_out, a.beta_out};
-    chunk_prep_kernel<K><<<pgrid, NTH, psmem, s>>>(mq, mk, a.g, a.beta, gt, a.cu, a.N, a.T, a.H, a.HV, a.l2,
+    chunk_prep_kernel<K><<<pgrid, NTH, psmem, s>>>(mq, mk, a.g, a.beta, gt, a.cu, cs, a.N, a.T, a.H, a.HV, a.l2,
                                                    static_cast<unsigned char *>(a.ws), a.dev_status);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -1034,7 +1065,7 @@ cudaError_t launch_k(const gdn_host::ChunkArgs &a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   dim3 grid(a.V / VT, a.HV, a.N);
   chunk_walk_kernel<K><<<grid, WALK_THREADS, wsmem, s>>>(mq, mk, mv, a.scale, a.h0, a.cu, a.T, a.H, a.HV, a.V,
-                                                static_cast<const unsigned char *>(a.ws), a.o, a.ht, a.hsave,
+                                                static_cast<const unsigned char *>(a.ws), a.o, a.ht, a.hsave, cs,
                                                 a.dev_status);
   return cudaGetLastError();
 }

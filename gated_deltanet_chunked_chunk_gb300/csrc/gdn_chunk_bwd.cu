@@ -161,8 +161,8 @@ template <int K>
 __global__ void __launch_bounds__(BT, 1) chunk_dh_kernel(
     const uint16_t *__restrict__ q, const uint16_t *__restrict__ k, const uint16_t *__restrict__ dout,
     const unsigned char *__restrict__ ws, float *__restrict__ DH, const float *__restrict__ dht,
-    float *__restrict__ dh0, float scale, const int32_t *__restrict__ cu, int T, int H, int HV, int V,
-    int32_t *dev_status) {
+    float *__restrict__ dh0, float scale, const int32_t *__restrict__ cu, const int32_t *__restrict__ cs, int T,
+    int H, int HV, int V, int32_t *dev_status) {
   using Ly = DhLay<K>;
   using R = Rec<K>;
   constexpr int KE = Ly::KROW / 2;  // bf16 elements per staged K / Q row
@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(BT, 1) chunk_dh_kernel(
     return;
   }
   const int NC = chunks_of(len);
-  const int64_t cb = chunk_base(cu, n, T);
+  const int64_t cb = chunk_base(cs, n, T);
   const int64_t sbase = ((int64_t)n * HV + hv) * K;
   float dh[NTD][4];
   cvisit(dh, [&](int, int r, int c, float &x) {
@@ -333,7 +333,8 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
     const uint16_t *__restrict__ q, const uint16_t *__restrict__ k, const uint16_t *__restrict__ v,
     const float *__restrict__ g, const float *__restrict__ beta, const uint16_t *__restrict__ dout,
     const float *__restrict__ Hs, const float *__restrict__ DH, float scale, const int32_t *__restrict__ cu,
-    int N, int T, int H, int HV, int V, int l2, float *__restrict__ dq, float *__restrict__ dk,
+    const int32_t *__restrict__ cs, int N, int T, int H, int HV, int V, int l2, float *__restrict__ dq,
+    float *__restrict__ dk,
     float *__restrict__ dv, float *__restrict__ dg, float *__restrict__ dbeta, int32_t *dev_status) {
   using Ly = GradLay<K>;
   constexpr int BR = Ly::BROW;
@@ -374,26 +375,10 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
   const int mt = warp & 3, hf = warp >> 2, r0 = 16 * mt;
 
   // Which sequence / chunk?
-  int c = 0;
+  int n = 0, c = 0;
   int64_t tok0 = 0, len = 0;
   const int64_t slot = gc;
-  {
-    int64_t base = 0;
-    bool found = false;
-    for (int m = 0; m < N && !found; ++m) {
-      int64_t t0, l0;
-      if (!seq_bounds(cu, m, T, t0, l0)) continue;
-      const int nc = chunks_of(l0);
-      if (gc < base + nc) {
-        found = true;
-        c = (int)(gc - base);
-        tok0 = t0;
-        len = l0;
-      }
-      base += nc;
-    }
-    if (!found) return;
-  }
+  if (!slot_chunk(cs, N, T, gc, n, c) || !seq_bounds(cu, n, T, tok0, len)) return;
   const int64_t rem = len - (int64_t)c * C;
   const int L = rem < C ? (int)rem : C;
   const int64_t trow0 = tok0 + (int64_t)c * C;
@@ -836,6 +821,9 @@ cudaError_t launch_bwd_k(const gdn_host::ChunkBwdArgs &a, cudaStream_t s) {
   const size_t rec_bytes = gdn_host::chunk_workspace_bytes(a.B, a.T, a.H, a.HV, K, a.V, a.N, a.cu != nullptr);
   float *Hs = reinterpret_cast<float *>(wsb + rec_bytes);
   float *DH = reinterpret_cast<float *>(wsb + rec_bytes + hbytes);
+  // The forward below writes the chunk starts of cu_seqlens input right after its records.
+  const int32_t *cs =
+      a.cu ? reinterpret_cast<const int32_t *>(wsb + (size_t)slots * a.HV * Rec<K>::BYTES) : nullptr;
   const int64_t rows = (int64_t)a.B * a.T;
   cudaError_t e;
   if (rows > 0) {
@@ -857,8 +845,8 @@ cudaError_t launch_bwd_k(const gdn_host::ChunkBwdArgs &a, cudaStream_t s) {
     e = cudaFuncSetAttribute(chunk_dh_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     chunk_dh_kernel<K><<<dim3(a.V / 32, a.HV, a.N), BT, smem, s>>>(
-        a.q, a.k, a.dout, static_cast<const unsigned char *>(a.ws), DH, a.dht, a.dh0, a.scale, a.cu, a.T, a.H,
-        a.HV, a.V, a.dev_status);
+        a.q, a.k, a.dout, static_cast<const unsigned char *>(a.ws), DH, a.dht, a.dh0, a.scale, a.cu, cs, a.T,
+        a.H, a.HV, a.V, a.dev_status);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -868,8 +856,8 @@ cudaError_t launch_bwd_k(const gdn_host::ChunkBwdArgs &a, cudaStream_t s) {
     e = cudaFuncSetAttribute(chunk_grad_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     chunk_grad_kernel<K><<<dim3((unsigned)(slots * a.HV)), BT, smem, s>>>(
-        a.q, a.k, a.v, a.g, a.beta, a.dout, Hs, DH, a.scale, a.cu, a.N, a.T, a.H, a.HV, a.V, a.l2, a.dq, a.dk,
-        a.dv, a.dg, a.dbeta, a.dev_status);
+        a.q, a.k, a.v, a.g, a.beta, a.dout, Hs, DH, a.scale, a.cu, cs, a.N, a.T, a.H, a.HV, a.V, a.l2, a.dq,
+        a.dk, a.dv, a.dg, a.dbeta, a.dev_status);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

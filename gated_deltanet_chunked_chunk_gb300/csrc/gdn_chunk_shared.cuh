@@ -51,16 +51,32 @@ __device__ __forceinline__ bool seq_bounds(const int32_t *cu, int n, int T, int6
   return true;
 }
 __device__ __forceinline__ int chunks_of(int64_t len) { return static_cast<int>((len + C - 1) / C); }
-// Index of the first chunk of sequence n in the workspace: sum of the chunk
-// counts of the sequences before it (offsets that break the rules count 0).
-__device__ __forceinline__ int64_t chunk_base(const int32_t *cu, int n, int T) {
-  if (!cu) return static_cast<int64_t>(n) * chunks_of(T);
-  int64_t b = 0;
-  for (int m = 0; m < n; ++m) {
-    int64_t t0, l0;
-    if (seq_bounds(cu, m, T, t0, l0)) b += chunks_of(l0);
+// Index of the first chunk of sequence n in the workspace: cs[n], the prefix
+// sums of the sequences' chunk counts (written by the chunk-starts kernel for
+// cu_seqlens input; offsets that break the rules count 0 chunks), or
+// n * chunks_of(T) for dense input (cs == NULL).
+__device__ __forceinline__ int64_t chunk_base(const int32_t *cs, int n, int T) {
+  return cs ? static_cast<int64_t>(cs[n]) : static_cast<int64_t>(n) * chunks_of(T);
+}
+// Sequence n and chunk c of chunk slot gc (false past the last chunk): for
+// cu_seqlens input the largest n with cs[n] <= gc, by binary search.
+__device__ __forceinline__ bool slot_chunk(const int32_t *cs, int N, int T, int64_t gc, int &n, int &c) {
+  if (!cs) {
+    const int nc = chunks_of(T);
+    if (nc == 0 || gc >= static_cast<int64_t>(N) * nc) return false;
+    n = static_cast<int>(gc / nc);
+    c = static_cast<int>(gc % nc);
+    return true;
   }
-  return b;
+  if (N <= 0 || gc >= cs[N]) return false;
+  int lo = 0, hi = N - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cs[mid] <= gc) lo = mid; else hi = mid - 1;
+  }
+  n = lo;
+  c = static_cast<int>(gc - cs[lo]);
+  return true;
 }
 
 // Upper bound on the number of chunk slots of a call (varlen: one ragged chunk
@@ -68,6 +84,11 @@ __device__ __forceinline__ int64_t chunk_base(const int32_t *cu, int n, int T) {
 inline int64_t total_chunk_slots(int B, int T, int N, bool varlen) {
   const int64_t per = (static_cast<int64_t>(T) + C - 1) / C;
   return varlen ? per + N : static_cast<int64_t>(B) * per;
+}
+// Bytes of the chunk-starts array (N + 1 int32, cu_seqlens input only), kept
+// in the workspace right after the records, in whole KB.
+inline size_t chunk_starts_bytes(int N, bool varlen) {
+  return varlen ? ((static_cast<size_t>(N) + 1) * 4 + 1023) / 1024 * 1024 : 0;
 }
 
 }  // namespace gdnc

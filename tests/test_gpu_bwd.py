@@ -103,3 +103,12 @@ def test_bwd_qwen_heads_sampled_group():
     for name, x, r in zip(["dq", "dk", "dv", "dg", "dbeta", "dh0"], gpu, ref):
         err = P.rel_l2(x.cpu().numpy().astype(np.float64), r)
         assert err <= BWD_REL_L2, f"{name}: rel-L2 {err:.3e}"
+
+
+def test_bwd_varlen_many_sequences():
+    # 120 sequences of 0..80 tokens: the chunk-start table in the backward kernels.
+    rng = np.random.default_rng(46)
+    lens = [int(x) if rng.random() > 0.2 else 0 for x in rng.integers(1, 81, 120)]
+    case = W.prefill_case("bwd_many", 46, 1, sum(lens), 1, 2, 64, 64, init="all",
+                          cu_seqlens=W.cu_from_lengths(lens))
+    _run(case, seed=6)

@@ -89,6 +89,20 @@ def test_varlen_with_empty_and_short_sequences():
             np.testing.assert_array_equal(ht_gpu[n], h0[n])
 
 
+def test_varlen_many_sequences():
+    # 1500 sequences of 0..150 tokens (every kind of ragged tail, a fifth of them
+    # empty): exercises the chunk-start table that maps chunk slots to sequences.
+    rng = np.random.default_rng(21)
+    lens = [int(x) if rng.random() > 0.2 else 0 for x in rng.integers(1, 151, 1500)]
+    cu = W.cu_from_lengths(lens)
+    case = W.prefill_case("varlen_many", 21, 1, cu[-1], 1, 2, 64, 64, cu_seqlens=cu, init="all")
+    o_gpu, ht_gpu, o_ref, ht_ref = _check_case(case)
+    h0 = case.initial_state.numpy()
+    for n, L in enumerate(lens):
+        if L == 0:
+            np.testing.assert_array_equal(ht_gpu[n], h0[n])
+
+
 def test_varlen_equals_separate_dense_calls_bitwise():
     lens = [70, 1, 129, 64]
     cu = W.cu_from_lengths(lens)
