@@ -346,7 +346,7 @@ def kernel_source_sha():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_deltanet_chunked_chunk_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f in ("gdn_chunk.cu", "gdn_sm103.cuh", "gdn_common.cuh"):
+        if f in ("gdn_chunk.cu", "gdn_chunk_shared.cuh", "gdn_sm103.cuh", "gdn_common.cuh"):
             h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 

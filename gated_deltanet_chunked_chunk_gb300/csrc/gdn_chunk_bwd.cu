@@ -111,6 +111,55 @@ __device__ __forceinline__ void wgemm(float (&c)[NT][4], int k0, int k1, FA fa, 
     }
   }
 }
+// The same product, software pipelined (the operands of step k + 8 are read
+// while step k runs): faster where several warps share a scheduler's latency
+// budget with long reductions (the per-chunk gradients), slower in the dh walk.
+template <int NT, bool AX, bool BX, class FA, class FB>
+__device__ __forceinline__ void wgemm_pipe(float (&c)[NT][4], int k0, int k1, FA fa, FB fb) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  if (k0 >= k1) return;
+  // Software pipelined: the operands of step k + 8 are read while step k runs.
+  float av[4], bv[NT][2];
+  auto fetch = [&](int k) {
+    av[0] = fa(g, k + t);
+    av[1] = fa(g + 8, k + t);
+    av[2] = fa(g, k + t + 4);
+    av[3] = fa(g + 8, k + t + 4);
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      bv[n][0] = fb(k + t, 8 * n + g);
+      bv[n][1] = fb(k + t + 4, 8 * n + g);
+    }
+  };
+  fetch(k0);
+  for (int k = k0; k < k1; k += 8) {
+    uint32_t ah[4], al[4], bh[NT][2], bl[NT][2];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      ah[e] = AX ? __float_as_uint(av[e]) : tf32_rna(av[e]);
+      al[e] = AX ? 0u : tf32_rna(av[e] - __uint_as_float(ah[e]));
+    }
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        bh[n][u] = BX ? __float_as_uint(bv[n][u]) : tf32_rna(bv[n][u]);
+        bl[n][u] = BX ? 0u : tf32_rna(bv[n][u] - __uint_as_float(bh[n][u]));
+      }
+    if (k + 8 < k1) fetch(k + 8);
+    // passes outermost, so that consecutive products go to different accumulators
+#pragma unroll
+    for (int n = 0; n < NT; ++n) mma_tf32(c[n], ah, bh[n][0], bh[n][1]);
+    if (!BX) {
+#pragma unroll
+      for (int n = 0; n < NT; ++n) mma_tf32(c[n], ah, bl[n][0], bl[n][1]);
+    }
+    if (!AX) {
+#pragma unroll
+      for (int n = 0; n < NT; ++n) mma_tf32(c[n], al, bh[n][0], bh[n][1]);
+    }
+  }
+}
 // f(rh, r, n, x) for every accumulator element: row r = g + 8 rh, column n.
 template <int NT, class F>
 __device__ __forceinline__ void cvisit(float (&c)[NT][4], F f) {
@@ -443,8 +492,8 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
     auto fk = [&](int r, int x) { return kv(r0 + r, x); };
     auto fq = [&](int r, int x) { return qv(r0 + r, x); };
     auto fkt = [&](int x, int n) { return kv(32 * hf + n, x); };
-    wgemm<4, true, true>(ck, 0, K, fk, fkt);
-    wgemm<4, true, true>(cq, 0, K, fq, fkt);
+    wgemm_pipe<4, true, true>(ck, 0, K, fk, fkt);
+    wgemm_pipe<4, true, true>(cq, 0, K, fq, fkt);
     cvisit(ck, [&](int, int r, int n, float x) {
       const int i = r0 + r, j = 32 * hf + n;
       const float ek = (j < i) ? expf(gam[i] - gam[j]) * x * rk[i] * rk[j] : 0.f;
@@ -481,7 +530,7 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
       float cs[2][4] = {};
       auto fa = [&](int r, int m) { return Tm[(16 * bi + r) * MS + m]; };
       auto fb = [&](int m, int n) { return Tm[m * MS + 16 * warp + n]; };
-      wgemm<2, false, false>(cs, 16 * warp, 16 * bi, fa, fb);
+      wgemm_pipe<2, false, false>(cs, 16 * warp, 16 * bi, fa, fb);
       cvisit(cs, [&](int, int r, int n, float x) { Xs[r * 17 + n] = x; });
     }
     __syncthreads();
@@ -489,7 +538,7 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
       float ct[2][4] = {};
       auto fa = [&](int r, int m) { return Tm[(16 * bi + r) * MS + 16 * bi + m]; };
       auto fb = [&](int m, int n) { return Xs[m * 17 + n]; };
-      wgemm<2, false, false>(ct, 0, 16, fa, fb);
+      wgemm_pipe<2, false, false>(ct, 0, 16, fa, fb);
       cvisit(ct, [&](int, int r, int n, float x) { Tm[(16 * bi + r) * MS + 16 * warp + n] = -x; });
     }
     __syncthreads();
@@ -599,14 +648,14 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
       float cc[4][4] = {};
       auto fa = [&](int r, int m) { return Tm[(r0 + r) * MS + m]; };
       auto fb = [&](int m, int n) { return MvS[m * SS + n]; };
-      wgemm<4, false, false>(cc, 0, r0 + 16, fa, fb);
+      wgemm_pipe<4, false, false>(cc, 0, r0 + 16, fa, fb);
       cvisit(cc, [&](int, int r, int n, float x) { vnS[(r0 + r) * SS + n] = x; });
     } else {
       // dv_new = diag(sv) k^ dh' + scale P^T do (P^T upper)
       float cc[4][4] = {};
       auto fa = [&](int r, int m) { return Pm[m * MS + r0 + r]; };
       auto fb = [&](int m, int n) { return doS[m * SS + n]; };
-      wgemm<4, false, true>(cc, r0, 64, fa, fb);
+      wgemm_pipe<4, false, true>(cc, r0, 64, fa, fb);
       cvisit(cc, [&](int, int r, int n, float x) {
         const int i = r0 + r;
         dvnS[i * SS + n] = fmaf(sv[i], KdhS[i * SS + n], scale * x);
@@ -618,7 +667,7 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
       float cc[4][4] = {};
       auto fa = [&](int r, int m) { return Tm[m * MS + r0 + r]; };
       auto fb = [&](int m, int n) { return dvnS[m * SS + n]; };
-      wgemm<4, false, false>(cc, r0, 64, fa, fb);
+      wgemm_pipe<4, false, false>(cc, r0, 64, fa, fb);
       float sb[2] = {0.f, 0.f}, sg[2] = {0.f, 0.f};
       cvisit(cc, [&](int rh, int r, int n, float x) {
         const int i = r0 + r;
@@ -657,11 +706,11 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
       // dT += dv_new Mv^T ; dP += do v_new^T (j <= i)
       auto fa1 = [&](int r, int u) { return dvnS[(r0 + r) * SS + u]; };
       auto fb1 = [&](int u, int n) { return MvS[(32 * hf + n) * SS + u]; };
-      wgemm<4, false, false>(accT, 0, VS, fa1, fb1);
+      wgemm_pipe<4, false, false>(accT, 0, VS, fa1, fb1);
       if (!(hf == 1 && mt < 2)) {
         auto fa2 = [&](int r, int u) { return doS[(r0 + r) * SS + u]; };
         auto fb2 = [&](int u, int n) { return vnS[(32 * hf + n) * SS + u]; };
-        wgemm<4, true, false>(accP, 0, VS, fa2, fb2);
+        wgemm_pipe<4, true, false>(accP, 0, VS, fa2, fb2);
       }
       // dk^ += [-diag(beta og) Tu | diag(sv) v_new] [h | dh']^T ; do h^T
       auto fa3 = [&](int r, int u) {
@@ -669,10 +718,10 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
         return u < VS ? -bet[i] * og[i] * TuS[i * SS + u] : sv[i] * vnS[i * SS + u - VS];
       };
       auto fb3 = [&](int u, int n) { return u < VS ? hS[(x0 + n) * SS + u] : dhS[(x0 + n) * SS + u - VS]; };
-      wgemm<NH, false, false>(accK, 0, 2 * VS, fa3, fb3);
+      wgemm_pipe<NH, false, false>(accK, 0, 2 * VS, fa3, fb3);
       auto fa4 = [&](int r, int u) { return doS[(r0 + r) * SS + u]; };
       auto fb4 = [&](int u, int n) { return hS[(x0 + n) * SS + u]; };
-      wgemm<NH, true, false>(accQ, 0, VS, fa4, fb4);
+      wgemm_pipe<NH, true, false>(accQ, 0, VS, fa4, fb4);
     }
     __syncthreads();
   }
@@ -688,7 +737,7 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
     float cc[4][4] = {};
     auto fa = [&](int r, int m) { return DT[(r0 + r) * MS + m]; };
     auto fb = [&](int m, int n) { return Tm[(32 * hf + n) * MS + m]; };
-    wgemm<4, false, false>(cc, 0, 32 * hf + 32, fa, fb);
+    wgemm_pipe<4, false, false>(cc, 0, 32 * hf + 32, fa, fb);
     cvisit(cc, [&](int, int r, int n, float x) { Xm[(r0 + r) * MS + 32 * hf + n] = x; });
   }
   __syncthreads();
@@ -697,7 +746,7 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
     if (!(hf == 1 && mt < 2)) {
       auto fa = [&](int r, int m) { return Tm[m * MS + r0 + r]; };
       auto fb = [&](int m, int n) { return Xm[m * MS + 32 * hf + n]; };
-      wgemm<4, false, false>(cc, r0, 64, fa, fb);
+      wgemm_pipe<4, false, false>(cc, r0, 64, fa, fb);
     }
     cvisit(cc, [&](int, int r, int n, float x) {
       const int i = r0 + r, j = 32 * hf + n;
@@ -746,11 +795,11 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
   {
     auto fa = [&](int r, int m) { return m < 64 ? S1[(r0 + r) * MS + m] : S2[(r0 + r) * MS + m - 64]; };
     auto fb = [&](int m, int n) { return m < 64 ? kv(m, x0 + n) : qv(m - 64, x0 + n); };
-    wgemm<NH, false, true>(accK, 0, 128, fa, fb);
+    wgemm_pipe<NH, false, true>(accK, 0, 128, fa, fb);
     cvisit(accQ, [&](int, int r, int, float &x) { x *= scale * og[r0 + r]; });
     auto fa2 = [&](int r, int m) { return S3[(r0 + r) * MS + m]; };
     auto fb2 = [&](int m, int n) { return kv(m, x0 + n); };
-    wgemm<NH, false, true>(accQ, 0, r0 + 16, fa2, fb2);
+    wgemm_pipe<NH, false, true>(accQ, 0, r0 + 16, fa2, fb2);
   }
   // ---- through the L2 norms (dx = r (dx^ - x^ (x^ . dx^))), summed over the group's value heads
   {
