@@ -576,28 +576,25 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
       }
     }
     __syncthreads();
-    // k^ h, q^ h, k^ dh' (columns 16 hf ..): k, q exact, h, dh' split
+    // k^ h and k^ dh' (columns 16 hf ..): k exact, h, dh' split.  (The q^ h of
+    // d gamma's output term is not needed: sum_c (q^_i . h_c) do_ic equals
+    // q^_i . (do h^T)_i, formed from the dq^ accumulator after the slices.)
     {
-      float ckh[2][4] = {}, cqh[2][4] = {}, ckd[2][4] = {};
+      float ckh[2][4] = {}, ckd[2][4] = {};
       const int n0 = 16 * hf;
       auto fk = [&](int r, int x) { return kv(r0 + r, x); };
-      auto fq = [&](int r, int x) { return qv(r0 + r, x); };
       auto fh = [&](int x, int n) { return hS[x * SS + n0 + n]; };
       auto fd = [&](int x, int n) { return dhS[x * SS + n0 + n]; };
-      // one pass over K for the three products (shared fragments, six accumulators)
+      // one pass over K for the two products (shared fragments, four accumulators)
       {
         const int fr = lane >> 2, ft = lane & 3;
 #pragma unroll 2
         for (int kk = 0; kk < K; kk += 8) {
-          uint32_t ak[4], aq[4];
+          uint32_t ak[4];
           ak[0] = __float_as_uint(fk(fr, kk + ft));
           ak[1] = __float_as_uint(fk(fr + 8, kk + ft));
           ak[2] = __float_as_uint(fk(fr, kk + ft + 4));
           ak[3] = __float_as_uint(fk(fr + 8, kk + ft + 4));
-          aq[0] = __float_as_uint(fq(fr, kk + ft));
-          aq[1] = __float_as_uint(fq(fr + 8, kk + ft));
-          aq[2] = __float_as_uint(fq(fr, kk + ft + 4));
-          aq[3] = __float_as_uint(fq(fr + 8, kk + ft + 4));
           uint32_t hh[2][2], hl[2][2], dh_[2][2], dl[2][2];
 #pragma unroll
           for (int n = 0; n < 2; ++n)
@@ -612,13 +609,11 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
 #pragma unroll
           for (int n = 0; n < 2; ++n) {
             mma_tf32(ckh[n], ak, hh[n][0], hh[n][1]);
-            mma_tf32(cqh[n], aq, hh[n][0], hh[n][1]);
             mma_tf32(ckd[n], ak, dh_[n][0], dh_[n][1]);
           }
 #pragma unroll
           for (int n = 0; n < 2; ++n) {
             mma_tf32(ckh[n], ak, hl[n][0], hl[n][1]);
-            mma_tf32(cqh[n], aq, hl[n][0], hl[n][1]);
             mma_tf32(ckd[n], ak, dl[n][0], dl[n][1]);
           }
         }
@@ -630,17 +625,6 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
         MvS[i * SS + cc] = bet[i] * (vS[i * SS + cc] - og[i] * kh);
       });
       cvisit(ckd, [&](int, int r, int n, float x) { KdhS[(r0 + r) * SS + n0 + n] = x * rk[r0 + r]; });
-      float sq[2] = {0.f, 0.f};
-      cvisit(cqh, [&](int rh, int r, int n, float x) {
-        const int i = r0 + r;
-        sq[rh] = fmaf(x * rq[i], doS[i * SS + n0 + n], sq[rh]);
-      });
-      sq[0] = quad_sum(sq[0]);
-      sq[1] = quad_sum(sq[1]);
-      if (t4 == 0) {
-        atomicAdd(&SQ[r0 + g8], sq[0]);
-        atomicAdd(&SQ[r0 + g8 + 8], sq[1]);
-      }
     }
     __syncthreads();
     if (warp < 4) {
@@ -796,6 +780,17 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
     auto fa = [&](int r, int m) { return m < 64 ? S1[(r0 + r) * MS + m] : S2[(r0 + r) * MS + m - 64]; };
     auto fb = [&](int m, int n) { return m < 64 ? kv(m, x0 + n) : qv(m - 64, x0 + n); };
     wgemm_pipe<NH, false, true>(accK, 0, 128, fa, fb);
+    // d gamma's output term: sum_c (q^_i . h_c) do_ic = q^_i . (do h^T)_i
+    {
+      float sq[2] = {0.f, 0.f};
+      cvisit(accQ, [&](int rh, int r, int n, float x) { sq[rh] = fmaf(qv(r0 + r, x0 + n), x, sq[rh]); });
+#pragma unroll
+      for (int u = 0; u < 2; ++u) sq[u] = quad_sum(sq[u]);
+      if (t4 == 0) {
+        atomicAdd(&SQ[r0 + g8], rq[r0 + g8] * sq[0]);
+        atomicAdd(&SQ[r0 + g8 + 8], rq[r0 + g8 + 8] * sq[1]);
+      }
+    }
     cvisit(accQ, [&](int, int r, int, float &x) { x *= scale * og[r0 + r]; });
     auto fa2 = [&](int r, int m) { return S3[(r0 + r) * MS + m]; };
     auto fb2 = [&](int m, int n) { return kv(m, x0 + n); };
