@@ -179,13 +179,17 @@ constexpr int MS = 68;  // fp32 row stride of a 64 x 64 tile
 constexpr int SS = 36;  // fp32 row stride of a 32-column slice
 
 // ------------------------------------------------------------------ dh walk
-// One CTA per (32-column slice of V, value head, sequence), last chunk first.
-// dh (K x 32 fp32) lives in the mma accumulators of the eight warps (warp w:
+// One CTA per (64-column slice of V, value head, sequence), last chunk first
+// (64 columns: at V = 128 the grid of HV x N x 2 CTAs fits one wave of SMs for
+// the usual head counts, where 32-column slices needed two).
+// dh (K x 64 fp32) lives in the mma accumulators of the eight warps (warp w:
 // rows of tile w % (K / 16), a share of the columns); per chunk K, Q, W, P,
 // the scalars and the do slice are staged in shared memory (cp.async, double
 // buffered).  Both products of a chunk run on mma.sync tf32: the raw bf16 k,
 // q, W, P hi / lo and do are exact in tf32, the computed dh' and dv_new are
 // split hi + lo.
+constexpr int DVC = 64;  // V columns per dh-walk CTA
+
 template <int K>
 struct DhLay {
   static constexpr int KROW = K * 2 + 16;             // padded bf16 row of K keys
@@ -194,12 +198,12 @@ struct DhLay {
   static constexpr int OFF_REC = OFF_Q + 64 * KROW;   // record bytes W | PH | PL (contiguous in the record)
   static constexpr int REC_BYTES = Rec<K>::TS;        // W + PH + PL
   static constexpr int OFF_SC = OFF_REC + REC_BYTES;  // record scalars (1 KB)
-  static constexpr int DOROW = 96;                    // padded bf16 row of the 32-column do slice
+  static constexpr int DOROW = DVC * 2 + 32;          // padded bf16 row of the do slice (bytes)
   static constexpr int OFF_DO = OFF_SC + 1024;        // do slice [64][DOROW bytes]
   static constexpr int STAGE = OFF_DO + 64 * DOROW;
   // dh' and dv_new are read as B operands (row k + t, column g of a fragment):
   // a row stride of 8 (mod 32) words keeps those reads free of bank conflicts.
-  static constexpr int BS = 40;
+  static constexpr int BS = DVC + 8;
   static constexpr int OFF_DHS = 2 * STAGE;           // dh' [K][BS] fp32
   static constexpr int OFF_DVN = OFF_DHS + K * BS * 4;  // dv_new [64][BS] fp32
   static constexpr int BYTES = OFF_DVN + 64 * BS * 4;
@@ -217,9 +221,9 @@ __global__ void __launch_bounds__(BT, 1) chunk_dh_kernel(
   constexpr int KE = Ly::KROW / 2;  // bf16 elements per staged K / Q row
   constexpr int MTK = K / 16;       // row tiles of dh
   constexpr int WPM = 8 / MTK;      // warps per row tile
-  constexpr int NTD = 4 / WPM;      // n-tiles (8 columns) per warp
+  constexpr int NTD = DVC / 8 / WPM;  // n-tiles (8 columns) per warp
   extern __shared__ __align__(16) unsigned char smem[];
-  const int vt0 = blockIdx.x * 32, hv = blockIdx.y, n = blockIdx.z;
+  const int vt0 = blockIdx.x * DVC, hv = blockIdx.y, n = blockIdx.z;
   const int h = hv / (HV / H);
   const int tid = threadIdx.x, warp = tid >> 5;
   const int dm0 = 16 * (warp % MTK), dc0 = 8 * NTD * (warp / MTK);  // this warp's block of dh
@@ -253,8 +257,8 @@ __global__ void __launch_bounds__(BT, 1) chunk_dh_kernel(
     const unsigned char *rec = ws + ((size_t)(cb + c) * HV + hv) * R::BYTES;
     for (int e = tid; e < Ly::REC_BYTES / 16; e += BT) cp_async16(S + Ly::OFF_REC + e * 16, rec + e * 16, true);
     for (int e = tid; e < 1024 / 16; e += BT) cp_async16(S + Ly::OFF_SC + e * 16, rec + R::SC + e * 16, true);
-    for (int e = tid; e < 64 * 4; e += BT) {
-      const int row = e >> 2, ch = e & 3;
+    for (int e = tid; e < 64 * (DVC / 8); e += BT) {
+      const int row = e / (DVC / 8), ch = e % (DVC / 8);
       const bool ok = row < L;
       const int64_t g = ok ? ((trow + row) * HV + hv) * V + vt0 + ch * 8 : 0;
       cp_async16(S + Ly::OFF_DO + row * Ly::DOROW + ch * 16, dout + g, ok);
@@ -293,19 +297,20 @@ __global__ void __launch_bounds__(BT, 1) chunk_dh_kernel(
     const unsigned char *PL = S + Ly::OFF_REC + (R::PL - R::W);
     // dv_new = diag(sv) K dh' + scale (P_hi + P_lo)^T do   (sv carries 1/||k||)
     {
-      float ca[2][4] = {}, cp[2][4] = {};
-      const int n0 = 16 * hf;
+      constexpr int NTV = DVC / 16;  // n-tiles of a warp's half of the columns
+      float ca[NTV][4] = {}, cp[NTV][4] = {};
+      const int n0 = (DVC / 2) * hf;
       auto fk = [&](int r, int x) { return bf2f(Ks[(r0 + r) * KE + x]); };
       auto fd = [&](int x, int nn) { return dhs[x * Ly::BS + n0 + nn]; };
-      wgemm<2, true, false>(ca, 0, K, fk, fd);
+      wgemm<NTV, true, false>(ca, 0, K, fk, fd);
       auto fph = [&](int r, int i) { return tile64(PH, i, r0 + r); };
       auto fpl = [&](int r, int i) { return tile64(PL, i, r0 + r); };
       auto fo = [&](int i, int nn) { return bf2f(Ds[i * (Ly::DOROW / 2) + n0 + nn]); };
-      wgemm<2, true, true>(cp, r0, 64, fph, fo);
-      wgemm<2, true, true>(cp, r0, 64, fpl, fo);
+      wgemm<NTV, true, true>(cp, r0, 64, fph, fo);
+      wgemm<NTV, true, true>(cp, r0, 64, fpl, fo);
       const int g = (tid & 31) >> 2, t = tid & 3;
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < NTV; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int j = r0 + g + 8 * (e >> 1);
@@ -888,7 +893,7 @@ cudaError_t launch_bwd_k(const gdn_host::ChunkBwdArgs &a, cudaStream_t s) {
     const int smem = DhLay<K>::BYTES;
     e = cudaFuncSetAttribute(chunk_dh_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    chunk_dh_kernel<K><<<dim3(a.V / 32, a.HV, a.N), BT, smem, s>>>(
+    chunk_dh_kernel<K><<<dim3(a.V / DVC, a.HV, a.N), BT, smem, s>>>(
         a.q, a.k, a.dout, static_cast<const unsigned char *>(a.ws), DH, a.dht, a.dh0, a.scale, a.cu, cs, a.T,
         a.H, a.HV, a.V, a.dev_status);
     e = cudaGetLastError();
