@@ -744,17 +744,20 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
   }
   __syncthreads();
   // ---- through A_ij = beta_i EK_ij and P_ij: d beta, d gamma (row +, column -),
-  // and the coefficient tiles of the last products.
+  // and the coefficient tiles of the last products.  Thread (i, q4) takes
+  // elements (i, j) and (j, i) for j = q4 + 4 m, so both the row and the column
+  // sums of row / column i reduce within its quad (no shared atomics).
   {
     const int i = tid >> 2, q4 = tid & 3;
-    float sb = 0.f, sr = 0.f;
+    float sb = 0.f, sr = 0.f, sc = 0.f;
+#pragma unroll 4
     for (int m = 0; m < 16; ++m) {
       const int j = q4 + 4 * m;
-      const float da = DT[i * MS + j], dp = DP[i * MS + j];
-      const float term = fmaf(da * bet[i], EK[i * MS + j], dp * Pm[i * MS + j]);
-      sb = fmaf(da, EK[i * MS + j], sb);
-      sr += term;
-      atomicAdd(&DG[j], -term);
+      const float da = DT[i * MS + j], dp = DP[i * MS + j], ek = EK[i * MS + j];
+      const float daT = DT[j * MS + i], dpT = DP[j * MS + i];
+      sb = fmaf(da, ek, sb);
+      sr += fmaf(da * bet[i], ek, dp * Pm[i * MS + j]);
+      sc += fmaf(daT * bet[j], EK[j * MS + i], dpT * Pm[j * MS + i]);
       float s1 = 0.f, s2 = 0.f, s3 = 0.f;
       if (j < i) {
         const float e = expf(gam[i] - gam[j]);
@@ -762,8 +765,8 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
         s3 = dp * e * rk[j];
       } else if (j > i) {
         const float e = expf(gam[j] - gam[i]);
-        s1 = DT[j * MS + i] * bet[j] * e * rk[j];
-        s2 = DP[j * MS + i] * e * rq[j];
+        s1 = daT * bet[j] * e * rk[j];
+        s2 = dpT * e * rq[j];
       } else {
         s2 = dp * rq[j];
         s3 = dp * rk[j];
@@ -774,9 +777,10 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
     }
     sb = quad_sum(sb);
     sr = quad_sum(sr);
+    sc = quad_sum(sc);
     if (q4 == 0) {
       DB[i] += sb;
-      atomicAdd(&DG[i], sr);
+      DG[i] += sr - sc;
     }
   }
   __syncthreads();
