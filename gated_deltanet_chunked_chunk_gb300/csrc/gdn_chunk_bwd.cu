@@ -169,6 +169,7 @@ __device__ __forceinline__ void cvisit(float (&c)[NT][4], F f) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) f(e >> 1, g + 8 * (e >> 1), 8 * n + 2 * t + (e & 1), c[n][e]);
 }
+__device__ __forceinline__ void prefetch_l2(const void *p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 __device__ __forceinline__ float quad_sum(float x) {
   x += __shfl_xor_sync(0xffffffffu, x, 1);
   return x + __shfl_xor_sync(0xffffffffu, x, 2);
@@ -439,6 +440,16 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
   auto qv = [&](int i, int x) { return bf2f(Qb[i * BR + x]); };
   auto kv = [&](int i, int x) { return bf2f(Kb[i * BR + x]); };
 
+  // The rows of a V slice (h, dh': K rows of 128 bytes; v, do: L rows of 64)
+  // into L2, one line per thread; slice 0 lands while the chunk's own
+  // products run, slice s + 1 during slice s.
+  auto prefetch_slice = [&](int v0) {
+    const int64_t hb = ((slot * HV + hv) * K) * (int64_t)V + v0;
+    if (tid < 2 * K) prefetch_l2((tid < K ? Hs : DH) + hb + (int64_t)(tid % K) * V);
+    const int i = tid & 63;
+    if (tid < 128 && i < L) prefetch_l2((tid < 64 ? v : dout) + ((trow0 + i) * HV + hv) * V + v0);
+  };
+  prefetch_slice(0);
   // ---- raw q, k rows (zero past L), gates and their cumsum
   for (int e = tid; e < 64 * (K / 8); e += BT) {
     const int i = e / (K / 8), ch = e % (K / 8);
@@ -555,6 +566,7 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
   const int x0 = hf * (K / 2);
   for (int v0 = 0; v0 < V; v0 += VS) {
     const int64_t hb = ((slot * HV + hv) * K) * (int64_t)V + v0;
+    if (v0 + VS < V) prefetch_slice(v0 + VS);
     for (int e = tid; e < K * (VS / 4); e += BT) {
       const int x = e / (VS / 4), c4 = e % (VS / 4);
       *reinterpret_cast<float4 *>(hS + x * SS + 4 * c4) =
