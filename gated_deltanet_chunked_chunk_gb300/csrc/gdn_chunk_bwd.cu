@@ -160,6 +160,56 @@ __device__ __forceinline__ void wgemm_pipe(float (&c)[NT][4], int k0, int k1, FA
     }
   }
 }
+// The same product on mma.sync m16n8k16 in bf16 (twice the k of a tf32 step
+// per instruction): a computed operand is split into bf16 hi + lo (about 16
+// bits kept; hi*hi + hi*lo + lo*hi leaves a relative error near 2^-17), an
+// operand of raw bf16 values has no low part.  fa2(r, k) and fb2(k, n) return
+// the pairs (A[r][k], A[r][k + 1]) and (B[k][n], B[k + 1][n]).
+__device__ __forceinline__ void split_bf16(float2 v, uint32_t &hi, uint32_t &lo) {
+  hi = pack_bf16(v.x, v.y);
+  lo = pack_bf16(v.x - bf16lo_f(hi), v.y - bf16hi_f(hi));
+}
+template <int NT, bool AX, bool BX, class FA2, class FB2>
+__device__ __forceinline__ void wgemm_bf(float (&c)[NT][4], int k0, int k1, FA2 fa2, FB2 fb2) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll 2
+  for (int k = k0; k < k1; k += 16) {
+    const float2 av[4] = {fa2(g, k + 2 * t), fa2(g + 8, k + 2 * t), fa2(g, k + 2 * t + 8), fa2(g + 8, k + 2 * t + 8)};
+    uint32_t ah[4], al[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (AX) {
+        ah[e] = pack_bf16(av[e].x, av[e].y);
+        al[e] = 0u;
+      } else {
+        split_bf16(av[e], ah[e], al[e]);
+      }
+    }
+    uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      const float2 b0 = fb2(k + 2 * t, 8 * n + g), b1 = fb2(k + 2 * t + 8, 8 * n + g);
+      if (BX) {
+        bh[n][0] = pack_bf16(b0.x, b0.y);
+        bh[n][1] = pack_bf16(b1.x, b1.y);
+        bl[n][0] = bl[n][1] = 0u;
+      } else {
+        split_bf16(b0, bh[n][0], bl[n][0]);
+        split_bf16(b1, bh[n][1], bl[n][1]);
+      }
+    }
+#pragma unroll
+    for (int n = 0; n < NT; ++n) mma_bf16(c[n], ah, bh[n][0], bh[n][1]);
+    if (!BX) {
+#pragma unroll
+      for (int n = 0; n < NT; ++n) mma_bf16(c[n], ah, bl[n][0], bl[n][1]);
+    }
+    if (!AX) {
+#pragma unroll
+      for (int n = 0; n < NT; ++n) mma_bf16(c[n], al, bh[n][0], bh[n][1]);
+    }
+  }
+}
 // f(rh, r, n, x) for every accumulator element: row r = g + 8 rh, column n.
 template <int NT, class F>
 __device__ __forceinline__ void cvisit(float (&c)[NT][4], F f) {
@@ -704,25 +754,32 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
     }
     __syncthreads();
     {
-      // dT += dv_new Mv^T ; dP += do v_new^T (j <= i)
-      auto fa1 = [&](int r, int u) { return dvnS[(r0 + r) * SS + u]; };
-      auto fb1 = [&](int u, int n) { return MvS[(32 * hf + n) * SS + u]; };
-      wgemm_pipe<4, false, false>(accT, 0, VS, fa1, fb1);
+      // dT += dv_new Mv^T ; dP += do v_new^T (j <= i)   (bf16 m16n8k16, pairs along the slice)
+      auto ld2 = [](const float *p) { return *reinterpret_cast<const float2 *>(p); };
+      auto fa1 = [&](int r, int u) { return ld2(dvnS + (r0 + r) * SS + u); };
+      auto fb1 = [&](int u, int n) { return ld2(MvS + (32 * hf + n) * SS + u); };
+      wgemm_bf<4, false, false>(accT, 0, VS, fa1, fb1);
       if (!(hf == 1 && mt < 2)) {
-        auto fa2 = [&](int r, int u) { return doS[(r0 + r) * SS + u]; };
-        auto fb2 = [&](int u, int n) { return vnS[(32 * hf + n) * SS + u]; };
-        wgemm_pipe<4, true, false>(accP, 0, VS, fa2, fb2);
+        auto fa2 = [&](int r, int u) { return ld2(doS + (r0 + r) * SS + u); };
+        auto fb2 = [&](int u, int n) { return ld2(vnS + (32 * hf + n) * SS + u); };
+        wgemm_bf<4, true, false>(accP, 0, VS, fa2, fb2);
       }
       // dk^ += [-diag(beta og) Tu | diag(sv) v_new] [h | dh']^T ; do h^T
       auto fa3 = [&](int r, int u) {
         const int i = r0 + r;
-        return u < VS ? -bet[i] * og[i] * TuS[i * SS + u] : sv[i] * vnS[i * SS + u - VS];
+        if (u < VS) {
+          const float f = -bet[i] * og[i];
+          const float2 x = ld2(TuS + i * SS + u);
+          return make_float2(f * x.x, f * x.y);
+        }
+        const float2 x = ld2(vnS + i * SS + u - VS);
+        return make_float2(sv[i] * x.x, sv[i] * x.y);
       };
-      auto fb3 = [&](int u, int n) { return u < VS ? hS[(x0 + n) * SS + u] : dhS[(x0 + n) * SS + u - VS]; };
-      wgemm_pipe<NH, false, false>(accK, 0, 2 * VS, fa3, fb3);
-      auto fa4 = [&](int r, int u) { return doS[(r0 + r) * SS + u]; };
-      auto fb4 = [&](int u, int n) { return hS[(x0 + n) * SS + u]; };
-      wgemm_pipe<NH, true, false>(accQ, 0, VS, fa4, fb4);
+      auto fb3 = [&](int u, int n) { return u < VS ? ld2(hS + (x0 + n) * SS + u) : ld2(dhS + (x0 + n) * SS + u - VS); };
+      wgemm_bf<NH, false, false>(accK, 0, 2 * VS, fa3, fb3);
+      auto fa4 = [&](int r, int u) { return ld2(doS + (r0 + r) * SS + u); };
+      auto fb4 = [&](int u, int n) { return ld2(hS + (x0 + n) * SS + u); };
+      wgemm_bf<NH, true, false>(accQ, 0, VS, fa4, fb4);
     }
     __syncthreads();
   }
