@@ -489,6 +489,12 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
   const int64_t trow0 = tok0 + (int64_t)c * C;
   auto qv = [&](int i, int x) { return bf2f(Qb[i * BR + x]); };
   auto kv = [&](int i, int x) { return bf2f(Kb[i * BR + x]); };
+  // (x, x + 1) of a raw row, x even: one 32-bit load
+  auto pair_of = [](const uint16_t *p) {
+    const uint32_t w = *reinterpret_cast<const uint32_t *>(p);
+    return make_float2(bf16lo_f(w), bf16hi_f(w));
+  };
+  auto ld2 = [](const float *p) { return *reinterpret_cast<const float2 *>(p); };
 
   // The rows of a V slice (h, dh': K rows of 128 bytes; v, do: L rows of 64)
   // into L2, one line per thread; slice 0 lands while the chunk's own
@@ -555,11 +561,11 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
   // ---- k k^T and q k^T (exact bf16 operands): EK, A (into Tm), P
   {
     float ck[4][4] = {}, cq[4][4] = {};
-    auto fk = [&](int r, int x) { return kv(r0 + r, x); };
-    auto fq = [&](int r, int x) { return qv(r0 + r, x); };
-    auto fkt = [&](int x, int n) { return kv(32 * hf + n, x); };
-    wgemm_pipe<4, true, true>(ck, 0, K, fk, fkt);
-    wgemm_pipe<4, true, true>(cq, 0, K, fq, fkt);
+    auto fk = [&](int r, int x) { return pair_of(Kb + (r0 + r) * BR + x); };
+    auto fq = [&](int r, int x) { return pair_of(Qb + (r0 + r) * BR + x); };
+    auto fkt = [&](int x, int n) { return pair_of(Kb + (32 * hf + n) * BR + x); };
+    wgemm_bf<4, true, true>(ck, 0, K, fk, fkt);
+    wgemm_bf<4, true, true>(cq, 0, K, fq, fkt);
     cvisit(ck, [&](int, int r, int n, float x) {
       const int i = r0 + r, j = 32 * hf + n;
       const float ek = (j < i) ? expf(gam[i] - gam[j]) * x * rk[i] * rk[j] : 0.f;
@@ -649,39 +655,35 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
     {
       float ckh[2][4] = {}, ckd[2][4] = {};
       const int n0 = 16 * hf;
-      auto fk = [&](int r, int x) { return kv(r0 + r, x); };
-      auto fh = [&](int x, int n) { return hS[x * SS + n0 + n]; };
-      auto fd = [&](int x, int n) { return dhS[x * SS + n0 + n]; };
-      // one pass over K for the two products (shared fragments, four accumulators)
+      // one pass over K for the two products (shared fragments, four accumulators),
+      // bf16 m16n8k16: k raw (exact), h and dh' split hi + lo
       {
         const int fr = lane >> 2, ft = lane & 3;
 #pragma unroll 2
-        for (int kk = 0; kk < K; kk += 8) {
+        for (int kk = 0; kk < K; kk += 16) {
           uint32_t ak[4];
-          ak[0] = __float_as_uint(fk(fr, kk + ft));
-          ak[1] = __float_as_uint(fk(fr + 8, kk + ft));
-          ak[2] = __float_as_uint(fk(fr, kk + ft + 4));
-          ak[3] = __float_as_uint(fk(fr + 8, kk + ft + 4));
+          ak[0] = *reinterpret_cast<const uint32_t *>(Kb + (r0 + fr) * BR + kk + 2 * ft);
+          ak[1] = *reinterpret_cast<const uint32_t *>(Kb + (r0 + fr + 8) * BR + kk + 2 * ft);
+          ak[2] = *reinterpret_cast<const uint32_t *>(Kb + (r0 + fr) * BR + kk + 2 * ft + 8);
+          ak[3] = *reinterpret_cast<const uint32_t *>(Kb + (r0 + fr + 8) * BR + kk + 2 * ft + 8);
           uint32_t hh[2][2], hl[2][2], dh_[2][2], dl[2][2];
 #pragma unroll
           for (int n = 0; n < 2; ++n)
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-              const float x = fh(kk + ft + 4 * u, 8 * n + fr), y = fd(kk + ft + 4 * u, 8 * n + fr);
-              hh[n][u] = tf32_rna(x);
-              hl[n][u] = tf32_rna(x - __uint_as_float(hh[n][u]));
-              dh_[n][u] = tf32_rna(y);
-              dl[n][u] = tf32_rna(y - __uint_as_float(dh_[n][u]));
+              const int x = kk + 2 * ft + 8 * u, c = n0 + 8 * n + fr;
+              split_bf16(make_float2(hS[x * SS + c], hS[(x + 1) * SS + c]), hh[n][u], hl[n][u]);
+              split_bf16(make_float2(dhS[x * SS + c], dhS[(x + 1) * SS + c]), dh_[n][u], dl[n][u]);
             }
 #pragma unroll
           for (int n = 0; n < 2; ++n) {
-            mma_tf32(ckh[n], ak, hh[n][0], hh[n][1]);
-            mma_tf32(ckd[n], ak, dh_[n][0], dh_[n][1]);
+            mma_bf16(ckh[n], ak, hh[n][0], hh[n][1]);
+            mma_bf16(ckd[n], ak, dh_[n][0], dh_[n][1]);
           }
 #pragma unroll
           for (int n = 0; n < 2; ++n) {
-            mma_tf32(ckh[n], ak, hl[n][0], hl[n][1]);
-            mma_tf32(ckd[n], ak, dl[n][0], dl[n][1]);
+            mma_bf16(ckh[n], ak, hl[n][0], hl[n][1]);
+            mma_bf16(ckd[n], ak, dl[n][0], dl[n][1]);
           }
         }
       }
@@ -697,16 +699,16 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
     if (warp < 4) {
       // v_new = T Mv (T lower)
       float cc[4][4] = {};
-      auto fa = [&](int r, int m) { return Tm[(r0 + r) * MS + m]; };
-      auto fb = [&](int m, int n) { return MvS[m * SS + n]; };
-      wgemm_pipe<4, false, false>(cc, 0, r0 + 16, fa, fb);
+      auto fa = [&](int r, int m) { return ld2(Tm + (r0 + r) * MS + m); };
+      auto fb = [&](int m, int n) { return make_float2(MvS[m * SS + n], MvS[(m + 1) * SS + n]); };
+      wgemm_bf<4, false, false>(cc, 0, r0 + 16, fa, fb);
       cvisit(cc, [&](int, int r, int n, float x) { vnS[(r0 + r) * SS + n] = x; });
     } else {
       // dv_new = diag(sv) k^ dh' + scale P^T do (P^T upper)
       float cc[4][4] = {};
-      auto fa = [&](int r, int m) { return Pm[m * MS + r0 + r]; };
-      auto fb = [&](int m, int n) { return doS[m * SS + n]; };
-      wgemm_pipe<4, false, true>(cc, r0, 64, fa, fb);
+      auto fa = [&](int r, int m) { return make_float2(Pm[m * MS + r0 + r], Pm[(m + 1) * MS + r0 + r]); };
+      auto fb = [&](int m, int n) { return make_float2(doS[m * SS + n], doS[(m + 1) * SS + n]); };
+      wgemm_bf<4, false, true>(cc, r0, 64, fa, fb);
       cvisit(cc, [&](int, int r, int n, float x) {
         const int i = r0 + r;
         dvnS[i * SS + n] = fmaf(sv[i], KdhS[i * SS + n], scale * x);
@@ -716,9 +718,9 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
     if (warp < 4) {
       // Tu = T^T dv_new (T^T upper); dv = diag(beta) Tu; d beta, d gamma row sums
       float cc[4][4] = {};
-      auto fa = [&](int r, int m) { return Tm[m * MS + r0 + r]; };
-      auto fb = [&](int m, int n) { return dvnS[m * SS + n]; };
-      wgemm_pipe<4, false, false>(cc, r0, 64, fa, fb);
+      auto fa = [&](int r, int m) { return make_float2(Tm[m * MS + r0 + r], Tm[(m + 1) * MS + r0 + r]); };
+      auto fb = [&](int m, int n) { return make_float2(dvnS[m * SS + n], dvnS[(m + 1) * SS + n]); };
+      wgemm_bf<4, false, false>(cc, r0, 64, fa, fb);
       float sb[2] = {0.f, 0.f}, sg[2] = {0.f, 0.f};
       cvisit(cc, [&](int rh, int r, int n, float x) {
         const int i = r0 + r;
@@ -755,7 +757,6 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
     __syncthreads();
     {
       // dT += dv_new Mv^T ; dP += do v_new^T (j <= i)   (bf16 m16n8k16, pairs along the slice)
-      auto ld2 = [](const float *p) { return *reinterpret_cast<const float2 *>(p); };
       auto fa1 = [&](int r, int u) { return ld2(dvnS + (r0 + r) * SS + u); };
       auto fb1 = [&](int u, int n) { return ld2(MvS + (32 * hf + n) * SS + u); };
       wgemm_bf<4, false, false>(accT, 0, VS, fa1, fb1);
@@ -793,18 +794,18 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
   __syncthreads();
   {
     float cc[4][4] = {};
-    auto fa = [&](int r, int m) { return DT[(r0 + r) * MS + m]; };
-    auto fb = [&](int m, int n) { return Tm[(32 * hf + n) * MS + m]; };
-    wgemm_pipe<4, false, false>(cc, 0, 32 * hf + 32, fa, fb);
+    auto fa = [&](int r, int m) { return ld2(DT + (r0 + r) * MS + m); };
+    auto fb = [&](int m, int n) { return ld2(Tm + (32 * hf + n) * MS + m); };
+    wgemm_bf<4, false, false>(cc, 0, 32 * hf + 32, fa, fb);
     cvisit(cc, [&](int, int r, int n, float x) { Xm[(r0 + r) * MS + 32 * hf + n] = x; });
   }
   __syncthreads();
   {
     float cc[4][4] = {};
     if (!(hf == 1 && mt < 2)) {
-      auto fa = [&](int r, int m) { return Tm[m * MS + r0 + r]; };
-      auto fb = [&](int m, int n) { return Xm[m * MS + 32 * hf + n]; };
-      wgemm_pipe<4, false, false>(cc, r0, 64, fa, fb);
+      auto fa = [&](int r, int m) { return make_float2(Tm[m * MS + r0 + r], Tm[(m + 1) * MS + r0 + r]); };
+      auto fb = [&](int m, int n) { return make_float2(Xm[m * MS + 32 * hf + n], Xm[(m + 1) * MS + 32 * hf + n]); };
+      wgemm_bf<4, false, false>(cc, r0, 64, fa, fb);
     }
     cvisit(cc, [&](int, int r, int n, float x) {
       const int i = r0 + r, j = 32 * hf + n;
@@ -855,9 +856,11 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
   __syncthreads();
   // ---- dk^ += [S1 | S2] [k; q] ; dq^ = scale og (do h^T) + S3 k
   {
-    auto fa = [&](int r, int m) { return m < 64 ? S1[(r0 + r) * MS + m] : S2[(r0 + r) * MS + m - 64]; };
-    auto fb = [&](int m, int n) { return m < 64 ? kv(m, x0 + n) : qv(m - 64, x0 + n); };
-    wgemm_pipe<NH, false, true>(accK, 0, 128, fa, fb);
+    auto fa = [&](int r, int m) { return m < 64 ? ld2(S1 + (r0 + r) * MS + m) : ld2(S2 + (r0 + r) * MS + m - 64); };
+    auto fb = [&](int m, int n) {
+      return m < 64 ? make_float2(kv(m, x0 + n), kv(m + 1, x0 + n)) : make_float2(qv(m - 64, x0 + n), qv(m - 63, x0 + n));
+    };
+    wgemm_bf<NH, false, true>(accK, 0, 128, fa, fb);
     // d gamma's output term: sum_c (q^_i . h_c) do_ic = q^_i . (do h^T)_i
     {
       float sq[2] = {0.f, 0.f};
@@ -870,9 +873,9 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
       }
     }
     cvisit(accQ, [&](int, int r, int, float &x) { x *= scale * og[r0 + r]; });
-    auto fa2 = [&](int r, int m) { return S3[(r0 + r) * MS + m]; };
-    auto fb2 = [&](int m, int n) { return kv(m, x0 + n); };
-    wgemm_pipe<NH, false, true>(accQ, 0, r0 + 16, fa2, fb2);
+    auto fa2 = [&](int r, int m) { return ld2(S3 + (r0 + r) * MS + m); };
+    auto fb2 = [&](int m, int n) { return make_float2(kv(m, x0 + n), kv(m + 1, x0 + n)); };
+    wgemm_bf<NH, false, true>(accQ, 0, r0 + 16, fa2, fb2);
   }
   // ---- through the L2 norms (dx = r (dx^ - x^ (x^ . dx^))), summed over the group's value heads
   {
