@@ -160,6 +160,25 @@ __device__ __forceinline__ void wgemm_pipe(float (&c)[NT][4], int k0, int k1, FA
     }
   }
 }
+// f(rh, r, n, x) for every accumulator element: row r = g + 8 rh, column n.
+template <int NT, class F>
+__device__ __forceinline__ void cvisit(float (&c)[NT][4], F f) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int n = 0; n < NT; ++n)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) f(e >> 1, g + 8 * (e >> 1), 8 * n + 2 * t + (e & 1), c[n][e]);
+}
+__device__ __forceinline__ void prefetch_l2(const void *p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+__device__ __forceinline__ float quad_sum(float x) {
+  x += __shfl_xor_sync(0xffffffffu, x, 1);
+  return x + __shfl_xor_sync(0xffffffffu, x, 2);
+}
+
+constexpr int VS = 32;  // V columns per slice
+constexpr int MS = 68;  // fp32 row stride of a 64 x 64 tile
+constexpr int SS = 36;  // fp32 row stride of a 32-column slice
+
 // The same product on mma.sync m16n8k16 in bf16 (twice the k of a tf32 step
 // per instruction): a computed operand is split into bf16 hi + lo (about 16
 // bits kept; hi*hi + hi*lo + lo*hi leaves a relative error near 2^-17), an
@@ -210,25 +229,6 @@ __device__ __forceinline__ void wgemm_bf(float (&c)[NT][4], int k0, int k1, FA2 
     }
   }
 }
-// f(rh, r, n, x) for every accumulator element: row r = g + 8 rh, column n.
-template <int NT, class F>
-__device__ __forceinline__ void cvisit(float (&c)[NT][4], F f) {
-  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-#pragma unroll
-  for (int n = 0; n < NT; ++n)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) f(e >> 1, g + 8 * (e >> 1), 8 * n + 2 * t + (e & 1), c[n][e]);
-}
-__device__ __forceinline__ void prefetch_l2(const void *p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
-__device__ __forceinline__ float quad_sum(float x) {
-  x += __shfl_xor_sync(0xffffffffu, x, 1);
-  return x + __shfl_xor_sync(0xffffffffu, x, 2);
-}
-
-constexpr int VS = 32;  // V columns per slice
-constexpr int MS = 68;  // fp32 row stride of a 64 x 64 tile
-constexpr int SS = 36;  // fp32 row stride of a 32-column slice
-
 // ------------------------------------------------------------------ dh walk
 // One CTA per (64-column slice of V, value head, sequence), last chunk first
 // (64 columns: at V = 128 the grid of HV x N x 2 CTAs fits one wave of SMs for
@@ -351,14 +351,20 @@ __global__ void __launch_bounds__(BT, 1) chunk_dh_kernel(
       constexpr int NTV = DVC / 16;  // n-tiles of a warp's half of the columns
       float ca[NTV][4] = {}, cp[NTV][4] = {};
       const int n0 = (DVC / 2) * hf;
-      auto fk = [&](int r, int x) { return bf2f(Ks[(r0 + r) * KE + x]); };
-      auto fd = [&](int x, int nn) { return dhs[x * Ly::BS + n0 + nn]; };
-      wgemm<NTV, true, false>(ca, 0, K, fk, fd);
-      auto fph = [&](int r, int i) { return tile64(PH, i, r0 + r); };
-      auto fpl = [&](int r, int i) { return tile64(PL, i, r0 + r); };
-      auto fo = [&](int i, int nn) { return bf2f(Ds[i * (Ly::DOROW / 2) + n0 + nn]); };
-      wgemm<NTV, true, true>(cp, r0, 64, fph, fo);
-      wgemm<NTV, true, true>(cp, r0, 64, fpl, fo);
+      // bf16 m16n8k16: raw k, P halves and do exact, dh' split hi + lo
+      auto fk = [&](int r, int x) {
+        const uint32_t w = *reinterpret_cast<const uint32_t *>(Ks + (r0 + r) * KE + x);
+        return make_float2(bf16lo_f(w), bf16hi_f(w));
+      };
+      auto fd = [&](int x, int nn) { return make_float2(dhs[x * Ly::BS + n0 + nn], dhs[(x + 1) * Ly::BS + n0 + nn]); };
+      wgemm_bf<NTV, true, false>(ca, 0, K, fk, fd);
+      auto fph = [&](int r, int i) { return make_float2(tile64(PH, i, r0 + r), tile64(PH, i + 1, r0 + r)); };
+      auto fpl = [&](int r, int i) { return make_float2(tile64(PL, i, r0 + r), tile64(PL, i + 1, r0 + r)); };
+      auto fo = [&](int i, int nn) {
+        return make_float2(bf2f(Ds[i * (Ly::DOROW / 2) + n0 + nn]), bf2f(Ds[(i + 1) * (Ly::DOROW / 2) + n0 + nn]));
+      };
+      wgemm_bf<NTV, true, true>(cp, r0, 64, fph, fo);
+      wgemm_bf<NTV, true, true>(cp, r0, 64, fpl, fo);
       const int g = (tid & 31) >> 2, t = tid & 3;
 #pragma unroll
       for (int nt = 0; nt < NTV; ++nt)
@@ -373,12 +379,15 @@ __global__ void __launch_bounds__(BT, 1) chunk_dh_kernel(
     {
       const float dL = sc[RS_DL];
       float t1[NTD][4] = {}, t2[NTD][4] = {};  // separate accumulators: independent mma chains
-      auto fq = [&](int r, int i) { return bf2f(Qs[i * KE + dm0 + r]); };
-      auto fo = [&](int i, int cc) { return scale * sc[RS_OG + i] * bf2f(Ds[i * (Ly::DOROW / 2) + dc0 + cc]); };
-      wgemm<NTD, true, false>(t1, 0, 64, fq, fo);
-      auto fw = [&](int r, int j) { return rec_w(Wt, j, dm0 + r); };
-      auto fv = [&](int j, int cc) { return dvn[j * Ly::BS + dc0 + cc]; };
-      wgemm<NTD, true, false>(t2, 0, 64, fw, fv);
+      auto fq = [&](int r, int i) { return make_float2(bf2f(Qs[i * KE + dm0 + r]), bf2f(Qs[(i + 1) * KE + dm0 + r])); };
+      auto fo = [&](int i, int cc) {
+        return make_float2(scale * sc[RS_OG + i] * bf2f(Ds[i * (Ly::DOROW / 2) + dc0 + cc]),
+                           scale * sc[RS_OG + i + 1] * bf2f(Ds[(i + 1) * (Ly::DOROW / 2) + dc0 + cc]));
+      };
+      wgemm_bf<NTD, true, false>(t1, 0, 64, fq, fo);
+      auto fw = [&](int r, int j) { return make_float2(rec_w(Wt, j, dm0 + r), rec_w(Wt, j + 1, dm0 + r)); };
+      auto fv = [&](int j, int cc) { return make_float2(dvn[j * Ly::BS + dc0 + cc], dvn[(j + 1) * Ly::BS + dc0 + cc]); };
+      wgemm_bf<NTD, true, false>(t2, 0, 64, fw, fv);
 #pragma unroll
       for (int nt = 0; nt < NTD; ++nt)
 #pragma unroll
