@@ -21,8 +21,8 @@
 //
 // The forward is re-run first (prep + walk kernels of gdn_chunk.cu) with the
 // walk saving the state entering every chunk; the dh walk saves dh' of every
-// chunk (fp32, CUDA cores).  The per-chunk gradients run their products on the
-// tensor cores (mma.sync tf32, operands split hi + lo for fp32 accuracy).
+// chunk.  Both backward kernels run their products on the tensor cores
+// (warp-level mma.sync, computed operands split hi + lo; see the helpers).
 #include <math.h>
 #include <string.h>
 
@@ -58,10 +58,11 @@ __device__ __forceinline__ float tile64(const unsigned char *t, int i, int j) {
 }
 
 // ------------------------------------------------------------- mma helpers
-// Warp-level mma.sync m16n8k8 in tf32 with fp32 accumulation.  A computed fp32
-// operand is split into tf32 hi + lo parts and the product takes hi*hi + hi*lo
-// + lo*hi, which keeps fp32-level accuracy; an operand holding raw bf16 values
-// is exact in tf32 and has no low part.
+// Warp-level mma.sync with fp32 accumulation.  A computed fp32 operand is split
+// into hi + lo parts and a product takes hi*hi + hi*lo + lo*hi; an operand
+// holding raw bf16 values is exact and has no low part.  wgemm_bf (bf16
+// m16n8k16, relative error near 2^-17) carries the large products, wgemm_tf32
+// (tf32 m16n8k8, fp32-level accuracy) the small blocks of the inverse T.
 __device__ __forceinline__ uint32_t tf32_rna(float x) {
   uint32_t r;
   asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
@@ -76,49 +77,12 @@ __device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], 
 
 // c (16 x 8 NT) += A (16 x [k0, k1)) B ([k0, k1) x 8 NT) for one warp, with
 // fa(r, k) = A[r][k] (r < 16) and fb(k, n) = B[k][n]; k0, k1 multiples of 8.
-// AX / BX: that operand is exact in tf32.
+// AX / BX: that operand is exact in tf32.  Software pipelined: the operands of
+// step k + 8 are read while step k runs.
 template <int NT, bool AX, bool BX, class FA, class FB>
-__device__ __forceinline__ void wgemm(float (&c)[NT][4], int k0, int k1, FA fa, FB fb) {
-  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-#pragma unroll 2
-  for (int k = k0; k < k1; k += 8) {
-    const float av[4] = {fa(g, k + t), fa(g + 8, k + t), fa(g, k + t + 4), fa(g + 8, k + t + 4)};
-    uint32_t ah[4], al[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      ah[e] = AX ? __float_as_uint(av[e]) : tf32_rna(av[e]);
-      al[e] = AX ? 0u : tf32_rna(av[e] - __uint_as_float(ah[e]));
-    }
-    uint32_t bh[NT][2], bl[NT][2];
-#pragma unroll
-    for (int n = 0; n < NT; ++n) {
-      const float b0 = fb(k + t, 8 * n + g), b1 = fb(k + t + 4, 8 * n + g);
-      bh[n][0] = BX ? __float_as_uint(b0) : tf32_rna(b0);
-      bh[n][1] = BX ? __float_as_uint(b1) : tf32_rna(b1);
-      bl[n][0] = BX ? 0u : tf32_rna(b0 - __uint_as_float(bh[n][0]));
-      bl[n][1] = BX ? 0u : tf32_rna(b1 - __uint_as_float(bh[n][1]));
-    }
-    // passes outermost, so that consecutive products go to different accumulators
-#pragma unroll
-    for (int n = 0; n < NT; ++n) mma_tf32(c[n], ah, bh[n][0], bh[n][1]);
-    if (!BX) {
-#pragma unroll
-      for (int n = 0; n < NT; ++n) mma_tf32(c[n], ah, bl[n][0], bl[n][1]);
-    }
-    if (!AX) {
-#pragma unroll
-      for (int n = 0; n < NT; ++n) mma_tf32(c[n], al, bh[n][0], bh[n][1]);
-    }
-  }
-}
-// The same product, software pipelined (the operands of step k + 8 are read
-// while step k runs): faster where several warps share a scheduler's latency
-// budget with long reductions (the per-chunk gradients), slower in the dh walk.
-template <int NT, bool AX, bool BX, class FA, class FB>
-__device__ __forceinline__ void wgemm_pipe(float (&c)[NT][4], int k0, int k1, FA fa, FB fb) {
+__device__ __forceinline__ void wgemm_tf32(float (&c)[NT][4], int k0, int k1, FA fa, FB fb) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   if (k0 >= k1) return;
-  // Software pipelined: the operands of step k + 8 are read while step k runs.
   float av[4], bv[NT][2];
   auto fetch = [&](int k) {
     av[0] = fa(g, k + t);
@@ -183,7 +147,8 @@ constexpr int SS = 36;  // fp32 row stride of a 32-column slice
 // per instruction): a computed operand is split into bf16 hi + lo (about 16
 // bits kept; hi*hi + hi*lo + lo*hi leaves a relative error near 2^-17), an
 // operand of raw bf16 values has no low part.  fa2(r, k) and fb2(k, n) return
-// the pairs (A[r][k], A[r][k + 1]) and (B[k][n], B[k + 1][n]).
+// the pairs (A[r][k], A[r][k + 1]) and (B[k][n], B[k + 1][n]); k0, k1 are
+// multiples of 16.
 __device__ __forceinline__ void split_bf16(float2 v, uint32_t &hi, uint32_t &lo) {
   hi = pack_bf16(v.x, v.y);
   lo = pack_bf16(v.x - bf16lo_f(hi), v.y - bf16hi_f(hi));
@@ -611,7 +576,7 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
       float cs[2][4] = {};
       auto fa = [&](int r, int m) { return Tm[(16 * bi + r) * MS + m]; };
       auto fb = [&](int m, int n) { return Tm[m * MS + 16 * warp + n]; };
-      wgemm_pipe<2, false, false>(cs, 16 * warp, 16 * bi, fa, fb);
+      wgemm_tf32<2, false, false>(cs, 16 * warp, 16 * bi, fa, fb);
       cvisit(cs, [&](int, int r, int n, float x) { Xs[r * 17 + n] = x; });
     }
     __syncthreads();
@@ -619,7 +584,7 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
       float ct[2][4] = {};
       auto fa = [&](int r, int m) { return Tm[(16 * bi + r) * MS + 16 * bi + m]; };
       auto fb = [&](int m, int n) { return Xs[m * 17 + n]; };
-      wgemm_pipe<2, false, false>(ct, 0, 16, fa, fb);
+      wgemm_tf32<2, false, false>(ct, 0, 16, fa, fb);
       cvisit(ct, [&](int, int r, int n, float x) { Tm[(16 * bi + r) * MS + 16 * warp + n] = -x; });
     }
     __syncthreads();
