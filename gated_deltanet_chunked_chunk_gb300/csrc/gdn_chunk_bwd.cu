@@ -214,12 +214,13 @@ struct DhLay {
   static constexpr int OFF_REC = OFF_Q + 64 * KROW;   // record bytes W | PH | PL (contiguous in the record)
   static constexpr int REC_BYTES = Rec<K>::TS;        // W + PH + PL
   static constexpr int OFF_SC = OFF_REC + REC_BYTES;  // record scalars (1 KB)
-  static constexpr int DOROW = DVC * 2 + 32;          // padded bf16 row of the do slice (bytes)
+  static constexpr int DOROW = DVC * 2 + 16;          // padded bf16 row of the do slice (bytes)
   static constexpr int OFF_DO = OFF_SC + 1024;        // do slice [64][DOROW bytes]
   static constexpr int STAGE = OFF_DO + 64 * DOROW;
-  // dh' and dv_new are read as B operands (row k + t, column g of a fragment):
-  // a row stride of 8 (mod 32) words keeps those reads free of bank conflicts.
-  static constexpr int BS = DVC + 8;
+  // dh', dv_new and do are read as bf16 B operands (rows k + 2t and k + 2t + 1,
+  // column g of a fragment): a row stride of 4 (mod 16) words keeps those reads
+  // free of bank conflicts (DOROW = 144 bytes = 36 words as well).
+  static constexpr int BS = DVC + 4;
   static constexpr int OFF_DHS = 2 * STAGE;           // dh' [K][BS] fp32
   static constexpr int OFF_DVN = OFF_DHS + K * BS * 4;  // dv_new [64][BS] fp32
   static constexpr int BYTES = OFF_DVN + 64 * BS * 4;
