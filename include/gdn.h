@@ -84,7 +84,9 @@ int gdn_gating(const float *A_log, const uint16_t *a, const uint16_t *b,
 
 /*
  * gdn_chunk_fwd_workspace_size -- bytes of device workspace gdn_chunk_fwd
- * needs for these sizes (0 means none; pass workspace = NULL then).
+ * needs for these sizes (0 means none; pass workspace = NULL then): one
+ * record per (chunk slot, value head), and with cu_seqlens (varlen != 0) a
+ * table of N + 1 chunk starts that the call fills first.
  */
 size_t gdn_chunk_fwd_workspace_size(int B, int T, int H, int HV, int K, int V,
                                     int N, int varlen);
@@ -188,7 +190,8 @@ int gdn_recurrent_decode(const uint16_t *q, const uint16_t *k,
 
 /*
  * gdn_chunk_bwd_workspace_size -- bytes of device workspace gdn_chunk_bwd
- * needs (the forward's records plus two fp32 states per chunk and value head).
+ * needs (the forward's workspace -- records, and the chunk-start table for
+ * cu_seqlens input -- plus two fp32 states per chunk and value head).
  */
 size_t gdn_chunk_bwd_workspace_size(int B, int T, int H, int HV, int K, int V,
                                     int N, int varlen);
@@ -207,8 +210,12 @@ size_t gdn_chunk_bwd_workspace_size(int B, int T, int H, int HV, int K, int V,
  * use_qk_l2norm); do: bf16 [B, T, HV, V]; dht: fp32 [N, HV, K, V] or NULL
  * (zero).  The forward is recomputed inside (the call saves the state
  * entering every chunk in the workspace), then the state gradients run last
- * chunk first, then the per-chunk gradients in parallel: four launches plus
- * two memsets of dq, dk on `stream`.  Errors as gdn_chunk_fwd; the workspace
+ * chunk first, then the per-chunk gradients in parallel: four launches (five
+ * with cu_seqlens) plus two memsets of dq, dk on `stream`.  Products run on the
+ * tensor cores with computed operands split into bf16 hi + lo parts (relative
+ * error near 2^-17 per product, fp32 accumulation); dq, dk (over the value
+ * heads of a group) and parts of dg are summed with atomic adds, so two runs
+ * agree to rounding, not bit for bit.  Errors as gdn_chunk_fwd; the workspace
  * must hold gdn_chunk_bwd_workspace_size() bytes.
  */
 int gdn_chunk_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
