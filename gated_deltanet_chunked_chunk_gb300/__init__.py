@@ -560,6 +560,13 @@ def gdn_chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
     B, T, H, K = q.shape
     HV, V = v.shape[2], v.shape[3]
     N = (cu_seqlens.shape[0] - 1) if cu_seqlens is not None else B
+    if tuple(k.shape) != (B, T, H, K) or tuple(v.shape[:2]) != (B, T) or tuple(do.shape) != (B, T, HV, V):
+        raise ValueError("gdn_chunk_bwd: q, k [B,T,H,K], v and do [B,T,HV,V] must agree")
+    if tuple(g.shape) != (B, T, HV) or tuple(beta.shape) != (B, T, HV):
+        raise ValueError(f"gdn_chunk_bwd: g and beta must be [B,T,HV] = {(B, T, HV)}")
+    for t, n in ((initial_state, "initial_state"), (dht, "dht")):
+        if t is not None and tuple(t.shape) != (N, HV, K, V):
+            raise ValueError(f"gdn_chunk_bwd: {n} must be [N,HV,K,V] = {(N, HV, K, V)}")
     dq = torch.empty(B, T, H, K, dtype=torch.float32, device=dev)
     dk = torch.empty_like(dq)
     dv = torch.empty(B, T, HV, V, dtype=torch.float32, device=dev)

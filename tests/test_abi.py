@@ -192,3 +192,16 @@ def test_decode_variants_host_validation(lib):
     assert mtp(ld=0) == gdn.GDN_EINVAL
     assert mtp(pool=NULL) == gdn.GDN_EINVAL
     assert mtp(N=70000) == gdn.GDN_EUNSUPPORTED
+
+
+def test_backward_binding_checks_shapes_before_calling():
+    import torch
+    q = torch.zeros(1, 8, 2, 64, dtype=torch.bfloat16)
+    v = torch.zeros(1, 8, 4, 64, dtype=torch.bfloat16)
+    g = torch.zeros(1, 8, 4)
+    with pytest.raises(ValueError):   # do has the wrong head count
+        gdn.gdn_chunk_bwd(q, q, v, g, g, torch.zeros(1, 8, 2, 64, dtype=torch.bfloat16))
+    with pytest.raises(ValueError):   # g, beta must be [B,T,HV]
+        gdn.gdn_chunk_bwd(q, q, v, g[..., :2], g[..., :2], v)
+    with pytest.raises(ValueError):   # dht must be [N,HV,K,V]
+        gdn.gdn_chunk_bwd(q, q, v, g, g, v, dht=torch.zeros(1, 4, 64, 32))
