@@ -194,6 +194,43 @@ __device__ __forceinline__ void wgemm_bf(float (&c)[NT][4], int k0, int k1, FA2 
     }
   }
 }
+// wgemm_bf with a B operand stored already split: fbp(k, n) returns the bf16
+// pairs {hi (B[k][n], B[k + 1][n]), lo (B[k][n], B[k + 1][n])}.
+template <int NT, bool AX, class FA2, class FBP>
+__device__ __forceinline__ void wgemm_bf_pb(float (&c)[NT][4], int k0, int k1, FA2 fa2, FBP fbp) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll 2
+  for (int k = k0; k < k1; k += 16) {
+    const float2 av[4] = {fa2(g, k + 2 * t), fa2(g + 8, k + 2 * t), fa2(g, k + 2 * t + 8), fa2(g + 8, k + 2 * t + 8)};
+    uint32_t ah[4], al[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (AX) {
+        ah[e] = pack_bf16(av[e].x, av[e].y);
+        al[e] = 0u;
+      } else {
+        split_bf16(av[e], ah[e], al[e]);
+      }
+    }
+    uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      const uint2 b0 = fbp(k + 2 * t, 8 * n + g), b1 = fbp(k + 2 * t + 8, 8 * n + g);
+      bh[n][0] = b0.x;
+      bl[n][0] = b0.y;
+      bh[n][1] = b1.x;
+      bl[n][1] = b1.y;
+    }
+#pragma unroll
+    for (int n = 0; n < NT; ++n) mma_bf16(c[n], ah, bh[n][0], bh[n][1]);
+#pragma unroll
+    for (int n = 0; n < NT; ++n) mma_bf16(c[n], ah, bl[n][0], bl[n][1]);
+    if (!AX) {
+#pragma unroll
+      for (int n = 0; n < NT; ++n) mma_bf16(c[n], al, bh[n][0], bh[n][1]);
+    }
+  }
+}
 // ------------------------------------------------------------------ dh walk
 // One CTA per (64-column slice of V, value head, sequence), last chunk first
 // (64 columns: at V = 128 the grid of HV x N x 2 CTAs fits one wave of SMs for
@@ -376,16 +413,17 @@ template <int K>
 struct GradLay {
   static constexpr int BROW = K + 8;                     // bf16 row stride of raw q, k
   static constexpr int M64 = 64 * MS * 4;
-  static constexpr int HS = K * SS * 4, RS = 64 * SS * 4;
+  static constexpr int HSB = VS + 8;                     // bf16 row stride of a split h / dh' slice
+  static constexpr int HS = K * HSB * 2, RS = 64 * SS * 4;
   static constexpr int OFF_QB = 0;                       // raw q [64][BROW] bf16
   static constexpr int OFF_KB = OFF_QB + 64 * BROW * 2;  // raw k
   static constexpr int OFF_T = OFF_KB + 64 * BROW * 2;   // A, then T = (I + A)^-1
   static constexpr int OFF_P = OFF_T + M64;              // P_ij = e^{gamma_i-gamma_j} q^_i.k^_j (j <= i)
   static constexpr int OFF_EK = OFF_P + M64;             // e^{gamma_i-gamma_j} k^_i.k^_j (j < i)
   static constexpr int OFF_SL = OFF_EK + M64;            // V-slice buffers, reused afterwards
-  static constexpr int OFF_H = OFF_SL;                   // h slice [K][SS]
-  static constexpr int OFF_DH = OFF_H + HS;              // dh' slice
-  static constexpr int OFF_V = OFF_DH + HS;              // v slice [64][SS]
+  static constexpr int OFF_H = OFF_SL;                   // h slice [K][HSB] as bf16 hi, then lo
+  static constexpr int OFF_DH = OFF_H + 2 * HS;          // dh' slice, hi then lo
+  static constexpr int OFF_V = OFF_DH + 2 * HS;          // v slice [64][SS]
   static constexpr int OFF_DO = OFF_V + RS;              // do slice
   static constexpr int OFF_KH = OFF_DO + RS;             // k^ h
   static constexpr int OFF_KDH = OFF_KH + RS;            // k^ dh'
@@ -425,8 +463,16 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
   float *Tm = reinterpret_cast<float *>(smem + Ly::OFF_T);
   float *Pm = reinterpret_cast<float *>(smem + Ly::OFF_P);
   float *EK = reinterpret_cast<float *>(smem + Ly::OFF_EK);
-  float *hS = reinterpret_cast<float *>(smem + Ly::OFF_H);
-  float *dhS = reinterpret_cast<float *>(smem + Ly::OFF_DH);
+  // h, dh' of the current slice, split once into bf16 hi + lo when loaded
+  uint16_t *Hhi = reinterpret_cast<uint16_t *>(smem + Ly::OFF_H);
+  uint16_t *Hlo = reinterpret_cast<uint16_t *>(smem + Ly::OFF_H + Ly::HS);
+  uint16_t *DHhi = reinterpret_cast<uint16_t *>(smem + Ly::OFF_DH);
+  uint16_t *DHlo = reinterpret_cast<uint16_t *>(smem + Ly::OFF_DH + Ly::HS);
+  constexpr int HSB = Ly::HSB;
+  auto pair16 = [](const uint16_t *p, int stride) {  // (p[0], p[stride]) as a bf16 pair
+    return static_cast<uint32_t>(p[0]) | (static_cast<uint32_t>(p[stride]) << 16);
+  };
+  auto word16 = [](const uint16_t *p) { return *reinterpret_cast<const uint32_t *>(p); };
   float *vS = reinterpret_cast<float *>(smem + Ly::OFF_V);
   float *doS = reinterpret_cast<float *>(smem + Ly::OFF_DO);
   float *KhS = reinterpret_cast<float *>(smem + Ly::OFF_KH);
@@ -600,10 +646,17 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
     if (v0 + VS < V) prefetch_slice(v0 + VS);
     for (int e = tid; e < K * (VS / 4); e += BT) {
       const int x = e / (VS / 4), c4 = e % (VS / 4);
-      *reinterpret_cast<float4 *>(hS + x * SS + 4 * c4) =
-          *reinterpret_cast<const float4 *>(Hs + hb + (int64_t)x * V + 4 * c4);
-      *reinterpret_cast<float4 *>(dhS + x * SS + 4 * c4) =
-          *reinterpret_cast<const float4 *>(DH + hb + (int64_t)x * V + 4 * c4);
+      const float4 hv4 = *reinterpret_cast<const float4 *>(Hs + hb + (int64_t)x * V + 4 * c4);
+      const float4 dv4 = *reinterpret_cast<const float4 *>(DH + hb + (int64_t)x * V + 4 * c4);
+      uint32_t hi[2], lo[2];
+      split_bf16(make_float2(hv4.x, hv4.y), hi[0], lo[0]);
+      split_bf16(make_float2(hv4.z, hv4.w), hi[1], lo[1]);
+      *reinterpret_cast<uint2 *>(Hhi + x * HSB + 4 * c4) = make_uint2(hi[0], hi[1]);
+      *reinterpret_cast<uint2 *>(Hlo + x * HSB + 4 * c4) = make_uint2(lo[0], lo[1]);
+      split_bf16(make_float2(dv4.x, dv4.y), hi[0], lo[0]);
+      split_bf16(make_float2(dv4.z, dv4.w), hi[1], lo[1]);
+      *reinterpret_cast<uint2 *>(DHhi + x * HSB + 4 * c4) = make_uint2(hi[0], hi[1]);
+      *reinterpret_cast<uint2 *>(DHlo + x * HSB + 4 * c4) = make_uint2(lo[0], lo[1]);
     }
     for (int e = tid; e < 64 * (VS / 8); e += BT) {
       const int i = e / (VS / 8), c8 = e % (VS / 8);
@@ -647,8 +700,10 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
               const int x = kk + 2 * ft + 8 * u, c = n0 + 8 * n + fr;
-              split_bf16(make_float2(hS[x * SS + c], hS[(x + 1) * SS + c]), hh[n][u], hl[n][u]);
-              split_bf16(make_float2(dhS[x * SS + c], dhS[(x + 1) * SS + c]), dh_[n][u], dl[n][u]);
+              hh[n][u] = pair16(Hhi + x * HSB + c, HSB);
+              hl[n][u] = pair16(Hlo + x * HSB + c, HSB);
+              dh_[n][u] = pair16(DHhi + x * HSB + c, HSB);
+              dl[n][u] = pair16(DHlo + x * HSB + c, HSB);
             }
 #pragma unroll
           for (int n = 0; n < 2; ++n) {
@@ -725,7 +780,10 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
       s += __shfl_xor_sync(0xffffffffu, s, 1);
       if ((tt & 1) == 0) SLv[i] += s;
       float hh = 0.f;
-      for (int e = tt; e < K * VS; e += 128) hh = fmaf(dhS[(e / VS) * SS + e % VS], hS[(e / VS) * SS + e % VS], hh);
+      for (int e = tt; e < K * VS; e += 128) {
+        const int o16 = (e / VS) * HSB + e % VS;
+        hh = fmaf(bf2f(DHhi[o16]) + bf2f(DHlo[o16]), bf2f(Hhi[o16]) + bf2f(Hlo[o16]), hh);
+      }
       hh = warp_sum(hh);
       if (lane == 0) atomicAdd(&misc[0], hh);
     }
@@ -751,11 +809,17 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
         const float2 x = ld2(vnS + i * SS + u - VS);
         return make_float2(sv[i] * x.x, sv[i] * x.y);
       };
-      auto fb3 = [&](int u, int n) { return u < VS ? ld2(hS + (x0 + n) * SS + u) : ld2(dhS + (x0 + n) * SS + u - VS); };
-      wgemm_bf<NH, false, false>(accK, 0, 2 * VS, fa3, fb3);
+      auto fb3 = [&](int u, int n) {
+        const int o16 = (x0 + n) * HSB + (u < VS ? u : u - VS);
+        return u < VS ? make_uint2(word16(Hhi + o16), word16(Hlo + o16)) : make_uint2(word16(DHhi + o16), word16(DHlo + o16));
+      };
+      wgemm_bf_pb<NH, false>(accK, 0, 2 * VS, fa3, fb3);
       auto fa4 = [&](int r, int u) { return ld2(doS + (r0 + r) * SS + u); };
-      auto fb4 = [&](int u, int n) { return ld2(hS + (x0 + n) * SS + u); };
-      wgemm_bf<NH, true, false>(accQ, 0, VS, fa4, fb4);
+      auto fb4 = [&](int u, int n) {
+        const int o16 = (x0 + n) * HSB + u;
+        return make_uint2(word16(Hhi + o16), word16(Hlo + o16));
+      };
+      wgemm_bf_pb<NH, true>(accQ, 0, VS, fa4, fb4);
     }
     __syncthreads();
   }
