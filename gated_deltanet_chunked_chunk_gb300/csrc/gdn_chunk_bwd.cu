@@ -58,72 +58,10 @@ __device__ __forceinline__ float tile64(const unsigned char *t, int i, int j) {
 }
 
 // ------------------------------------------------------------- mma helpers
-// Warp-level mma.sync with fp32 accumulation.  A computed fp32 operand is split
-// into hi + lo parts and a product takes hi*hi + hi*lo + lo*hi; an operand
-// holding raw bf16 values is exact and has no low part.  wgemm_bf (bf16
-// m16n8k16, relative error near 2^-17) carries the large products, wgemm_tf32
-// (tf32 m16n8k8, fp32-level accuracy) the small blocks of the inverse T.
-__device__ __forceinline__ uint32_t tf32_rna(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
-}
-__device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// c (16 x 8 NT) += A (16 x [k0, k1)) B ([k0, k1) x 8 NT) for one warp, with
-// fa(r, k) = A[r][k] (r < 16) and fb(k, n) = B[k][n]; k0, k1 multiples of 8.
-// AX / BX: that operand is exact in tf32.  Software pipelined: the operands of
-// step k + 8 are read while step k runs.
-template <int NT, bool AX, bool BX, class FA, class FB>
-__device__ __forceinline__ void wgemm_tf32(float (&c)[NT][4], int k0, int k1, FA fa, FB fb) {
-  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  if (k0 >= k1) return;
-  float av[4], bv[NT][2];
-  auto fetch = [&](int k) {
-    av[0] = fa(g, k + t);
-    av[1] = fa(g + 8, k + t);
-    av[2] = fa(g, k + t + 4);
-    av[3] = fa(g + 8, k + t + 4);
-#pragma unroll
-    for (int n = 0; n < NT; ++n) {
-      bv[n][0] = fb(k + t, 8 * n + g);
-      bv[n][1] = fb(k + t + 4, 8 * n + g);
-    }
-  };
-  fetch(k0);
-  for (int k = k0; k < k1; k += 8) {
-    uint32_t ah[4], al[4], bh[NT][2], bl[NT][2];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      ah[e] = AX ? __float_as_uint(av[e]) : tf32_rna(av[e]);
-      al[e] = AX ? 0u : tf32_rna(av[e] - __uint_as_float(ah[e]));
-    }
-#pragma unroll
-    for (int n = 0; n < NT; ++n)
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        bh[n][u] = BX ? __float_as_uint(bv[n][u]) : tf32_rna(bv[n][u]);
-        bl[n][u] = BX ? 0u : tf32_rna(bv[n][u] - __uint_as_float(bh[n][u]));
-      }
-    if (k + 8 < k1) fetch(k + 8);
-    // passes outermost, so that consecutive products go to different accumulators
-#pragma unroll
-    for (int n = 0; n < NT; ++n) mma_tf32(c[n], ah, bh[n][0], bh[n][1]);
-    if (!BX) {
-#pragma unroll
-      for (int n = 0; n < NT; ++n) mma_tf32(c[n], ah, bl[n][0], bl[n][1]);
-    }
-    if (!AX) {
-#pragma unroll
-      for (int n = 0; n < NT; ++n) mma_tf32(c[n], al, bh[n][0], bh[n][1]);
-    }
-  }
-}
+// Warp-level mma.sync m16n8k16 in bf16 with fp32 accumulation (wgemm_bf,
+// wgemm_bf_pb below).  A computed fp32 operand is split into bf16 hi + lo parts
+// and a product takes hi*hi + hi*lo + lo*hi (relative error near 2^-17); an
+// operand holding raw bf16 values is exact and has no low part.
 // f(rh, r, n, x) for every accumulator element: row r = g + 8 rh, column n.
 template <int NT, class F>
 __device__ __forceinline__ void cvisit(float (&c)[NT][4], F f) {
@@ -621,17 +559,17 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
     float *Xs = DT + warp * 16 * 17;  // the slice area is free here
     if (warp < bi) {
       float cs[2][4] = {};
-      auto fa = [&](int r, int m) { return Tm[(16 * bi + r) * MS + m]; };
-      auto fb = [&](int m, int n) { return Tm[m * MS + 16 * warp + n]; };
-      wgemm_tf32<2, false, false>(cs, 16 * warp, 16 * bi, fa, fb);
+      auto fa = [&](int r, int m) { return ld2(Tm + (16 * bi + r) * MS + m); };
+      auto fb = [&](int m, int n) { return make_float2(Tm[m * MS + 16 * warp + n], Tm[(m + 1) * MS + 16 * warp + n]); };
+      wgemm_bf<2, false, false>(cs, 16 * warp, 16 * bi, fa, fb);
       cvisit(cs, [&](int, int r, int n, float x) { Xs[r * 17 + n] = x; });
     }
     __syncthreads();
     if (warp < bi) {
       float ct[2][4] = {};
-      auto fa = [&](int r, int m) { return Tm[(16 * bi + r) * MS + 16 * bi + m]; };
-      auto fb = [&](int m, int n) { return Xs[m * 17 + n]; };
-      wgemm_tf32<2, false, false>(ct, 0, 16, fa, fb);
+      auto fa = [&](int r, int m) { return ld2(Tm + (16 * bi + r) * MS + 16 * bi + m); };
+      auto fb = [&](int m, int n) { return make_float2(Xs[m * 17 + n], Xs[(m + 1) * 17 + n]); };
+      wgemm_bf<2, false, false>(ct, 0, 16, fa, fb);
       cvisit(ct, [&](int, int r, int n, float x) { Tm[(16 * bi + r) * MS + 16 * warp + n] = -x; });
     }
     __syncthreads();
