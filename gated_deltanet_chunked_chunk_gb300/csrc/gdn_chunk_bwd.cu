@@ -81,12 +81,12 @@ constexpr int VS = 32;  // V columns per slice
 constexpr int MS = 68;  // fp32 row stride of a 64 x 64 tile
 constexpr int SS = 36;  // fp32 row stride of a 32-column slice
 
-// The same product on mma.sync m16n8k16 in bf16 (twice the k of a tf32 step
-// per instruction): a computed operand is split into bf16 hi + lo (about 16
-// bits kept; hi*hi + hi*lo + lo*hi leaves a relative error near 2^-17), an
-// operand of raw bf16 values has no low part.  fa2(r, k) and fb2(k, n) return
-// the pairs (A[r][k], A[r][k + 1]) and (B[k][n], B[k + 1][n]); k0, k1 are
-// multiples of 16.
+// c (16 x 8 NT) += A (16 x [k0, k1)) B ([k0, k1) x 8 NT) for one warp on
+// mma.sync m16n8k16 in bf16: a computed operand is split into bf16 hi + lo
+// (about 16 bits kept; hi*hi + hi*lo + lo*hi leaves a relative error near
+// 2^-17), an operand of raw bf16 values has no low part (AX / BX).  fa2(r, k)
+// and fb2(k, n) return the pairs (A[r][k], A[r][k + 1]) and (B[k][n],
+// B[k + 1][n]); k0, k1 are multiples of 16.
 __device__ __forceinline__ void split_bf16(float2 v, uint32_t &hi, uint32_t &lo) {
   hi = pack_bf16(v.x, v.y);
   lo = pack_bf16(v.x - bf16lo_f(hi), v.y - bf16hi_f(hi));
@@ -176,8 +176,8 @@ __device__ __forceinline__ void wgemm_bf_pb(float (&c)[NT][4], int k0, int k1, F
 // dh (K x 64 fp32) lives in the mma accumulators of the eight warps (warp w:
 // rows of tile w % (K / 16), a share of the columns); per chunk K, Q, W, P,
 // the scalars and the do slice are staged in shared memory (cp.async, double
-// buffered).  Both products of a chunk run on mma.sync tf32: the raw bf16 k,
-// q, W, P hi / lo and do are exact in tf32, the computed dh' and dv_new are
+// buffered).  Both products of a chunk run on mma.sync m16n8k16 in bf16: the
+// raw k, q, W, P hi / lo and do are exact, the computed dh' and dv_new are
 // split hi + lo.
 constexpr int DVC = 64;  // V columns per dh-walk CTA
 
