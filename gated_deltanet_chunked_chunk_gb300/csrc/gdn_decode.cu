@@ -6,14 +6,18 @@
 // is skipped.  The LightLLM "gdn.py" decode path hands A_log, dt_bias and the
 // raw a, b to the same kernel, so the gates are computed in-kernel.
 //
-// Design: the op moves 2 x K x V x 4 bytes of state per (request, value head)
-// and does ~6 K V flops on it, so it is HBM-bound.  One 256-thread block owns
-// one (value head, request) state.  Lane l holds V/32 consecutive columns of
-// K/8 rows (warp w owns rows [w K/8, (w+1) K/8)), so every warp-wide load or
-// store is one contiguous 512-byte (V = 128) row segment, issued as 16-byte
-// streaming loads all at once before any arithmetic.  The two reductions over
-// K (S^T k and S^T q) go through shared memory across the 8 warps.  The
-// updated state is written back with streaming stores.
+// Design: the op moves 2 x K x V x sizeof(state) bytes per (request, value
+// head) and does ~6 K V flops on it, so it is HBM-bound.  One 256-thread block
+// owns one (value head, request) state; lane l works on V/32 consecutive
+// columns of K/8 rows (warp w owns rows [w K/8, (w+1) K/8)), so every warp
+// access is one contiguous row segment, and the two reductions over K
+// (S^T k and S^T q) go through shared memory across the 8 warps.  One token
+// per request (decode_staged_kernel): the state is staged in shared memory by
+// one bulk asynchronous copy and written back by one, so several blocks share
+// an SM and much of the pool is in flight.  Several tokens per request (the
+// MTP form, decode_kernel): the state stays in registers across the tokens,
+// loaded with 16-byte streaming loads all at once before any arithmetic and
+// stored with streaming stores after each token.
 #include "gdn_chunk_shared.cuh"
 #include "gdn_common.cuh"
 #include "gdn_sm103.cuh"
