@@ -28,6 +28,7 @@ using gdn::bulk_commit;
 using gdn::bulk_load;
 using gdn::bulk_store;
 using gdn::bulk_wait_all;
+using gdn::bulk_wait_read_all;
 using gdn::fence_proxy_async_smem;
 using gdn::mbar_arrive_expect_tx;
 using gdn::mbar_fence_init;
@@ -273,13 +274,21 @@ template <int N> struct SmemIO<uint16_t, N> {
 
 constexpr int kStagedThreads = kWarps * 32;  // the register kernel's row split and summation order
 
-template <int K, int V, typename ST>
-__global__ void __launch_bounds__(kStagedThreads) decode_staged_kernel(
+// Request n owns tokens [t0, t1) (t0 = n, t1 = n + 1 without cu); it starts
+// from pool[read_idx[n * ld + num_acc[n] - 1]] (column 0 without num_acc) and
+// the state after its i-th token goes to pool[write_idx[n * ld + i]] (-1: not
+// stored).  The staged state is updated in place token by token; each stored
+// state leaves with one bulk copy, and the next token overwrites the staged
+// state only after that copy has read it.  MT = false compiles the one-token
+// form (t1 = t0 + 1, ld = 1, the state written back to its own slot).
+template <int K, int V, typename ST, bool MT>
+__global__ void __launch_bounds__(kStagedThreads, 5) decode_staged_kernel(
     const uint16_t *__restrict__ q, const uint16_t *__restrict__ k, const uint16_t *__restrict__ v,
     const float *__restrict__ g_in, const float *__restrict__ beta_in, const float *__restrict__ A_log,
     const uint16_t *__restrict__ a_raw, const uint16_t *__restrict__ b_raw, const float *__restrict__ dt_bias,
-    float scale, int l2, ST *pool, int P, const int32_t *__restrict__ idx, int H, int HV,
-    uint16_t *__restrict__ o, int32_t *dev_status) {
+    float scale, int l2, ST *pool, int P, const int32_t *__restrict__ cu, int Ttot,
+    const int32_t *__restrict__ read_idx, const int32_t *__restrict__ write_idx, int ld,
+    const int32_t *__restrict__ num_acc, int H, int HV, uint16_t *__restrict__ o, int32_t *dev_status) {
   constexpr int NW = kStagedThreads / 32, VPL = V / 32, RPW = K / NW;
   constexpr uint32_t SBYTES = K * V * sizeof(ST);
   extern __shared__ __align__(128) unsigned char dsm[];
@@ -290,149 +299,185 @@ __global__ void __launch_bounds__(kStagedThreads) decode_staged_kernel(
   __shared__ __align__(8) uint64_t bar;
   const int hv = blockIdx.x, n = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int s = idx[n];
+  int t0 = n, t1 = n + 1;
+  int s = -1;
+  if constexpr (MT) {
+    if (cu) {
+      t0 = cu[n];
+      t1 = cu[n + 1];
+      if (t0 < 0 || t1 < t0 || t1 > Ttot || t1 - t0 > ld) {
+        if (tid == 0) gdn::set_status(dev_status, GDN_DEV_BAD_CU_SEQLENS);
+        return;
+      }
+    }
+    const int acc = num_acc ? num_acc[n] : 1;
+    if (acc >= 1 && acc <= ld) {
+      s = read_idx[(int64_t)n * ld + acc - 1];
+    } else if (tid == 0) {
+      gdn::set_status(dev_status, GDN_DEV_BAD_SLOT);
+    }
+  } else {
+    s = read_idx[n];
+  }
   if (s < 0 || s >= P) {
     if (s != -1 && tid == 0) gdn::set_status(dev_status, GDN_DEV_BAD_SLOT);
-    for (int j = tid; j < V; j += blockDim.x) o[((int64_t)n * HV + hv) * V + j] = 0;
+    for (int t = t0; t < t1; ++t)
+      for (int j = tid; j < V; j += blockDim.x) o[((int64_t)t * HV + hv) * V + j] = 0;
     return;
   }
+  if (MT && t1 == t0) return;
   const int h = hv / (HV / H);
-  ST *S = pool + ((int64_t)s * HV + hv) * (int64_t)K * V;
   const uint32_t b_ld = smem_u32(&bar), ss = smem_u32(Ss);
   if (tid == 0) {
     mbar_init(b_ld, 1);
     mbar_fence_init();
     mbar_arrive_expect_tx(b_ld, SBYTES);
-    bulk_load(ss, S, SBYTES, b_ld);
+    bulk_load(ss, pool + ((int64_t)s * HV + hv) * (int64_t)K * V, SBYTES, b_ld);
   }
   __syncthreads();  // the barrier is initialised before anyone polls it
-  // While the state lands: q, k and their norms, the gates, this lane's v.
-  float qx = 0.f, kx = 0.f;
-  if (tid < K) {
-    qx = gdn::bf2f(q[((int64_t)n * H + h) * K + tid]);
-    kx = gdn::bf2f(k[((int64_t)n * H + h) * K + tid]);
-  }
-  if (l2) {
-    const float qs = gdn::warp_sum(qx * qx), ks = gdn::warp_sum(kx * kx);
-    if (lane == 0 && w < K / 32) {
-      red[0][w] = qs;
-      red[1][w] = ks;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      float a0 = 0.f, b0 = 0.f;
-      for (int i = 0; i < K / 32; ++i) {
-        a0 += red[0][i];
-        b0 += red[1][i];
-      }
-      sh_norm[0] = rsqrtf(a0 + GDN_L2_EPS);
-      sh_norm[1] = rsqrtf(b0 + GDN_L2_EPS);
-    }
-    __syncthreads();
+  for (int t = t0; t < (MT ? t1 : t0 + 1); ++t) {
+    if (MT && t > t0) __syncthreads();  // the previous token's readers of qn, kn, red are done
+    // q, k and their norms, the gates, this lane's v (for the first token while the state lands)
+    float qx = 0.f, kx = 0.f;
     if (tid < K) {
-      qn[tid] = qx * sh_norm[0];
-      kn[tid] = kx * sh_norm[1];
+      qx = gdn::bf2f(q[((int64_t)t * H + h) * K + tid]);
+      kx = gdn::bf2f(k[((int64_t)t * H + h) * K + tid]);
     }
-  } else if (tid < K) {
-    qn[tid] = qx;
-    kn[tid] = kx;
-  }
-  const int64_t gi = (int64_t)n * HV + hv;
-  float gg, bb;
-  if (g_in) {
-    gg = g_in[gi];
-    bb = beta_in[gi];
-  } else {
-    gg = -expf(A_log[hv]) * gdn::softplus_f(gdn::bf2f(a_raw[gi]) + dt_bias[hv]);
-    bb = gdn::sigmoid_f(gdn::bf2f(b_raw[gi]));
-  }
-  const float decay = expf(gg);
-  float vv[VPL];
+    if (l2) {
+      const float qs = gdn::warp_sum(qx * qx), ks = gdn::warp_sum(kx * kx);
+      if (lane == 0 && w < K / 32) {
+        red[0][w] = qs;
+        red[1][w] = ks;
+      }
+      __syncthreads();
+      if (tid == 0) {
+        float a0 = 0.f, b0 = 0.f;
+        for (int i = 0; i < K / 32; ++i) {
+          a0 += red[0][i];
+          b0 += red[1][i];
+        }
+        sh_norm[0] = rsqrtf(a0 + GDN_L2_EPS);
+        sh_norm[1] = rsqrtf(b0 + GDN_L2_EPS);
+      }
+      __syncthreads();
+      if (tid < K) {
+        qn[tid] = qx * sh_norm[0];
+        kn[tid] = kx * sh_norm[1];
+      }
+    } else if (tid < K) {
+      qn[tid] = qx;
+      kn[tid] = kx;
+    }
+    const int64_t gi = (int64_t)t * HV + hv;
+    float gg, bb;
+    if (g_in) {
+      gg = g_in[gi];
+      bb = beta_in[gi];
+    } else {
+      gg = -expf(A_log[hv]) * gdn::softplus_f(gdn::bf2f(a_raw[gi]) + dt_bias[hv]);
+      bb = gdn::sigmoid_f(gdn::bf2f(b_raw[gi]));
+    }
+    const float decay = expf(gg);
+    float vv[VPL];
 #pragma unroll
-  for (int c = 0; c < VPL; ++c) vv[c] = gdn::bf2f(v[gi * V + lane * VPL + c]);
-  // Every thread sees the copy complete (bounded); on expiry the block waits
-  // once more for the copy to drain, records the error and leaves.
-  const bool landed = __syncthreads_and(mbar_wait_bounded(b_ld, 0, gdnc::kWaitLimit) ? 1 : 0) != 0;
-  if (!landed) {
+    for (int c = 0; c < VPL; ++c) vv[c] = gdn::bf2f(v[gi * V + lane * VPL + c]);
+    if (!MT || t == t0) {
+      // Every thread sees the copy complete (bounded); on expiry the block waits
+      // once more for the copy to drain, records the error and leaves.
+      const bool landed = __syncthreads_and(mbar_wait_bounded(b_ld, 0, gdnc::kWaitLimit) ? 1 : 0) != 0;
+      if (!landed) {
+        if (tid == 0) {
+          mbar_wait_bounded(b_ld, 0, gdnc::kWaitLimit);
+          gdn::set_status(dev_status, GDN_DEV_WAIT_TIMEOUT);
+        }
+        return;
+      }
+    } else {
+      __syncthreads();  // qn, kn visible
+    }
+    // r = S^T k over this warp's rows
+    float part[VPL], x[VPL];
+#pragma unroll
+    for (int c = 0; c < VPL; ++c) part[c] = 0.f;
+#pragma unroll 8
+    for (int i = 0; i < RPW; ++i) {
+      const int row = w * RPW + i;
+      SmemIO<ST, VPL>::load(Ss + row * V + lane * VPL, x);
+      const float kk = kn[row];
+#pragma unroll
+      for (int c = 0; c < VPL; ++c) part[c] = fmaf(x[c], kk, part[c]);
+    }
+#pragma unroll
+    for (int c = 0; c < VPL; ++c) red[w][lane * VPL + c] = part[c];
+    __syncthreads();
+    float delta[VPL];
+#pragma unroll
+    for (int c = 0; c < VPL; ++c) {
+      float rs = 0.f;
+#pragma unroll
+      for (int j = 0; j < NW; ++j) rs += red[j][lane * VPL + c];
+      delta[c] = bb * (vv[c] - decay * rs);
+    }
+    if (MT && t > t0 && tid == 0) bulk_wait_read_all();  // the previous token's stored state has been read
+    __syncthreads();  // red is reused below; the staged state may be overwritten
+    // S <- a S + k delta^T in place, o partial = S^T q
+#pragma unroll
+    for (int c = 0; c < VPL; ++c) part[c] = 0.f;
+#pragma unroll 8
+    for (int i = 0; i < RPW; ++i) {
+      const int row = w * RPW + i;
+      SmemIO<ST, VPL>::load(Ss + row * V + lane * VPL, x);
+      const float kk = kn[row], qq = qn[row];
+#pragma unroll
+      for (int c = 0; c < VPL; ++c) {
+        x[c] = fmaf(decay, x[c], kk * delta[c]);
+        part[c] = fmaf(x[c], qq, part[c]);
+      }
+      SmemIO<ST, VPL>::store(Ss + row * V + lane * VPL, x);
+    }
+#pragma unroll
+    for (int c = 0; c < VPL; ++c) red[w][lane * VPL + c] = part[c];
+    fence_proxy_async_smem();  // the new state, visible to the bulk copy
+    __syncthreads();
     if (tid == 0) {
-      mbar_wait_bounded(b_ld, 0, gdnc::kWaitLimit);
-      gdn::set_status(dev_status, GDN_DEV_WAIT_TIMEOUT);
+      const int ws = MT ? write_idx[(int64_t)n * ld + (t - t0)] : s;
+      if (ws >= 0 && ws < P) {
+        if (MT) bulk_wait_all();  // stores land in token order (a slot written twice keeps the later state)
+        bulk_store(pool + ((int64_t)ws * HV + hv) * (int64_t)K * V, ss, SBYTES);
+        bulk_commit();
+      } else if (ws != -1) {
+        gdn::set_status(dev_status, GDN_DEV_BAD_SLOT);
+      }
     }
-    return;
-  }
-  // r = S^T k over this warp's rows
-  float part[VPL], x[VPL];
+    if (w == NW - 1) {
+      uint16_t *orow = o + gi * V;
 #pragma unroll
-  for (int c = 0; c < VPL; ++c) part[c] = 0.f;
-#pragma unroll 8
-  for (int i = 0; i < RPW; ++i) {
-    const int row = w * RPW + i;
-    SmemIO<ST, VPL>::load(Ss + row * V + lane * VPL, x);
-    const float kk = kn[row];
+      for (int c = 0; c < VPL; ++c) {
+        float os = 0.f;
 #pragma unroll
-    for (int c = 0; c < VPL; ++c) part[c] = fmaf(x[c], kk, part[c]);
-  }
-#pragma unroll
-  for (int c = 0; c < VPL; ++c) red[w][lane * VPL + c] = part[c];
-  __syncthreads();
-  float delta[VPL];
-#pragma unroll
-  for (int c = 0; c < VPL; ++c) {
-    float rs = 0.f;
-#pragma unroll
-    for (int j = 0; j < NW; ++j) rs += red[j][lane * VPL + c];
-    delta[c] = bb * (vv[c] - decay * rs);
-  }
-  __syncthreads();  // red is reused below
-  // S <- a S + k delta^T in place, o partial = S^T q
-#pragma unroll
-  for (int c = 0; c < VPL; ++c) part[c] = 0.f;
-#pragma unroll 8
-  for (int i = 0; i < RPW; ++i) {
-    const int row = w * RPW + i;
-    SmemIO<ST, VPL>::load(Ss + row * V + lane * VPL, x);
-    const float kk = kn[row], qq = qn[row];
-#pragma unroll
-    for (int c = 0; c < VPL; ++c) {
-      x[c] = fmaf(decay, x[c], kk * delta[c]);
-      part[c] = fmaf(x[c], qq, part[c]);
-    }
-    SmemIO<ST, VPL>::store(Ss + row * V + lane * VPL, x);
-  }
-#pragma unroll
-  for (int c = 0; c < VPL; ++c) red[w][lane * VPL + c] = part[c];
-  fence_proxy_async_smem();  // the new state, visible to the bulk copy
-  __syncthreads();
-  if (tid == 0) {
-    bulk_store(S, ss, SBYTES);
-    bulk_commit();
-  }
-  if (w == NW - 1) {
-    uint16_t *orow = o + gi * V;
-#pragma unroll
-    for (int c = 0; c < VPL; ++c) {
-      float os = 0.f;
-#pragma unroll
-      for (int j = 0; j < NW; ++j) os += red[j][lane * VPL + c];
-      orow[lane * VPL + c] = gdn::f2bf(scale * os);
+        for (int j = 0; j < NW; ++j) os += red[j][lane * VPL + c];
+        orow[lane * VPL + c] = gdn::f2bf(scale * os);
+      }
     }
   }
-  if (tid == 0) bulk_wait_all();  // the staged state must outlive the copy
+  if (tid == 0) bulk_wait_all();  // the staged state must outlive the copies
 }
 
 template <int K, int V, typename ST>
 cudaError_t launch_kv(const gdn_host::DecodeArgs &a, ST *pool, cudaStream_t s) {
   dim3 grid(a.HV, a.N);
-  // One token per request, in place, and a 16-byte aligned pool (bulk copies).
-  if (!a.cu && a.ld == 1 && !a.num_acc && a.read_idx == a.write_idx &&
-      (reinterpret_cast<uintptr_t>(pool) & 15) == 0) {
+  // A 16-byte aligned pool (bulk copies): the state staged in shared memory.
+  // A bf16 state staged in shared memory would be rounded after every token,
+  // so several tokens per request against a bf16 pool keep the register kernel.
+  const bool one_token = !a.cu && a.ld == 1 && !a.num_acc && a.read_idx == a.write_idx;
+  if ((reinterpret_cast<uintptr_t>(pool) & 15) == 0 && (sizeof(ST) == 4 || one_token)) {
     constexpr int smem = K * V * (int)sizeof(ST);
-    cudaError_t e = cudaFuncSetAttribute(decode_staged_kernel<K, V, ST>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    auto kern = one_token ? decode_staged_kernel<K, V, ST, false> : decode_staged_kernel<K, V, ST, true>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    decode_staged_kernel<K, V, ST><<<grid, kStagedThreads, smem, s>>>(
-        a.q, a.k, a.v, a.g, a.beta, a.A_log, a.a, a.b, a.dt_bias, a.scale, a.l2, pool, a.P, a.read_idx, a.H,
-        a.HV, a.o, a.dev_status);
+    kern<<<grid, kStagedThreads, smem, s>>>(a.q, a.k, a.v, a.g, a.beta, a.A_log, a.a, a.b, a.dt_bias, a.scale, a.l2,
+                                           pool, a.P, a.cu, a.Ttot, a.read_idx, a.write_idx, a.ld, a.num_acc, a.H,
+                                           a.HV, a.o, a.dev_status);
     return cudaGetLastError();
   }
   decode_kernel<K, V, ST><<<grid, kWarps * 32, 0, s>>>(
