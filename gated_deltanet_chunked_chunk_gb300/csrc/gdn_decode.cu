@@ -28,13 +28,15 @@ using gdn::bulk_commit;
 using gdn::bulk_load;
 using gdn::bulk_store;
 using gdn::bulk_wait_all;
-using gdn::bulk_wait_read_all;
 using gdn::fence_proxy_async_smem;
 using gdn::mbar_arrive_expect_tx;
 using gdn::mbar_fence_init;
 using gdn::mbar_init;
 using gdn::mbar_wait_bounded;
 using gdn::smem_u32;
+
+// Waits until every committed bulk store of this thread has read its source.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 constexpr int kWarps = 8;
 
