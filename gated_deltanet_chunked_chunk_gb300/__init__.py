@@ -26,7 +26,8 @@ __all__ = ["gdn_gating", "gdn_chunk_fwd", "gdn_recurrent_decode", "chunk_fwd_wor
            "gdn_causal_conv1d_update", "gdn_conv_decode_pack", "gdn_recurrent_decode_bf16",
            "gdn_recurrent_decode_mtp", "gdn_chunk_bwd", "chunk_bwd_workspace_size",
            "gdn_chunk_fwd_gated", "chunk_gated_delta_rule", "GDNError", "lib_path", "load_library", "status_string", "DEV_BAD_CU_SEQLENS",
-           "DEV_BAD_SLOT", "DEV_WAIT_TIMEOUT", "EXPORTED_SYMBOLS"]
+           "DEV_BAD_SLOT", "DEV_WAIT_TIMEOUT", "DEV_DRAIN_TIMEOUT", "EXPORTED_SYMBOLS",
+           "testing_force_wait_expiry"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "_build", "libgdn.so")
@@ -34,14 +35,14 @@ _lib = None
 _lock = threading.Lock()
 
 GDN_OK, GDN_EINVAL, GDN_EUNSUPPORTED, GDN_ECUDA, GDN_EWORKSPACE, GDN_ESCRATCH_LIMIT = 0, 1, 2, 3, 4, 5
-DEV_BAD_CU_SEQLENS, DEV_BAD_SLOT, DEV_WAIT_TIMEOUT = 1, 2, 4
+DEV_BAD_CU_SEQLENS, DEV_BAD_SLOT, DEV_WAIT_TIMEOUT, DEV_DRAIN_TIMEOUT = 1, 2, 4, 8
 
 #: Every symbol include/gdn.h declares (checked by the tests).
 EXPORTED_SYMBOLS = ("gdn_status_string", "gdn_version", "gdn_gating", "gdn_chunk_fwd_workspace_size",
                     "gdn_chunk_fwd", "gdn_recurrent_decode", "gdn_chunk_fwd_noalloc",
                     "gdn_causal_conv1d_fwd", "gdn_causal_conv1d_update", "gdn_conv_decode_pack",
                     "gdn_recurrent_decode_bf16", "gdn_recurrent_decode_mtp", "gdn_chunk_bwd_workspace_size",
-                    "gdn_chunk_bwd", "gdn_chunk_fwd_gated")
+                    "gdn_chunk_bwd", "gdn_chunk_fwd_gated", "gdn_testing_force_wait_expiry")
 
 #: Size of the fixed scratch buffer behind gdn_chunk_fwd_noalloc (bytes).
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -72,6 +73,8 @@ def load_library():
         lib.gdn_status_string.restype = ctypes.c_char_p
         lib.gdn_version.argtypes = []
         lib.gdn_version.restype = I
+        lib.gdn_testing_force_wait_expiry.argtypes = [I]
+        lib.gdn_testing_force_wait_expiry.restype = I
         lib.gdn_gating.argtypes = [P, P, P, P, I64, I, P, P, P]
         lib.gdn_gating.restype = I
         lib.gdn_chunk_fwd_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
@@ -112,6 +115,13 @@ def status_string(code: int) -> str:
         return load_library().gdn_status_string(int(code)).decode()
     except RuntimeError:
         return f"status {code}"
+
+
+def testing_force_wait_expiry(on: bool) -> bool:
+    """Testing hook of the C ABI (gdn_testing_force_wait_expiry): while on, the
+    first bounded wait of every decode block and chunk-forward chain runs out
+    and the kernels take their failure path.  Returns the previous setting."""
+    return bool(load_library().gdn_testing_force_wait_expiry(1 if on else 0))
 
 
 def _ptr(t: Optional[torch.Tensor]):

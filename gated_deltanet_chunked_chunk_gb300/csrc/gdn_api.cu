@@ -2,11 +2,16 @@
 // launches.  No entry point allocates device memory or synchronises.
 #include <math.h>
 
+#include <atomic>
+
 #include "gdn_common.cuh"
 
 namespace {
 
 bool head_dim_ok(int d) { return d == 64 || d == 128; }
+
+// Testing hook (gdn_testing_force_wait_expiry): read at every launch.
+std::atomic<int> g_force_wait_expiry{0};
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ECUDA; }
 
@@ -18,7 +23,7 @@ const char *gdn_status_string(int status) {
   switch (status) {
     case GDN_OK: return "ok";
     case GDN_EINVAL: return "invalid argument (null pointer, inconsistent shape, HV % H != 0, or B != 1 with cu_seqlens)";
-    case GDN_EUNSUPPORTED: return "unsupported configuration (head dims K and V must be 64 or 128)";
+    case GDN_EUNSUPPORTED: return "unsupported configuration (head dims K and V must be 64 or 128; at most 65535 sequences or requests per call)";
     case GDN_ECUDA: return "CUDA error while launching";
     case GDN_EWORKSPACE: return "workspace missing or too small";
     case GDN_ESCRATCH_LIMIT: return "input needs more workspace than the fixed no-allocation scratch holds; call gdn_chunk_fwd with a workspace";
@@ -26,7 +31,9 @@ const char *gdn_status_string(int status) {
   }
 }
 
-int gdn_version(void) { return 100; }
+int gdn_version(void) { return 200; }
+
+int gdn_testing_force_wait_expiry(int on) { return g_force_wait_expiry.exchange(on ? 1 : 0); }
 
 int gdn_gating(const float *A_log, const uint16_t *a, const uint16_t *b,
                const float *dt_bias, int64_t Ttok, int HV, float *g,
@@ -58,6 +65,7 @@ int chunk_fwd_common(gdn_host::ChunkArgs &a, const uint16_t *q, const uint16_t *
     return GDN_EINVAL;
   }
   if (!head_dim_ok(K) || !head_dim_ok(V)) return GDN_EUNSUPPORTED;
+  if (N > 65535) return GDN_EUNSUPPORTED;
   const bool has_tokens = (int64_t)B * T > 0;
   const bool gates = a.A_log ? (a.ga && a.gb && a.dt_bias) : (a.g && a.beta);
   if (has_tokens && (!q || !k || !v || !gates || !o)) return GDN_EINVAL;
@@ -71,6 +79,7 @@ int chunk_fwd_common(gdn_host::ChunkArgs &a, const uint16_t *q, const uint16_t *
   a.l2 = use_qk_l2norm ? 1 : 0;
   a.o = o; a.ht = final_state; a.ws = workspace; a.ws_bytes = workspace_bytes;
   a.dev_status = dev_status;
+  a.force_expiry = g_force_wait_expiry.load();
   return cuda_status(gdn_host::launch_chunk(a, static_cast<cudaStream_t>(stream)));
 }
 }  // namespace
@@ -118,6 +127,7 @@ int gdn_chunk_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const
     return GDN_EINVAL;
   }
   if (!head_dim_ok(K) || !head_dim_ok(V)) return GDN_EUNSUPPORTED;
+  if (N > 65535) return GDN_EUNSUPPORTED;
   const bool has_tokens = (int64_t)B * T > 0;
   if (has_tokens && (!q || !k || !v || !g || !beta || !dout || !dq || !dk || !dv || !dg || !dbeta))
     return GDN_EINVAL;
@@ -143,6 +153,9 @@ int decode_common(const uint16_t *q, const uint16_t *k, const uint16_t *v, const
   if (HV % H != 0) return GDN_EINVAL;
   if (!head_dim_ok(K) || !head_dim_ok(V)) return GDN_EUNSUPPORTED;
   if (!q || !k || !v || !o || !pool) return GDN_EINVAL;
+  // The state moves in 16-byte vectors and bulk copies: a misaligned pool (a
+  // view at an odd offset) is refused here instead of faulting on the device.
+  if (reinterpret_cast<uintptr_t>(pool) & 15u) return GDN_EINVAL;
   const bool given = g || beta;
   const bool fused = A_log || a || b || dt_bias;
   if (given == fused) return GDN_EINVAL;  // exactly one gate group
@@ -152,6 +165,7 @@ int decode_common(const uint16_t *q, const uint16_t *k, const uint16_t *v, const
   d.scale = (scale > 0.f) ? scale : 1.f / sqrtf((float)K);  // also catches NaN
   d.l2 = use_qk_l2norm ? 1 : 0;
   d.H = H; d.HV = HV; d.K = K; d.V = V;
+  d.force_expiry = g_force_wait_expiry.load();
   return GDN_OK;
 }
 }  // namespace
@@ -168,6 +182,7 @@ int gdn_recurrent_decode(const uint16_t *q, const uint16_t *k,
   if (H <= 0 || HV <= 0 || K <= 0 || V <= 0 || HV % H != 0) return GDN_EINVAL;
   if (!head_dim_ok(K) || !head_dim_ok(V)) return GDN_EUNSUPPORTED;
   if (R == 0) return GDN_OK;
+  if (R > 65535) return GDN_EUNSUPPORTED;  // requests index the grid's y dimension
   if (!ssm_indices) return GDN_EINVAL;
   gdn_host::DecodeArgs d{};
   const int rc = decode_common(q, k, v, g, beta, A_log, a, b, dt_bias, scale, use_qk_l2norm, ssm_pool, H, HV,
@@ -189,6 +204,7 @@ int gdn_recurrent_decode_bf16(const uint16_t *q, const uint16_t *k, const uint16
   if (H <= 0 || HV <= 0 || K <= 0 || V <= 0 || HV % H != 0) return GDN_EINVAL;
   if (!head_dim_ok(K) || !head_dim_ok(V)) return GDN_EUNSUPPORTED;
   if (R == 0) return GDN_OK;
+  if (R > 65535) return GDN_EUNSUPPORTED;  // requests index the grid's y dimension
   if (!ssm_indices) return GDN_EINVAL;
   gdn_host::DecodeArgs d{};
   const int rc = decode_common(q, k, v, g, beta, A_log, a, b, dt_bias, scale, use_qk_l2norm, ssm_pool, H, HV,

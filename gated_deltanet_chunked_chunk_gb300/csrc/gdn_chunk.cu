@@ -901,7 +901,7 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
       if (warp < 4 || warp == 6) {
         tc_fence_after();
         umma_commit(b_drain);
-        mbar_wait_bounded(b_drain, 0, kWaitLimit);
+        if (!mbar_wait_bounded(b_drain, 0, kWaitLimit)) set_status(dev_status, GDN_DEV_DRAIN_TIMEOUT);
       }
     }
     if (ht && krow && !*abort_flag) {
@@ -941,7 +941,8 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
     if (lane == 0 && *abort_flag) {
       // Nothing of this CTA may still be in flight at exit.
       for (int k = (issued > NS ? issued - NS : 0); k < issued; ++k)
-        mbar_wait_bounded(bar(FULL, k % NS), (k / NS) & 1, kWaitLimit);
+        if (!mbar_wait_bounded(bar(FULL, k % NS), (k / NS) & 1, kWaitLimit))
+          set_status(dev_status, GDN_DEV_DRAIN_TIMEOUT);
     }
   }
   tc_fence_before();

@@ -10,6 +10,7 @@ namespace gdnc {
 
 constexpr int C = 64;                           // chunk length
 constexpr long long kWaitLimit = 2000000000LL;  // clock cycles (about 1 s) before a wait gives up
+constexpr long long kTestWaitLimit = 4000;       // the testing hook's wait on a barrier nothing completes
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Per-(chunk, value head) record, byte offsets; also its shared-memory image.

@@ -76,6 +76,7 @@ struct DecodeArgs {
   int H, HV, K, V;
   uint16_t *o;
   int32_t *dev_status;
+  int force_expiry;  // testing hook: the first bounded wait of every block runs out
 };
 cudaError_t launch_decode_general(const DecodeArgs &a, cudaStream_t s);
 struct ChunkArgs {
@@ -98,6 +99,7 @@ struct ChunkArgs {
   void *ws;
   size_t ws_bytes;
   int32_t *dev_status;
+  int force_expiry;  // testing hook: the first bounded wait of every chain runs out
 };
 size_t chunk_workspace_bytes(int B, int T, int H, int HV, int K, int V, int N,
                              int varlen);

@@ -11,13 +11,17 @@
 // owns one (value head, request) state; lane l works on V/32 consecutive
 // columns of K/8 rows (warp w owns rows [w K/8, (w+1) K/8)), so every warp
 // access is one contiguous row segment, and the two reductions over K
-// (S^T k and S^T q) go through shared memory across the 8 warps.  One token
-// per request (decode_staged_kernel): the state is staged in shared memory by
-// one bulk asynchronous copy and written back by one, so several blocks share
-// an SM and much of the pool is in flight.  Several tokens per request (the
-// MTP form, decode_kernel): the state stays in registers across the tokens,
-// loaded with 16-byte streaming loads all at once before any arithmetic and
-// stored with streaming stores after each token.
+// (S^T k and S^T q) go through shared memory across the 8 warps.  The fp32
+// pool, one token or several per request (decode_staged_kernel; the MTP form
+// adds a token loop): the state is staged in shared memory by one bulk
+// asynchronous copy, updated in place and written back by one bulk copy per
+// kept state, so several blocks share an SM and much of the pool is in
+// flight.  The bf16 pool with one token per request takes the same kernel;
+// with several tokens per request (decode_kernel) the state stays in fp32
+// registers across the tokens (a bf16 copy staged in shared memory would be
+// rounded after every token), loaded with 16-byte streaming loads all at once
+// before any arithmetic and stored after each kept token.  Pools are 16-byte
+// aligned (the entry points refuse others).
 #include "gdn_chunk_shared.cuh"
 #include "gdn_common.cuh"
 #include "gdn_sm103.cuh"
@@ -290,7 +294,8 @@ __global__ void __launch_bounds__(kStagedThreads, 5) decode_staged_kernel(
     const uint16_t *__restrict__ a_raw, const uint16_t *__restrict__ b_raw, const float *__restrict__ dt_bias,
     float scale, int l2, ST *pool, int P, const int32_t *__restrict__ cu, int Ttot,
     const int32_t *__restrict__ read_idx, const int32_t *__restrict__ write_idx, int ld,
-    const int32_t *__restrict__ num_acc, int H, int HV, uint16_t *__restrict__ o, int32_t *dev_status) {
+    const int32_t *__restrict__ num_acc, int H, int HV, uint16_t *__restrict__ o, int32_t *dev_status,
+    int force_expiry) {
   constexpr int NW = kStagedThreads / 32, VPL = V / 32, RPW = K / NW;
   constexpr uint32_t SBYTES = K * V * sizeof(ST);
   extern __shared__ __align__(128) unsigned char dsm[];
@@ -298,7 +303,7 @@ __global__ void __launch_bounds__(kStagedThreads, 5) decode_staged_kernel(
   __shared__ float qn[K], kn[K];
   __shared__ float red[NW][V];
   __shared__ float sh_norm[2];
-  __shared__ __align__(8) uint64_t bar;
+  __shared__ __align__(8) uint64_t bar, never;
   const int hv = blockIdx.x, n = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   int t0 = n, t1 = n + 1;
@@ -329,9 +334,10 @@ __global__ void __launch_bounds__(kStagedThreads, 5) decode_staged_kernel(
   }
   if (MT && t1 == t0) return;
   const int h = hv / (HV / H);
-  const uint32_t b_ld = smem_u32(&bar), ss = smem_u32(Ss);
+  const uint32_t b_ld = smem_u32(&bar), ss = smem_u32(Ss), b_never = smem_u32(&never);
   if (tid == 0) {
     mbar_init(b_ld, 1);
+    mbar_init(b_never, 1);  // nothing ever arrives: the testing hook's wait
     mbar_fence_init();
     mbar_arrive_expect_tx(b_ld, SBYTES);
     bulk_load(ss, pool + ((int64_t)s * HV + hv) * (int64_t)K * V, SBYTES, b_ld);
@@ -384,13 +390,19 @@ __global__ void __launch_bounds__(kStagedThreads, 5) decode_staged_kernel(
 #pragma unroll
     for (int c = 0; c < VPL; ++c) vv[c] = gdn::bf2f(v[gi * V + lane * VPL + c]);
     if (!MT || t == t0) {
-      // Every thread sees the copy complete (bounded); on expiry the block waits
-      // once more for the copy to drain, records the error and leaves.
-      const bool landed = __syncthreads_and(mbar_wait_bounded(b_ld, 0, gdnc::kWaitLimit) ? 1 : 0) != 0;
+      // Every thread sees the copy complete (bounded).  On expiry thread 0
+      // waits once more, with the full limit, for the copy into this block's
+      // shared memory; the block then leaves without writing anything.  If that
+      // second wait runs out as well the copy may still land after the block
+      // has exited, which GDN_DEV_DRAIN_TIMEOUT reports.  The testing hook
+      // replaces the first wait by a short one on a barrier nothing completes.
+      const bool got = force_expiry ? mbar_wait_bounded(b_never, 0, gdnc::kTestWaitLimit)
+                                    : mbar_wait_bounded(b_ld, 0, gdnc::kWaitLimit);
+      const bool landed = __syncthreads_and(got ? 1 : 0) != 0;
       if (!landed) {
         if (tid == 0) {
-          mbar_wait_bounded(b_ld, 0, gdnc::kWaitLimit);
-          gdn::set_status(dev_status, GDN_DEV_WAIT_TIMEOUT);
+          const bool drained = mbar_wait_bounded(b_ld, 0, gdnc::kWaitLimit);
+          gdn::set_status(dev_status, GDN_DEV_WAIT_TIMEOUT | (drained ? 0 : GDN_DEV_DRAIN_TIMEOUT));
         }
         return;
       }
@@ -468,18 +480,19 @@ __global__ void __launch_bounds__(kStagedThreads, 5) decode_staged_kernel(
 template <int K, int V, typename ST>
 cudaError_t launch_kv(const gdn_host::DecodeArgs &a, ST *pool, cudaStream_t s) {
   dim3 grid(a.HV, a.N);
-  // A 16-byte aligned pool (bulk copies): the state staged in shared memory.
-  // A bf16 state staged in shared memory would be rounded after every token,
-  // so several tokens per request against a bf16 pool keep the register kernel.
+  // The pool is 16-byte aligned (checked by the entry points): the state is
+  // staged in shared memory by bulk copies.  A bf16 state staged in shared
+  // memory would be rounded after every token, so several tokens per request
+  // against a bf16 pool keep the register kernel.
   const bool one_token = !a.cu && a.ld == 1 && !a.num_acc && a.read_idx == a.write_idx;
-  if ((reinterpret_cast<uintptr_t>(pool) & 15) == 0 && (sizeof(ST) == 4 || one_token)) {
+  if (sizeof(ST) == 4 || one_token) {
     constexpr int smem = K * V * (int)sizeof(ST);
     auto kern = one_token ? decode_staged_kernel<K, V, ST, false> : decode_staged_kernel<K, V, ST, true>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, kStagedThreads, smem, s>>>(a.q, a.k, a.v, a.g, a.beta, a.A_log, a.a, a.b, a.dt_bias, a.scale, a.l2,
                                            pool, a.P, a.cu, a.Ttot, a.read_idx, a.write_idx, a.ld, a.num_acc, a.H,
-                                           a.HV, a.o, a.dev_status);
+                                           a.HV, a.o, a.dev_status, a.force_expiry);
     return cudaGetLastError();
   }
   decode_kernel<K, V, ST><<<grid, kWarps * 32, 0, s>>>(

@@ -56,7 +56,12 @@ enum gdn_status_code {
 enum gdn_device_status_bits {
   GDN_DEV_BAD_CU_SEQLENS = 1, /* cu_seqlens not non-decreasing from 0, or past T */
   GDN_DEV_BAD_SLOT = 2,       /* decode slot index < -1 or >= P (row treated as PAD) */
-  GDN_DEV_WAIT_TIMEOUT = 4    /* a bounded wait inside a kernel gave up */
+  GDN_DEV_WAIT_TIMEOUT = 4,   /* a bounded wait inside a kernel gave up */
+  GDN_DEV_DRAIN_TIMEOUT = 8   /* after GDN_DEV_WAIT_TIMEOUT, the wait for the
+                                 block's own copies (or tensor-core products)
+                                 in flight gave up too: shared or tensor memory
+                                 of that block may still have been written after
+                                 it exited; treat the context as suspect */
 };
 
 /* Static text for a gdn_status_code.  Never NULL. */
@@ -64,6 +69,21 @@ const char *gdn_status_string(int status);
 
 /* Library version as major*10000 + minor*100 + patch. */
 int gdn_version(void);
+
+/*
+ * gdn_testing_force_wait_expiry -- a testing hook for the failure path of the
+ * bounded waits; the pages have no counterpart.  Never set it in production.
+ * While `on` is nonzero (process-wide), the first bounded wait of every block
+ * of the decode kernels (gdn_recurrent_decode, _bf16, _mtp) and of every
+ * chain of the chunked forward waits on a barrier that nothing completes,
+ * with a limit of a few thousand cycles, so it runs out every time.  The block
+ * then takes the path a real expiry takes: it waits, with the normal limit,
+ * for the copies (and tensor-core products) it has in flight, writes nothing
+ * to the state pool, ORs GDN_DEV_WAIT_TIMEOUT into dev_status (and
+ * GDN_DEV_DRAIN_TIMEOUT if that second wait ran out too) and returns.  Outputs
+ * of such a call are unspecified.  Returns the previous setting.
+ */
+int gdn_testing_force_wait_expiry(int on);
 
 /*
  * gdn_gating -- fused gate computation, one launch.
@@ -119,6 +139,7 @@ size_t gdn_chunk_fwd_workspace_size(int B, int T, int H, int HV, int K, int V,
  *                   (NULL when that size is 0)
  * Chunks restart at every sequence start; the last chunk of a sequence may be
  * partial.  A sequence of length 0 writes final_state = initial_state (or 0).
+ * N > 65535 returns GDN_EUNSUPPORTED.
  */
 int gdn_chunk_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                   const float *g, const float *beta, float scale,
@@ -177,7 +198,9 @@ int gdn_chunk_fwd_gated(const uint16_t *q, const uint16_t *k, const uint16_t *v,
  *                 GDN_DEV_BAD_SLOT and are treated like PAD.  Two requests
  *                 naming the same slot is a caller error (undefined result).
  *   o           : bf16 [R, 1, HV, V] output
- * R = 0 is a no-op.
+ * R = 0 is a no-op.  The pool must be 16-byte aligned (the state moves in
+ * 16-byte vectors and bulk copies); a misaligned pool returns GDN_EINVAL
+ * before anything is launched.  R > 65535 returns GDN_EUNSUPPORTED.
  */
 int gdn_recurrent_decode(const uint16_t *q, const uint16_t *k,
                          const uint16_t *v, const float *g, const float *beta,
@@ -232,8 +255,8 @@ int gdn_chunk_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
  * state bytes of the fp32 pool (the bf16 state-pool variant of the LightLLM
  * "gdn.py" backend's ssm cache).  The step runs in fp32 on the stored values;
  * o is computed from the updated fp32 state, which is then rounded to bf16
- * (to nearest, ties to even) when stored.  Everything else as
- * gdn_recurrent_decode.
+ * (to nearest, ties to even) when stored.  Everything else, including the
+ * 16-byte alignment of the pool and R <= 65535, as gdn_recurrent_decode.
  */
 int gdn_recurrent_decode_bf16(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                               const float *g, const float *beta, const float *A_log,
@@ -265,7 +288,9 @@ int gdn_recurrent_decode_bf16(const uint16_t *q, const uint16_t *k, const uint16
  *   num_accepted_tokens : int32 [N] in [1, ld], or NULL (read column 0)
  *   o             : bf16 [Ttot, HV, V]
  * The read slot is loaded before any store of the request, so it may also be
- * one of its write slots.  Requests must not share slots.  One launch.
+ * one of its write slots; a slot written twice by one request keeps the later
+ * state.  Requests must not share slots.  The pool must be 16-byte aligned
+ * (else GDN_EINVAL); N > 65535 returns GDN_EUNSUPPORTED.  One launch.
  */
 int gdn_recurrent_decode_mtp(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                              const float *g, const float *beta, const float *A_log,
@@ -293,7 +318,9 @@ int gdn_recurrent_decode_mtp(const uint16_t *q, const uint16_t *k, const uint16_
  *
  * The first call on a device looks up the buffer's device address (with that
  * device current) and caches it; make that first call before any stream
- * capture.  The call allocates nothing and calls no allocating library
+ * capture.  The cached address belongs to the device's current context: after
+ * cudaDeviceReset() the process must not call this entry point again on that
+ * device (the cache would hand the kernels a stale address).  The call allocates nothing and calls no allocating library
  * routine.  All calls on a device share the buffer: calls that overlap on the
  * GPU (different streams without ordering) race on it.  Nothing in the buffer
  * needs to start at zero.

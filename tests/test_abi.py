@@ -205,3 +205,43 @@ def test_backward_binding_checks_shapes_before_calling():
         gdn.gdn_chunk_bwd(q, q, v, g[..., :2], g[..., :2], v)
     with pytest.raises(ValueError):   # dht must be [N,HV,K,V]
         gdn.gdn_chunk_bwd(q, q, v, g, g, v, dht=torch.zeros(1, 4, 64, 32))
+
+
+def test_misaligned_pool_and_grid_limits_refused_before_launch(lib):
+    """A pool that is not 16-byte aligned (a view at an odd offset) would meet
+    16-byte vector accesses and bulk copies on the device: every decode entry
+    point refuses it on the host.  Request / sequence counts beyond the grid's
+    65535 come back as GDN_EUNSUPPORTED.  No call below reaches a launch."""
+    NULL = None
+    fake = ctypes.c_void_p(16)
+    odd = ctypes.c_void_p(16 + 8)     # 8-byte aligned, not 16
+    F = ctypes.c_float
+
+    def dec(pool=fake, R=2):
+        return lib.gdn_recurrent_decode(fake, fake, fake, fake, fake, NULL, NULL, NULL, NULL, F(-1.0), 1, pool, 4,
+                                        fake, R, 2, 4, 128, 128, fake, NULL, NULL)
+
+    def bf16(pool=fake, R=2):
+        return lib.gdn_recurrent_decode_bf16(fake, fake, fake, fake, fake, NULL, NULL, NULL, NULL, F(-1.0), 1, pool,
+                                             4, fake, R, 2, 4, 128, 128, fake, NULL, NULL)
+
+    def mtp(pool=fake):
+        return lib.gdn_recurrent_decode_mtp(fake, fake, fake, fake, fake, NULL, NULL, NULL, NULL, F(-1.0), 1,
+                                            pool, 8, fake, 2, 6, fake, fake, 3, NULL, 2, 4, 64, 64, fake, NULL,
+                                            NULL)
+
+    assert dec(pool=odd) == gdn.GDN_EINVAL
+    assert bf16(pool=odd) == gdn.GDN_EINVAL
+    assert mtp(pool=odd) == gdn.GDN_EINVAL
+    assert dec(R=70000) == gdn.GDN_EUNSUPPORTED
+    assert bf16(R=70000) == gdn.GDN_EUNSUPPORTED
+    assert _chunk(lib, cu=fake, B=1, N=70000, q=fake, k=fake, v=fake, g=fake, beta=fake,
+                  o=fake) == gdn.GDN_EUNSUPPORTED
+    assert "65535" in gdn.status_string(gdn.GDN_EUNSUPPORTED)
+
+
+def test_wait_expiry_hook_toggles(lib):
+    assert lib.gdn_testing_force_wait_expiry(0) == 0
+    assert lib.gdn_testing_force_wait_expiry(1) == 0
+    assert gdn.testing_force_wait_expiry(False) is True
+    assert lib.gdn_testing_force_wait_expiry(0) == 0

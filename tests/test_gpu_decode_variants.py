@@ -154,3 +154,38 @@ def test_bf16_pool_decode_matches_oracle(fused):
     for r in range(len(idx)):
         if idx[r] < 0:
             assert (o[r] == 0).all()
+
+
+def test_mtp_skipped_and_repeated_write_slots():
+    """A write slot of -1 in the middle of a request stores nothing for that
+    token, and a slot written twice by one request keeps the later state (the
+    kernel orders its per-token stores); every other slot stays bit-exact."""
+    N, ld, H, HV, K, V = 6, 4, 2, 4, 128, 128
+    x = _mtp_inputs(311, N, ld, H, HV, K, V, short_every=100)
+    write = x["write"].clone()
+    write[:, 1] = -1                   # token 1 of every request is not kept
+    write[:, 2] = write[:, 0]          # token 2 overwrites token 0's slot
+    gdn = _gdn()
+    pool = x["pool"].to(DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    o = gdn.gdn_recurrent_decode_mtp(
+        x["q"].to(DEV), x["k"].to(DEV), x["v"].to(DEV), pool, x["cu"].to(DEV), x["read"].to(DEV),
+        write.to(DEV), x["acc"].to(DEV), A_log=x["A_log"].to(DEV), a=x["a"].to(DEV), b=x["b"].to(DEV),
+        dt_bias=x["dt"].to(DEV), dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    g_ref, b_ref = oracle.gating(x["A_log"], x["a"], x["b"], x["dt"])
+    o_ref, pool_ref, bad = oracle.decode_mtp(x["q"], x["k"], x["v"], g_ref, b_ref, x["pool"], x["cu"].numpy(),
+                                             x["read"].numpy(), write.numpy(), x["acc"].numpy())
+    assert bad == 0
+    P.assert_o_close(o.float().cpu().numpy(), o_ref, "o (mtp, skipped / repeated slots)")
+    pool_np = pool.cpu().numpy()
+    written = sorted({int(s) for s in write.flatten().tolist() if s >= 0 and
+                      any(int(write[n, i]) == s for n in range(N) for i in range(int(x["cu"][n + 1] - x["cu"][n])))})
+    P.assert_state_close(pool_np[written], pool_ref[written], "written states")
+    for s in written:   # the kept state is the later token's, not token 0's
+        n = s // ld
+        if int(x["cu"][n + 1] - x["cu"][n]) >= 3:
+            assert not np.allclose(pool_ref[s], x["pool"].numpy()[s])
+    rest = sorted(set(range(pool_np.shape[0])) - set(written))
+    np.testing.assert_array_equal(pool_np[rest], x["pool"].numpy()[rest])
