@@ -570,7 +570,7 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
     const __grid_constant__ CUtensorMap tm_v, float scale, const float *__restrict__ h0,
     const int32_t *__restrict__ cu, int T, int H, int HV, int V, const unsigned char *__restrict__ ws,
     uint16_t *__restrict__ o, float *__restrict__ ht, float *__restrict__ hsave, const int32_t *__restrict__ cs,
-    int32_t *dev_status) {
+    int32_t *dev_status, int force_expiry) {
   using Ly = WalkLay<K>;
   using R = Rec<K>;
   constexpr int KA = K / 64;
@@ -607,6 +607,7 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
   enum { FULL = 0, CDONE = 1 };
   auto bar = [&](int kind, int b) { return sb + Ly::OFF_BAR + 8 * (2 * kind + b); };
   const uint32_t b_m1 = sb + Ly::OFF_BAR + 32, b_m2 = sb + Ly::OFF_BAR + 40, b_drain = sb + Ly::OFF_BAR + 48;
+  const uint32_t b_never = sb + Ly::OFF_BAR + 56;  // nothing arrives: the testing hook's wait
   if (tid == 0) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(FULL, b), 2);
@@ -615,6 +616,7 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
     mbar_init(b_m1, 5);
     mbar_init(b_m2, 2);
     mbar_init(b_drain, 5);
+    mbar_init(b_never, 1);
     misc[1] = 0;
     mbar_fence_init();
     mbar_arrive(bar(FULL, 0));  // no output product precedes chunk 0
@@ -630,21 +632,29 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
 
   // Bounded wait; lane 0 polls and the result is warp-uniform.  After an
   // expired wait every later wait of this warp returns false at once (loops
-  // run to their end without work but still pass every named barrier); other
-  // warps see their own waits expire.  The shared flag only records the abort
-  // (reading it on every wait would queue behind the TMA traffic).
+  // run to their end without work but still pass every named barrier).  A
+  // wait also gives up once another warp has recorded an abort in the shared
+  // flag (read every 64 polls only: reading it on every poll would queue
+  // behind the TMA traffic).
   bool dead = false;
-  auto waitb = [&](uint32_t b, uint32_t parity) -> bool {
+  auto waitl = [&](uint32_t b, uint32_t parity, long long limit) -> bool {
     uint32_t ok = 0;
     if (lane == 0 && !dead) {
-      ok = mbar_wait_bounded(b, parity, kWaitLimit) ? 1u : 0u;
-      if (!ok) *abort_flag = 1;
+      const long long t0 = clock64();
+      for (int it = 1;; ++it) {
+        if (mbar_try_wait(b, parity)) { ok = 1; break; }
+        if ((it & 63) == 0) {
+          if (*abort_flag) break;
+          if (clock64() - t0 > limit) { *abort_flag = 1; break; }
+        }
+      }
     }
     __syncwarp();
     ok = __shfl_sync(0xffffffffu, ok, 0);
     dead = dead || !ok;
     return ok != 0;
   };
+  auto waitb = [&](uint32_t b, uint32_t parity) { return waitl(b, parity, kWaitLimit); };
   auto waitc = [&](int kind, int c) { return waitb(bar(kind, c & 1), (c >> 1) & 1); };
   auto chunk_rows = [&](int c) {
     const int64_t rem = len - static_cast<int64_t>(c) * C;
@@ -778,7 +788,9 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
 #pragma unroll
         for (int j = 0; j < 16; j += 4) *reinterpret_cast<float4 *>(dst + j) = make_float4(hr[j], hr[j + 1], hr[j + 2], hr[j + 3]);
       }
-      go = waitc(FULL, c) && go;  // also: the output product of chunk c - 1 is done
+      // also: the output product of chunk c - 1 is done.  The testing hook
+      // replaces the first wait by one on a barrier nothing completes.
+      go = ((force_expiry && c == 0) ? waitl(b_never, 0, kTestWaitLimit) : waitc(FULL, c)) && go;
       // [W; Q] [h_hi | h_lo]: warp p < 4 takes k-steps [p KA, p KA + KA).
       if (warp < 4 && lane == 0 && go) {
         tc_fence_after();
@@ -1067,7 +1079,7 @@ cudaError_t launch_k(const gdn_host::ChunkArgs &a, cudaStream_t s) {
   dim3 grid(a.V / VT, a.HV, a.N);
   chunk_walk_kernel<K><<<grid, WALK_THREADS, wsmem, s>>>(mq, mk, mv, a.scale, a.h0, a.cu, a.T, a.H, a.HV, a.V,
                                                 static_cast<const unsigned char *>(a.ws), a.o, a.ht, a.hsave, cs,
-                                                a.dev_status);
+                                                a.dev_status, a.force_expiry);
   return cudaGetLastError();
 }
 

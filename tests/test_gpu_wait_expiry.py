@@ -88,3 +88,32 @@ def test_mtp_decode_wait_expiry_reports_and_writes_nothing():
     assert int(st.item()) & gdn.DEV_WAIT_TIMEOUT
     assert not int(st.item()) & gdn.DEV_DRAIN_TIMEOUT
     assert torch.equal(pool, before)
+
+
+def test_chunk_fwd_wait_expiry_reports_and_writes_no_state():
+    """The state walk of the prefill with its first wait forced to run out: the
+    walk drains its loads and products, writes no final state, reports the
+    expiry, and the next normal call is correct."""
+    gdn = _gdn()
+    case = W.prefill_case("expire_chunk", 93, 1, 300, 2, 4, 128, 128, init="all")
+    g, beta = P.oracle_gates(case)
+    d = lambda t: t.cuda().contiguous()
+    q, k, v, gg, bb, h0 = map(d, (case.q, case.k, case.v, g, beta, case.initial_state))
+    ht = torch.full_like(h0, 12345.0)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    prev = gdn.testing_force_wait_expiry(True)
+    try:
+        gdn.gdn_chunk_fwd(q, k, v, gg, bb, initial_state=h0, final_state=ht, dev_status=st)
+        torch.cuda.synchronize()
+    finally:
+        gdn.testing_force_wait_expiry(prev)
+    assert int(st.item()) & gdn.DEV_WAIT_TIMEOUT
+    assert not int(st.item()) & gdn.DEV_DRAIN_TIMEOUT
+    assert bool((ht == 12345.0).all())
+    st.zero_()
+    o, ht2 = gdn.gdn_chunk_fwd(q, k, v, gg, bb, initial_state=h0, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    o_ref, ht_ref = P.run_chunk_oracle(case, g, beta)
+    P.assert_o_close(o.float().cpu().numpy(), o_ref)
+    P.assert_state_close(ht2.cpu().numpy(), ht_ref)
