@@ -23,7 +23,8 @@ import torch
 
 __all__ = ["gdn_gating", "gdn_chunk_fwd", "gdn_recurrent_decode", "chunk_fwd_workspace_size",
            "gdn_chunk_fwd_noalloc", "NOALLOC_SCRATCH_BYTES", "gdn_causal_conv1d_fwd",
-           "gdn_causal_conv1d_update", "gdn_conv_decode_pack", "gdn_recurrent_decode_bf16",
+           "gdn_causal_conv1d_update", "gdn_causal_conv1d_update_spec", "gdn_conv_decode_pack",
+           "gdn_recurrent_decode_bf16",
            "gdn_recurrent_decode_mtp", "gdn_chunk_bwd", "chunk_bwd_workspace_size",
            "gdn_chunk_fwd_gated", "chunk_gated_delta_rule", "GDNError", "lib_path", "load_library", "status_string", "DEV_BAD_CU_SEQLENS",
            "DEV_BAD_SLOT", "DEV_WAIT_TIMEOUT", "DEV_DRAIN_TIMEOUT", "EXPORTED_SYMBOLS",
@@ -42,7 +43,8 @@ EXPORTED_SYMBOLS = ("gdn_status_string", "gdn_version", "gdn_gating", "gdn_chunk
                     "gdn_chunk_fwd", "gdn_recurrent_decode", "gdn_chunk_fwd_noalloc",
                     "gdn_causal_conv1d_fwd", "gdn_causal_conv1d_update", "gdn_conv_decode_pack",
                     "gdn_recurrent_decode_bf16", "gdn_recurrent_decode_mtp", "gdn_chunk_bwd_workspace_size",
-                    "gdn_chunk_bwd", "gdn_chunk_fwd_gated", "gdn_testing_force_wait_expiry")
+                    "gdn_chunk_bwd", "gdn_chunk_fwd_gated", "gdn_testing_force_wait_expiry",
+                    "gdn_causal_conv1d_update_spec")
 
 #: Size of the fixed scratch buffer behind gdn_chunk_fwd_noalloc (bytes).
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -93,6 +95,8 @@ def load_library():
         lib.gdn_causal_conv1d_fwd.restype = I
         lib.gdn_causal_conv1d_update.argtypes = [P, P, I, I, P, P, P, I, I, I, I, P, P, P]
         lib.gdn_causal_conv1d_update.restype = I
+        lib.gdn_causal_conv1d_update_spec.argtypes = [P, P, I, I, P, P, P, P, P, I, I, I, I, I, I, P, P, P]
+        lib.gdn_causal_conv1d_update_spec.restype = I
         lib.gdn_conv_decode_pack.argtypes = [P, P, I, I, P, P, P, I, I, I, I, I, I, I, P, P, P, P, P]
         lib.gdn_conv_decode_pack.restype = I
         lib.gdn_recurrent_decode_bf16.argtypes = [P, P, P, P, P, P, P, P, P, F, I, P, I, P, I, I, I, I, I,
@@ -453,6 +457,38 @@ def gdn_causal_conv1d_update(x: torch.Tensor, conv_state: torch.Tensor, weight: 
         _stream(dev))
     if rc != GDN_OK:
         raise GDNError("gdn_causal_conv1d_update", rc)
+    return out
+
+
+def gdn_causal_conv1d_update_spec(x: torch.Tensor, conv_state: torch.Tensor, weight: torch.Tensor,
+                                  bias: Optional[torch.Tensor], conv_state_indices: torch.Tensor,
+                                  num_accepted_tokens: Optional[torch.Tensor], query_start_loc: torch.Tensor,
+                                  mtp_step: int, activation="silu", out: Optional[torch.Tensor] = None,
+                                  dev_status: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Multi-token (MTP) decode conv; see include/gdn.h.  x [Ttot, dim] bf16;
+    conv_state [P, dim, state_len] bf16 (in place, state_len >= width - 1 +
+    mtp_step); conv_state_indices int32 [N]; num_accepted_tokens int32 [N] or
+    None; query_start_loc int32 [N + 1].  Returns out [Ttot, dim]."""
+    dev = x.device
+    _check(x, "x", torch.bfloat16, dev, 2)
+    _check(conv_state, "conv_state", torch.bfloat16, dev, 3)
+    _check(weight, "weight", torch.bfloat16, dev, 2)
+    _check(bias, "bias", torch.bfloat16, dev, 1)
+    _check(conv_state_indices, "conv_state_indices", torch.int32, dev, 1)
+    _check(num_accepted_tokens, "num_accepted_tokens", torch.int32, dev, 1)
+    _check(query_start_loc, "query_start_loc", torch.int32, dev, 1)
+    Ttot, dim = x.shape
+    N = conv_state_indices.shape[0]
+    if query_start_loc.shape[0] != N + 1:
+        raise ValueError("query_start_loc must hold N + 1 offsets")
+    if out is None:
+        out = torch.empty_like(x)
+    rc = load_library().gdn_causal_conv1d_update_spec(
+        _ptr(x), _ptr(conv_state), conv_state.shape[0], conv_state.shape[2], _ptr(weight), _ptr(bias),
+        _ptr(conv_state_indices), _ptr(num_accepted_tokens), _ptr(query_start_loc), N, Ttot, int(mtp_step), dim,
+        weight.shape[1], _act_code(activation), _ptr(out), _ptr(dev_status), _stream(dev))
+    if rc != GDN_OK:
+        raise GDNError("gdn_causal_conv1d_update_spec", rc)
     return out
 
 

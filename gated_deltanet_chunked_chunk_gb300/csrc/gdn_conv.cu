@@ -234,6 +234,63 @@ __global__ void __launch_bounds__(256) conv_update_kernel(
   srow[S - 1] = xv;
 }
 
+// Multi-token (speculative / MTP) decode, the LightLLM "gdn.py" MTP path's
+// causal_conv1d_update with mtp_step, num_accepted_tokens and query_start_loc.
+// A slot holds the last S inputs of its request's stream as of the previous
+// step, whose last m + 1 entries were that step's tokens; of those only A =
+// num_accepted_tokens[n] were accepted, so the accepted stream is the first
+// S - (m + 1 - A) entries.  The request's tokens follow it (each output uses
+// the W - 1 inputs before it) and the slot then holds the last S entries of
+// accepted ++ tokens (zeros in front if that is shorter).  One thread per
+// (request, channel); the accepted part of the row is read before the row is
+// rewritten.
+__global__ void __launch_bounds__(256) conv_update_spec_kernel(
+    const uint16_t *__restrict__ x, uint16_t *__restrict__ states, int P, int S, const uint16_t *__restrict__ w,
+    const uint16_t *__restrict__ bias, const int32_t *__restrict__ idx, const int32_t *__restrict__ num_acc,
+    const int32_t *__restrict__ qsl, int Ttot, int m, int dim, int W, int act, uint16_t *__restrict__ out,
+    int32_t *dev_status) {
+  const int d = blockIdx.x * blockDim.x + threadIdx.x;
+  const int n = blockIdx.y;
+  if (d >= dim) return;
+  const int t0 = qsl[n], t1 = qsl[n + 1];
+  if (t0 < 0 || t1 < t0 || t1 > Ttot || t1 - t0 > m + 1) {
+    if (d == 0) gdn::set_status(dev_status, GDN_DEV_BAD_CU_SEQLENS);
+    return;
+  }
+  const int slot = idx[n];
+  const int A = num_acc ? num_acc[n] : 1;
+  const bool bad_acc = A < 1 || A > m + 1;
+  if (slot < 0 || slot >= P || bad_acc) {
+    if ((slot != -1 || bad_acc) && d == 0) gdn::set_status(dev_status, GDN_DEV_BAD_SLOT);
+    for (int t = t0; t < t1; ++t) out[(int64_t)t * dim + d] = 0;  // PAD: zero rows, pool untouched
+    return;
+  }
+  uint16_t *srow = states + ((int64_t)slot * dim + d) * S;
+  const int la = S - (m + 1 - A);  // accepted entries (>= W - 1)
+  uint16_t hist[kConvMaxS];
+#pragma unroll
+  for (int j = 0; j < kConvMaxS; ++j)
+    if (j < la) hist[j] = srow[j];
+  float wf[kConvMaxW];
+#pragma unroll
+  for (int j = 0; j < kConvMaxW; ++j) wf[j] = j < W ? gdn::bf2f(w[(int64_t)d * W + j]) : 0.f;
+  const float b0 = bias ? gdn::bf2f(bias[d]) : 0.f;
+  auto at = [&](int p) -> uint16_t { return p < la ? hist[p] : x[(int64_t)(t0 + p - la) * dim + d]; };
+  const int nt = t1 - t0;
+  for (int i = 0; i < nt; ++i) {
+    float acc = b0;
+#pragma unroll
+    for (int j = 0; j < kConvMaxW; ++j)
+      if (j < W) acc = fmaf(wf[j], gdn::bf2f(at(la - (W - 1) + i + j)), acc);
+    out[(int64_t)(t0 + i) * dim + d] = gdn::f2bf(conv_act(acc, act));
+  }
+  const int len = la + nt;
+  for (int k = 0; k < S; ++k) {
+    const int p = len - S + k;
+    srow[k] = p < 0 ? (uint16_t)0 : at(p);
+  }
+}
+
 bool conv_dims_ok(int dim, int W, int S) {
   return dim > 0 && W >= 1 && W <= kConvMaxW && S >= W - 1 && S >= 1 && S <= kConvMaxS;
 }
@@ -295,6 +352,23 @@ int gdn_causal_conv1d_update(const uint16_t *x, uint16_t *conv_state, int P, int
   conv_update_kernel<<<dim3((dim + 255) / 256, R), 256, 0, static_cast<cudaStream_t>(stream)>>>(
       x, conv_state, P, state_len, weight, bias, conv_state_indices, dim, width, activation, out, out, out, dim,
       dim, dev_status);
+  return cuda_rc(cudaGetLastError());
+}
+
+int gdn_causal_conv1d_update_spec(const uint16_t *x, uint16_t *conv_state, int P, int state_len,
+                                  const uint16_t *weight, const uint16_t *bias, const int32_t *conv_state_indices,
+                                  const int32_t *num_accepted_tokens, const int32_t *query_start_loc, int N,
+                                  int Ttot, int mtp_step, int dim, int width, int activation, uint16_t *out,
+                                  int32_t *dev_status, void *stream) {
+  if (N < 0 || P < 0 || Ttot < 0 || dim <= 0 || mtp_step < 0 || (activation != 0 && activation != 1))
+    return GDN_EINVAL;
+  if (!conv_dims_ok(dim, width, state_len) || state_len < width - 1 + mtp_step) return GDN_EUNSUPPORTED;
+  if (N == 0) return GDN_OK;
+  if (N > 65535) return GDN_EUNSUPPORTED;
+  if (!x || !conv_state || !weight || !conv_state_indices || !query_start_loc || !out) return GDN_EINVAL;
+  conv_update_spec_kernel<<<dim3((dim + 255) / 256, N), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      x, conv_state, P, state_len, weight, bias, conv_state_indices, num_accepted_tokens, query_start_loc, Ttot,
+      mtp_step, dim, width, activation, out, dev_status);
   return cuda_rc(cudaGetLastError());
 }
 

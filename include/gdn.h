@@ -391,6 +391,42 @@ int gdn_causal_conv1d_update(const uint16_t *x, uint16_t *conv_state, int P, int
                              int activation, uint16_t *out, int32_t *dev_status, void *stream);
 
 /*
+ * gdn_causal_conv1d_update_spec -- the decode conv of multi-token (speculative
+ * / MTP) decoding.  LightLLM "gdn.py", _gdn_mtp_kernel (causal_conv1d_update
+ * called with mtp_step, num_accepted_tokens and query_start_loc) and its
+ * prefill path, which slices the last mtp_step entries off each conv state.
+ *   x                   : [Ttot, dim] token-major; request n owns rows
+ *                         [query_start_loc[n], query_start_loc[n + 1]), at most
+ *                         mtp_step + 1 of them (else GDN_DEV_BAD_CU_SEQLENS and
+ *                         the request is skipped)
+ *   conv_state          : [P, dim, state_len], read and written in place;
+ *                         state_len >= width - 1 + mtp_step
+ *   conv_state_indices  : int32 [N] slot per request (-1: PAD)
+ *   num_accepted_tokens : int32 [N] in [1, mtp_step + 1], or NULL (all 1);
+ *                         other values set GDN_DEV_BAD_SLOT and the request is
+ *                         treated like PAD
+ *   query_start_loc     : int32 [N + 1] device offsets
+ *   out                 : [Ttot, dim]
+ * Reading (the page gives the call, not the arithmetic): a slot holds the last
+ * state_len inputs of its request's stream as of the previous step, whose last
+ * mtp_step + 1 entries were that step's tokens; only the first A =
+ * num_accepted_tokens of them were accepted, so the accepted stream is the
+ * first state_len - (mtp_step + 1 - A) entries.  The request's tokens follow it
+ * (each output uses the width - 1 inputs before it, as in the single-token
+ * update), and the slot then holds the last state_len entries of accepted ++
+ * tokens.  After a prefill that wrote the first width - 1 entries (the page's
+ * sliced view), A = 1 reads exactly those.  mtp_step = 0 with one token is
+ * gdn_causal_conv1d_update.  PAD and bad slots as in gdn_causal_conv1d_update.
+ * N > 65535 returns GDN_EUNSUPPORTED.  One launch.
+ */
+int gdn_causal_conv1d_update_spec(const uint16_t *x, uint16_t *conv_state, int P, int state_len,
+                                  const uint16_t *weight, const uint16_t *bias,
+                                  const int32_t *conv_state_indices, const int32_t *num_accepted_tokens,
+                                  const int32_t *query_start_loc, int N, int Ttot, int mtp_step, int dim,
+                                  int width, int activation, uint16_t *out, int32_t *dev_status,
+                                  void *stream);
+
+/*
  * gdn_conv_decode_pack -- gdn_causal_conv1d_update over the packed channels
  * [q (H*K) | k (H*K) | v (HV*V)] (dim = 2*H*K + HV*V) of mixed_qkv [R, dim],
  * writing the three channel ranges straight into the layouts

@@ -142,3 +142,58 @@ def conv_decode_pack(mixed_qkv, conv_state, weight, bias, conv_state_indices, H,
     k = out[:, H * K:2 * H * K].reshape(R, 1, H, K)
     v = out[:, 2 * H * K:2 * H * K + HV * V].reshape(R, 1, HV, V)
     return q, k, v, states
+
+
+def causal_conv1d_update_spec(x, conv_state, weight, bias, conv_state_indices, num_accepted_tokens,
+                              query_start_loc, mtp_step, activation="silu"):
+    """Multi-token (speculative / MTP) decode conv, the ``causal_conv1d_update``
+    of LightLLM "gdn.py" ``_gdn_mtp_kernel`` (called with ``mtp_step``,
+    ``num_accepted_tokens`` and ``query_start_loc``).
+
+    x                   : [Ttot, dim] token-major; request n owns rows
+                          [query_start_loc[n], query_start_loc[n + 1]), at most
+                          mtp_step + 1 of them
+    conv_state          : [P, dim, S] pool, S >= W - 1 + mtp_step (the page keeps
+                          mtp_step extra entries per slot and slices them off for
+                          prefill); not modified, the new pool is returned
+    conv_state_indices  : [N] slot per request (-1: PAD, zero outputs, no write)
+    num_accepted_tokens : [N] in [1, mtp_step + 1], or None (all 1)
+
+    Reading (the page gives the call, not the arithmetic): a slot holds the last
+    S entries of its request's input stream as of the end of the previous step,
+    whose last mtp_step + 1 entries were that step's tokens; only the first A =
+    num_accepted_tokens of those were accepted, so the last (mtp_step + 1 - A)
+    entries are rejected drafts.  The accepted stream is slot[:S - (mtp_step + 1
+    - A)]; the new tokens follow it, each output uses the W - 1 inputs before it
+    (out[i] = act(bias + sum_j weight[:, j] * stream[i + j]) over the last W - 1
+    accepted entries ++ x), and afterwards the slot holds the last S entries of
+    accepted ++ x (zeros in front if that is shorter).  After a prefill, which
+    writes slot[:W - 1] through the sliced view, A = 1 selects exactly those
+    entries.  returns (out [Ttot, dim], new_states [P, dim, S]).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    weight = np.asarray(weight, dtype=np.float64)
+    states = np.array(conv_state, dtype=np.float64, copy=True)
+    Ttot, dim = x.shape
+    W = weight.shape[1]
+    S = states.shape[2]
+    m = int(mtp_step)
+    if S < W - 1 + m:
+        raise ValueError("state length must hold W - 1 + mtp_step entries")
+    out = np.zeros((Ttot, dim), dtype=np.float64)
+    qsl = [int(v) for v in query_start_loc]
+    for n in range(len(qsl) - 1):
+        t0, t1 = qsl[n], qsl[n + 1]
+        slot = int(conv_state_indices[n])
+        if slot == PAD_SLOT:
+            continue
+        A = 1 if num_accepted_tokens is None else int(num_accepted_tokens[n])
+        accepted = states[slot][:, :S - (m + 1 - A)]
+        new = x[t0:t1].T                                     # [dim, n_tokens]
+        stream = np.concatenate([accepted[:, accepted.shape[1] - (W - 1):], new], axis=1)
+        out[t0:t1] = conv_stream(stream, weight, bias, activation).T
+        whole = np.concatenate([accepted, new], axis=1)
+        if whole.shape[1] < S:
+            whole = np.concatenate([np.zeros((dim, S - whole.shape[1])), whole], axis=1)
+        states[slot] = whole[:, whole.shape[1] - S:]
+    return out, states

@@ -245,3 +245,19 @@ def test_wait_expiry_hook_toggles(lib):
     assert lib.gdn_testing_force_wait_expiry(1) == 0
     assert gdn.testing_force_wait_expiry(False) is True
     assert lib.gdn_testing_force_wait_expiry(0) == 0
+
+
+def test_conv_spec_host_validation(lib):
+    NULL = None
+    fake = ctypes.c_void_p(16)
+
+    def call(S=6, m=3, Wd=4, N=2, x=fake, qsl=fake):
+        return lib.gdn_causal_conv1d_update_spec(x, fake, 4, S, fake, NULL, fake, NULL, qsl, N, 8, m, 64, Wd, 1,
+                                                 fake, NULL, NULL)
+
+    assert call(N=0) == gdn.GDN_OK
+    assert call(S=5) == gdn.GDN_EUNSUPPORTED        # state too short for width - 1 + mtp_step
+    assert call(m=-1) == gdn.GDN_EINVAL
+    assert call(x=NULL) == gdn.GDN_EINVAL
+    assert call(qsl=NULL) == gdn.GDN_EINVAL
+    assert call(N=70000) == gdn.GDN_EUNSUPPORTED

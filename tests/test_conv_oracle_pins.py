@@ -170,3 +170,94 @@ def test_decode_pack_splits_q_k_v_in_channel_order():
     np.testing.assert_array_equal(v[:, 0].reshape(R, -1), out[:, 2 * H * K:])
     np.testing.assert_array_equal(new, new2)
     assert q[0, 0, 1, 2] == out[0, 1 * K + 2]
+
+
+# ------------------------------------------------------------ MTP decode conv
+
+def _spec_case(seed, N, m, dim, W, S, A=None):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal(((m + 1) * N, dim))
+    weight = rng.uniform(-0.5, 0.5, (dim, W))
+    bias = rng.normal(0, 0.1, dim)
+    states = rng.standard_normal((N + 2, dim, S))
+    qsl = np.arange(0, (m + 1) * N + 1, m + 1)
+    acc = np.asarray(A if A is not None else rng.integers(1, m + 2, N))
+    return x, weight, bias, states, qsl, acc
+
+
+def test_spec_with_no_draft_is_the_single_token_update():
+    """mtp_step = 0, one token, one accepted: exactly causal_conv1d_update."""
+    x, w, b, st, qsl, _ = _spec_case(1, 5, 0, 6, 4, 3)
+    idx = np.array([3, 0, -1, 4, 1])
+    o1, s1 = CO.causal_conv1d_update_spec(x, st, w, b, idx, np.ones(5, int), qsl, 0)
+    o2, s2 = CO.causal_conv1d_update(x, st, w, b, idx)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(s1, s2)
+
+
+def test_spec_all_accepted_continues_the_plain_stream():
+    """Two MTP steps with every token accepted give the plain stream's outputs
+    and leave the plain stream's last S inputs in the slot."""
+    m, W, dim = 3, 4, 5
+    S = W - 1 + m
+    rng = np.random.default_rng(2)
+    hist = rng.standard_normal((dim, S))
+    x1, x2 = rng.standard_normal((m + 1, dim)), rng.standard_normal((m + 1, dim))
+    w, b = rng.uniform(-0.5, 0.5, (dim, W)), rng.normal(0, 0.1, dim)
+    st = hist[None].copy()
+    qsl = np.array([0, m + 1])
+    o1, st = CO.causal_conv1d_update_spec(x1, st, w, b, [0], [m + 1], qsl, m)
+    o2, st = CO.causal_conv1d_update_spec(x2, st, w, b, [0], [m + 1], qsl, m)
+    # the first step starts from a slot whose last m + 1 entries were all accepted
+    stream = np.concatenate([hist[:, S - (W - 1):], x1.T, x2.T], axis=1)
+    ref = CO.conv_stream(stream, w, b, "silu")
+    np.testing.assert_allclose(np.concatenate([o1, o2]).T, ref, rtol=1e-13, atol=1e-13)
+    whole = np.concatenate([hist, x1.T, x2.T], axis=1)
+    np.testing.assert_array_equal(st[0], whole[:, -S:])
+
+
+def test_spec_rejected_drafts_never_reach_later_outputs():
+    """Speculative decoding's defining property: after a step of m + 1 tokens of
+    which A were accepted, the next step's outputs equal those of a plain stream
+    that only ever saw the A accepted tokens."""
+    m, W, dim = 3, 4, 6
+    S = W - 1 + m
+    rng = np.random.default_rng(3)
+    w, b = rng.uniform(-0.5, 0.5, (dim, W)), rng.normal(0, 0.1, dim)
+    hist = rng.standard_normal((dim, W - 1))
+    for A in range(1, m + 2):
+        x1, x2 = rng.standard_normal((m + 1, dim)), rng.standard_normal((m + 1, dim))
+        # a slot as prefill leaves it: the first W - 1 entries, then m unused ones
+        st = np.concatenate([hist, rng.standard_normal((dim, m)) * 1e6], axis=1)[None]
+        qsl = np.array([0, m + 1])
+        _, st = CO.causal_conv1d_update_spec(x1, st, w, b, [0], [1], qsl, m)
+        o2, _ = CO.causal_conv1d_update_spec(x2, st, w, b, [0], [A], qsl, m)
+        stream = np.concatenate([hist, x1[:A].T, x2.T], axis=1)
+        ref = CO.conv_stream(stream, w, b, "silu")[:, A:]
+        np.testing.assert_allclose(o2.T, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_spec_after_prefill_reads_only_the_prefill_state():
+    """num_accepted = 1 on a freshly prefilled slot (prefill writes slot[:W - 1]
+    through the sliced view) ignores the mtp_step unused entries."""
+    m, W, dim = 2, 4, 3
+    rng = np.random.default_rng(4)
+    w, b = rng.uniform(-0.5, 0.5, (dim, W)), None
+    prefill_state = rng.standard_normal((dim, W - 1))
+    junk = rng.standard_normal((dim, m)) * 1e9
+    st = np.concatenate([prefill_state, junk], axis=1)[None]
+    x = rng.standard_normal((m + 1, dim))
+    o, _ = CO.causal_conv1d_update_spec(x, st, w, b, [0], [1], [0, m + 1], m, activation=None)
+    ref = CO.conv_stream(np.concatenate([prefill_state, x.T], axis=1), w, b, None)
+    np.testing.assert_allclose(o.T, ref, rtol=1e-13, atol=1e-13)
+
+
+def test_spec_pad_request_and_linearity():
+    x, w, b, st, qsl, acc = _spec_case(5, 4, 2, 5, 3, 5)
+    idx = np.array([1, -1, 0, 3])
+    o, s = CO.causal_conv1d_update_spec(x, st, w, None, idx, acc, qsl, 2, activation=None)
+    assert (o[qsl[1]:qsl[2]] == 0).all()
+    np.testing.assert_array_equal(s[[2, 4, 5]], st[[2, 4, 5]])      # untouched slots
+    o2, s2 = CO.causal_conv1d_update_spec(2 * x, 2 * st, w, None, idx, acc, qsl, 2, activation=None)
+    np.testing.assert_allclose(o2, 2 * o, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(s2[[0, 1, 3]], 2 * s[[0, 1, 3]], rtol=1e-13, atol=1e-13)

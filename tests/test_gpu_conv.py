@@ -175,3 +175,71 @@ def test_prefill_then_decode_continue_the_same_stream():
     assert torch.equal(out_a, out_b[:, :T])
     assert torch.equal(dec[0], out_b[:, T])
     assert torch.equal(st_a, st_b)
+
+
+# ------------------------------------------------------------ MTP decode conv
+
+def _spec_inputs(seed, N, m, P, dim, Wd, S, short=True, pad=True):
+    gen = torch.Generator().manual_seed(seed)
+    lens = [m + 1 if not (short and n % 3 == 2) else max(1, m - 1) for n in range(N)]
+    qsl = torch.tensor(W.cu_from_lengths(lens), dtype=torch.int32)
+    Tt = int(qsl[-1])
+    x = torch.randn(Tt, dim, generator=gen).to(torch.bfloat16)
+    weight = (torch.rand(dim, Wd, generator=gen) - 0.5).to(torch.bfloat16)
+    bias = (torch.randn(dim, generator=gen) * 0.1).to(torch.bfloat16)
+    states = torch.randn(P, dim, S, generator=gen).to(torch.bfloat16)
+    idx = torch.randperm(P, generator=gen)[:N].to(torch.int32)
+    if pad:
+        idx[1] = -1
+    acc = torch.randint(1, m + 2, (N,), generator=gen, dtype=torch.int32)
+    return x, weight, bias, states, idx, acc, qsl
+
+
+@pytest.mark.parametrize("N,m,P,dim,Wd,S", [(12, 3, 20, 200, 4, 6), (7, 1, 9, 64, 4, 8), (256, 3, 512, 1024, 4, 6)])
+def test_spec_decode_update_matches_oracle(N, m, P, dim, Wd, S):
+    x, w, b, st, idx, acc, qsl = _spec_inputs(70 + N, N, m, P, dim, Wd, S)
+    states = st.to(DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = gdn.gdn_causal_conv1d_update_spec(x.to(DEV), states, w.to(DEV), b.to(DEV), idx.to(DEV), acc.to(DEV),
+                                            qsl.to(DEV), m, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref_out, ref_states = CO.causal_conv1d_update_spec(f64(x), f64(st), f64(w), f64(b), idx.numpy(), acc.numpy(),
+                                                       qsl.numpy(), m)
+    close(out, ref_out)
+    np.testing.assert_array_equal(f64(states), ref_states)   # every slot, bit for bit
+    assert torch.all(out[int(qsl[1]):int(qsl[2])] == 0)       # the PAD request
+
+
+def test_spec_decode_two_steps_carry_the_accepted_stream():
+    """Two MTP steps in a row on the device against two oracle steps (the second
+    step's accepted counts locate the history inside the first step's state)."""
+    N, m, P, dim, Wd, S = 16, 3, 24, 256, 4, 6
+    x1, w, b, st, idx, acc1, qsl = _spec_inputs(81, N, m, P, dim, Wd, S, short=False, pad=False)
+    x2 = torch.randn(tuple(x1.shape), generator=torch.Generator().manual_seed(82)).to(torch.bfloat16)
+    acc2 = torch.randint(1, m + 2, (N,), generator=torch.Generator().manual_seed(83), dtype=torch.int32)
+    states = st.to(DEV)
+    o1 = gdn.gdn_causal_conv1d_update_spec(x1.to(DEV), states, w.to(DEV), b.to(DEV), idx.to(DEV), acc1.to(DEV),
+                                           qsl.to(DEV), m)
+    o2 = gdn.gdn_causal_conv1d_update_spec(x2.to(DEV), states, w.to(DEV), b.to(DEV), idx.to(DEV), acc2.to(DEV),
+                                           qsl.to(DEV), m)
+    torch.cuda.synchronize()
+    r1, rs = CO.causal_conv1d_update_spec(f64(x1), f64(st), f64(w), f64(b), idx.numpy(), acc1.numpy(), qsl.numpy(), m)
+    r2, rs = CO.causal_conv1d_update_spec(f64(x2), rs, f64(w), f64(b), idx.numpy(), acc2.numpy(), qsl.numpy(), m)
+    close(o1, r1)
+    close(o2, r2)
+    np.testing.assert_array_equal(f64(states), rs)
+
+
+def test_spec_decode_bad_counts_flagged():
+    x, w, b, st, idx, acc, qsl = _spec_inputs(91, 5, 2, 8, 32, 4, 5, short=False, pad=False)
+    acc[3] = 0                                             # outside [1, m + 1]: treated as PAD
+    bad_q = qsl.clone()
+    states = st.to(DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = gdn.gdn_causal_conv1d_update_spec(x.to(DEV), states, w.to(DEV), b.to(DEV), idx.to(DEV), acc.to(DEV),
+                                            bad_q.to(DEV), 2, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & gdn.DEV_BAD_SLOT
+    assert torch.all(out[int(qsl[3]):int(qsl[4])] == 0)
+    assert torch.equal(states[int(idx[3])].cpu(), st[int(idx[3])])
