@@ -35,12 +35,31 @@ __device__ __forceinline__ float softplus_f(float x) {
 
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + expf(-x)); }
 
-// The same two functions with the hardware exponential (a relative error of a
-// few ulp in e^x moves log1p(e^x) and 1 / (1 + e^-x) by less than that, far
+// The same two functions in a few fused multiply-adds, for the streaming gate
+// kernels.  softplus(x) = max(x, 0) + log1p(e^-|x|), and for y = e^-|x| in
+// (0, 1], log1p(y) = 2 artanh(s) with s = y / (2 + y) in (0, 1/3], taken as
+// the odd Taylor series of artanh, 2 s (1 + s^2/3 + s^4/5 + ... + s^14/15):
+// the first omitted term is below 1e-9 of the sum.  The exponential is the
+// hardware one and the divisions are the fast ones (errors of a few ulp, far
 // inside the 1e-5 relative budget of the gates).  gdn_gating and the fused
 // gating of the prefill both use these, so their gates agree bit for bit.
-__device__ __forceinline__ float softplus_fast(float x) { return x > 20.f ? x : log1pf(__expf(x)); }
-__device__ __forceinline__ float sigmoid_fast(float x) { return 1.f / (1.f + __expf(-x)); }
+__device__ __forceinline__ float log1p_unit(float y) {  // y in [0, 1]
+  const float s = __fdividef(y, 2.f + y);
+  const float t = s * s;
+  float p = 1.f / 15.f;
+  p = fmaf(p, t, 1.f / 13.f);
+  p = fmaf(p, t, 1.f / 11.f);
+  p = fmaf(p, t, 1.f / 9.f);
+  p = fmaf(p, t, 1.f / 7.f);
+  p = fmaf(p, t, 1.f / 5.f);
+  p = fmaf(p, t, 1.f / 3.f);
+  p = fmaf(p, t, 1.f);
+  return 2.f * s * p;
+}
+__device__ __forceinline__ float softplus_fast(float x) {
+  return x > 20.f ? x : fmaxf(x, 0.f) + log1p_unit(__expf(-fabsf(x)));
+}
+__device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
 
 __device__ __forceinline__ void set_status(int32_t *st, int bits) {
   if (st) atomicOr(st, bits);

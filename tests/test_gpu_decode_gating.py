@@ -121,3 +121,16 @@ def test_decode_bad_slot_flagged_and_skipped():
     assert (o[1:].float() == 0).all()
     assert torch.equal(pool[1:], before[1:])
     assert not torch.equal(pool[0], before[0])
+
+
+def test_gating_accuracy_sweep():
+    """g and beta over a dense sweep of a + dt_bias in [-40, 40] (both softplus
+    branches, the far tails where softplus(x) ~ e^x and ~ x) against fp64."""
+    x = torch.linspace(-40.0, 40.0, 8 * 65536).to(torch.bfloat16).reshape(-1, 8)
+    A_log = torch.log(torch.linspace(1.0, 16.0, 8))
+    dt = torch.zeros(8)
+    g, beta = _gdn().gdn_gating(A_log.cuda(), x.cuda(), x.cuda(), dt.cuda())
+    torch.cuda.synchronize()
+    g_ref, b_ref = oracle.gating(A_log, x, x, dt)
+    np.testing.assert_allclose(g.cpu().numpy(), g_ref, rtol=P.GATE_RTOL, atol=P.GATE_ATOL)
+    np.testing.assert_allclose(beta.cpu().numpy(), b_ref, rtol=P.GATE_RTOL, atol=P.GATE_ATOL)
