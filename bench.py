@@ -74,6 +74,24 @@ def prefill_flops(tokens, H, HV, K, V):
     return tokens * HV * per
 
 
+def backward_bytes(B, T, H, HV, K, V, N):
+    """Algorithmic bytes of gdn_chunk_bwd: reads q, k, v, g, beta, do (bf16 /
+    fp32 as the entry point takes them), h0 and dht; writes dq, dk, dv, dg,
+    dbeta (fp32) and dh0.  Saved states and records are not algorithmic."""
+    tok = B * T
+    rd = tok * (2 * H * K * 2 + HV * V * 2 + 2 * HV * 4 + HV * V * 2)
+    wr = tok * (2 * H * K * 4 + HV * V * 4 + 2 * HV * 4)
+    st = N * HV * K * V * 4
+    return rd + wr + 3 * st
+
+
+def backward_flops(tokens, H, HV, K, V):
+    """Every product of the forward's flop count has two gradient products
+    (one per input), so the backward's own work is twice the forward's
+    (the forward recompute inside gdn_chunk_bwd is not counted)."""
+    return 2 * prefill_flops(tokens, H, HV, K, V)
+
+
 def gating_bytes(n_elem):
     return n_elem * (2 + 2 + 4 + 4)
 
@@ -323,7 +341,7 @@ def run_ours(args, rank, world, local_rank):
         line["gating"] = bench_gating(dev, stream, hbm, args)
         line["conv1d"] = bench_conv(dev, stream, hbm, args)
         line["decode_variants"] = bench_decode_variants(dev, stream, hbm, args)
-        line["backward"] = bench_backward(dev, stream, args)
+        line["backward"] = bench_backward(dev, stream, args, hbm, bf16_burst)
         line["fused_gating"] = bench_fused_gating(dev, stream, args,
                                                   (q, k, v, A_log, a, b, dt_bias, h0, o, ht, ws, B, T, HV))
         line["e2e"] = bench_e2e(case, dev, stream, args, world)
@@ -520,7 +538,7 @@ def bench_conv(dev, stream, hbm, args):
                        "achieved_GBps": bytes_d / (ms_d / 1e3) / 1e9}}
 
 
-def bench_backward(dev, stream, args):
+def bench_backward(dev, stream, args, hbm=None, bf16=None):
     """gdn_chunk_bwd on the dense prefill (B=2, T=4096, H=16, HV=32, K=V=128,
     initial state and final-state gradient): forward recompute, state-gradient
     walk and per-chunk gradients, timed together."""
@@ -553,9 +571,17 @@ def bench_backward(dev, stream, args):
         times.append(e0.elapsed_time(e1))
     ms = statistics.median(times)
     tokens = case.B * case.T
-    return {"workload": f"backward B={case.B} T={case.T} H={case.H} HV={case.HV} K={case.K} V={case.V}, "
-                        "initial state, final-state gradient, forward recomputed inside",
-            "ms": ms, "tokens_per_s": tokens / (ms / 1e3)}
+    out = {"workload": f"backward B={case.B} T={case.T} H={case.H} HV={case.HV} K={case.K} V={case.V}, "
+                       "initial state, final-state gradient, forward recomputed inside",
+           "ms": ms, "tokens_per_s": tokens / (ms / 1e3)}
+    if hbm and bf16:
+        ab = backward_bytes(case.B, case.T, case.H, case.HV, case.K, case.V, case.N)
+        af = backward_flops(tokens, case.H, case.HV, case.K, case.V)
+        roof_ms = max(ab / (hbm * 1e9), af / (bf16 * 1e12)) * 1e3
+        out.update({"alg_bytes": ab, "alg_flops": af, "roofline_ms": roof_ms,
+                    "bound": "hbm" if ab / (hbm * 1e9) >= af / (bf16 * 1e12) else "tensor",
+                    "frac": roof_ms / ms})
+    return out
 
 
 def bench_fused_gating(dev, stream, args, bufs):
