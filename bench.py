@@ -379,34 +379,28 @@ def bench_decode(dev, stream, hbm, args):
     A_log, a, b, dt = d(dc.A_log), d(dc.a), d(dc.b), d(dc.dt_bias)
     pool = d(dc.ssm_pool)
     o = torch.empty(dc.R, 1, dc.HV, dc.V, dtype=torch.bfloat16, device=dev)
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)  # 256 MB > L2
-
-    def call():
-        gdn.gdn_recurrent_decode(q, k, v, pool, idx, A_log=A_log, a=a, b=b, dt_bias=dt, o=o)
-    for _ in range(3):
-        call()
-    times = []
-    for _ in range(max(args.steps, 10)):
-        flush.zero_()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        call()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        times.append(e0.elapsed_time(e1))
-    ms = statistics.median(times)
+    ms = _timed_flush(dev, stream, lambda: gdn.gdn_recurrent_decode(
+        q, k, v, pool, idx, A_log=A_log, a=a, b=b, dt_bias=dt, o=o), max(args.steps, 10))
     valid = int((dc.ssm_indices >= 0).sum())
     state_b = 2 * valid * dc.HV * dc.K * dc.V * 4
     io_b = dc.R * (2 * dc.H * dc.K * 2 + dc.HV * dc.V * 2 * 2 + dc.HV * 2 * 2) + dc.R * 4
     gbs = (state_b + io_b) / (ms / 1e3) / 1e9
     return {"workload": "decode R=256 (valid %d) pool [512,32,128,128] fp32, fused gating" % valid,
             "ms": ms, "state_GBps": state_b / (ms / 1e3) / 1e9, "achieved_GBps": gbs, "peak": hbm,
-            "frac": gbs / hbm, "requests_per_s": dc.R / (ms / 1e3), "l2_flush": "256 MB memset before each call"}
+            "frac": gbs / hbm, "requests_per_s": dc.R / (ms / 1e3), "l2_flush": FLUSH_NOTE}
+
+
+FLUSH_NOTE = "512 MB memset before each timed call"
 
 
 def _timed_flush(dev, stream, call, reps):
+    """Median device time of one call.  A 512 MB memset (> L2) runs before
+    every timed call: the call starts with a cold L2, and the host finishes
+    launching it while the memset still occupies the GPU, so the events
+    bracket the kernels only (a short kernel timed alone would otherwise
+    include the host's launch overhead)."""
     import torch
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)  # 256 MB > L2
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     for _ in range(3):
         call()
     times = []
@@ -475,20 +469,10 @@ def bench_gating(dev, stream, hbm, args):
     dt = torch.zeros(HV, device=dev)
     g = torch.empty(n_tok, HV, device=dev)
     be = torch.empty(n_tok, HV, device=dev)
-    for _ in range(3):
-        gdn.gdn_gating(A_log, a, b, dt, g=g, beta=be)
-    times = []
-    for _ in range(max(args.steps, 10)):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        gdn.gdn_gating(A_log, a, b, dt, g=g, beta=be)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        times.append(e0.elapsed_time(e1))
-    ms = statistics.median(times)
+    ms = _timed_flush(dev, stream, lambda: gdn.gdn_gating(A_log, a, b, dt, g=g, beta=be), max(args.steps, 10))
     gbs = gating_bytes(n_tok * HV) / (ms / 1e3) / 1e9
-    return {"workload": f"gating {n_tok}x{HV} (bf16 a,b -> fp32 g,beta; 200 MB in+out > L2)",
-            "ms": ms, "achieved_GBps": gbs, "peak": hbm, "frac": gbs / hbm}
+    return {"workload": f"gating {n_tok}x{HV} (bf16 a,b -> fp32 g,beta; 200 MB in+out)",
+            "ms": ms, "achieved_GBps": gbs, "peak": hbm, "frac": gbs / hbm, "l2_flush": FLUSH_NOTE}
 
 
 def bench_conv(dev, stream, hbm, args):
@@ -501,17 +485,7 @@ def bench_conv(dev, stream, hbm, args):
     d = lambda t: t.to(dev).contiguous()
 
     def timed(fn, reps):
-        for _ in range(3):
-            fn()
-        times = []
-        for _ in range(reps):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            fn()
-            e1.record(stream)
-            torch.cuda.synchronize(dev)
-            times.append(e0.elapsed_time(e1))
-        return statistics.median(times)
+        return _timed_flush(dev, stream, fn, reps)
 
     pc = W.conv_prefill_long()
     x, w, b, st = d(pc.x), d(pc.weight), d(pc.bias), d(pc.conv_states)
@@ -559,21 +533,11 @@ def bench_backward(dev, stream, args, hbm=None, bf16=None):
 
     def call():
         gdn.gdn_chunk_bwd(q, k, v, g, beta, do, initial_state=h0, dht=dht, workspace=ws)
-    for _ in range(3):
-        call()
-    times = []
-    for _ in range(max(args.steps, 5)):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        call()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        times.append(e0.elapsed_time(e1))
-    ms = statistics.median(times)
+    ms = _timed_flush(dev, stream, call, max(args.steps, 5))
     tokens = case.B * case.T
     out = {"workload": f"backward B={case.B} T={case.T} H={case.H} HV={case.HV} K={case.K} V={case.V}, "
                        "initial state, final-state gradient, forward recomputed inside",
-           "ms": ms, "tokens_per_s": tokens / (ms / 1e3)}
+           "ms": ms, "tokens_per_s": tokens / (ms / 1e3), "l2_flush": FLUSH_NOTE}
     if hbm and bf16:
         ab = backward_bytes(case.B, case.T, case.H, case.HV, case.K, case.V, case.N)
         af = backward_flops(tokens, case.H, case.HV, case.K, case.V)
@@ -596,17 +560,7 @@ def bench_fused_gating(dev, stream, args, bufs):
     def call():
         gdn.gdn_chunk_fwd_gated(q, k, v, A_log, a3, b3, dt_bias, initial_state=h0, o=o, final_state=ht,
                                 workspace=ws)
-    for _ in range(3):
-        call()
-    times = []
-    for _ in range(max(args.steps, 5)):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        call()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        times.append(e0.elapsed_time(e1))
-    ms = statistics.median(times)
+    ms = _timed_flush(dev, stream, call, max(args.steps, 5))
     return {"workload": f"long-context prefill B={B} T={T}, gating fused (gdn_chunk_fwd_gated)",
             "ms": ms, "tokens_per_s": B * T / (ms / 1e3), "launches": 2}
 
