@@ -71,11 +71,6 @@ struct KQ {
 __device__ __forceinline__ unsigned char *align1024(unsigned char *p) {
   return reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
 }
-// Address of the 16-byte chunk holding keys [8 kc, 8 kc + 8) of row `row` in a
-// [rows][K] bf16 tile stored as 64-key SW128 atom columns of `rows` rows.
-__device__ __forceinline__ uint32_t tile_addr(uint32_t base, int rows, int row, int kc) {
-  return base + (kc >> 3) * (rows * 128) + sw128(row, kc & 7);
-}
 // acc (16 x 16 as two 16x8 tiles) += A (16 x 16) * B (16 x 16), fp32 row-major in
 // shared memory; fp32 bits go straight to the tf32 unit (low mantissa bits ignored).
 __device__ __forceinline__ void mm16_tf32(const float *A, int lda, const float *B, int ldb, float acc[2][4], int g4,
@@ -287,8 +282,7 @@ __global__ void __launch_bounds__(NTH, 4) chunk_prep_kernel(
     }
   }
   tc_fence_before();
-  __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 128);  // every TMEM read is done
+  __syncthreads();  // every read of [K;Q][K;Q]^T from TMEM is done: W reuses the columns
 
   // Per-row factors; the decay e^{gamma_i-gamma_j} is factored when the chunk's
   // total decay fits the fp32 range, else taken element by element.
@@ -475,41 +469,53 @@ __global__ void __launch_bounds__(NTH, 4) chunk_prep_kernel(
   }
   __syncthreads();
 
-  // W = Tp K (64 x K): warp -> 16 rows (mi) x half of the keys (nh), in two
-  // passes of a quarter of the keys each (fewer live accumulators).
-  {
-    const int mi = warp & 3, nh = warp >> 2;
-    constexpr int WN = K / 16, WQ = WN / 2;
+  // W = Tp K (64 x K) on tcgen05: A = Tp (K-major, its rows 64-127 whatever
+  // follows the tile: those accumulator lanes are not read), B = the K rows of
+  // the [K;Q] tile as an MN-major operand (keys contiguous, 64-key atoms 16 KB
+  // apart), fp32 accumulator in the TMEM columns of the first product.  The
+  // warps of TMEM lanes 0-63 turn it into the record's bf16 W, one row and
+  // 64 keys per thread, with 16-byte stores.
+  fence_proxy_async_smem();  // Tp and the zeroed K rows, for the tensor core
+  __syncthreads();
+  if (tid == 0) {
+    tc_fence_after();
+    constexpr uint32_t idw = umma_idesc_bf16(128, K, 0, 1);
 #pragma unroll
-    for (int pass = 0; pass < 2; ++pass) {
-      float acc[WQ][4];
+    for (int kk = 0; kk < 4; ++kk)
+      umma_bf16(tmem, umma_desc_sw128(sb + Ly::OFF_TP + kk * 32), umma_desc_sw128_mn(kq + kk * 2048, 16384), idw,
+                kk > 0 ? 1u : 0u);
+    umma_commit(b_mma);
+    if (!mbar_wait_bounded(b_mma, 1, kWaitLimit)) {
+      misc[1] = 1;
+      set_status(dev_status, GDN_DEV_WAIT_TIMEOUT);
+    }
+  }
+  __syncthreads();
+  if (!misc[1] && (warp & 3) < 2 && (warp >> 2) < KA) {
+    tc_fence_after();
+    const int i = 32 * (warp & 3) + lane, a = warp >> 2;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + 64 * a;
+    unsigned char *wrow = rec + R::W + a * 8192;
 #pragma unroll
-      for (int j = 0; j < WQ; ++j)
+    for (int q4 = 0; q4 < 4; ++q4) {
+      uint32_t x[16];
+      tmem_ld16_issue(tl + 16 * q4, x);
+      tmem_ld_wait16(x);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
+      for (int c2 = 0; c2 < 2; ++c2) {
+        uint32_t w[4];
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        uint32_t a[4];
-        ldsm_x4(sb + Ly::OFF_TP + sw128(16 * mi + (lane & 15), 2 * kk + (lane >> 4)), a);
-        const int mq = lane >> 3;
-        const int trow = 16 * kk + (lane & 7) + 8 * (mq & 1);
-#pragma unroll
-        for (int j = 0; j < WQ; j += 2) {
-          uint32_t b[4];
-          ldsm_x4_t(tile_addr(kq, 128, trow, nh * WN + pass * WQ + j + (mq >> 1)), b);
-          mma_bf16(acc[j], a, b[0], b[1]);
-          mma_bf16(acc[j + 1], a, b[2], b[3]);
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < WQ; ++j) {
-        const int key = 8 * (nh * WN + pass * WQ + j) + 2 * t4;
-        const int r0 = 16 * mi + g4;
-        unsigned char *base = rec + R::W + (key >> 6) * 8192 + (key & 7) * 2;
-        *reinterpret_cast<uint32_t *>(base + sw128(r0, (key & 63) >> 3)) = pack_bf16(acc[j][0], acc[j][1]);
-        *reinterpret_cast<uint32_t *>(base + sw128(r0 + 8, (key & 63) >> 3)) = pack_bf16(acc[j][2], acc[j][3]);
+        for (int e = 0; e < 4; ++e)
+          w[e] = pack_bf16(__uint_as_float(x[8 * c2 + 2 * e]), __uint_as_float(x[8 * c2 + 2 * e + 1]));
+        *reinterpret_cast<uint4 *>(wrow + sw128(i, 2 * q4 + c2)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 128);
   }
 }
 
