@@ -109,6 +109,14 @@ struct PrepLay {
   static constexpr int OFF_BAR = OFF_SC + 8 * 256;
   static constexpr int OFF_MISC = OFF_BAR + 16;
   static constexpr int BYTES = OFF_MISC + 16;
+  // Staging of the record for bulk stores (K = 128; at K = 64 P and Ts^T are
+  // stored directly): P hi and P lo in the two Q-row blocks (dead after the
+  // first product, read back by the bulk copies before Tp and the solve's
+  // scratch reuse them), Ts^T in the second Q-row block after the solve, and
+  // W in the K rows of the tile once W = Tp K has completed.
+  static constexpr int OFF_PH = 8192, OFF_PL = 16384 + 8192, OFF_TSS = 16384 + 8192;
+  static_assert(K < 128 || (OFF_PH + 8192 <= 16384 && OFF_PL + 8192 <= OFF_AT && OFF_TSS + 8192 <= OFF_AT),
+                "record staging inside the [K;Q] tile");
   static_assert(OFF_TP % 1024 == 0, "swizzled tile alignment");
   static_assert(4 * (BYTES + 1024 + 1024) <= 228 * 1024, "four CTAs per SM");
 };
@@ -156,8 +164,9 @@ __global__ void __launch_bounds__(NTH, 4) chunk_prep_kernel(
   float *rowA = scal + PS_RA * 64, *rowP = scal + PS_RP * 64, *colf = scal + PS_CF * 64, *ftp = scal + PS_FTP * 64;
   float *AT = reinterpret_cast<float *>(sm + Ly::OFF_AT);
   float *Xs = reinterpret_cast<float *>(sm + Ly::OFF_X);
-  // The record goes straight to the workspace: every byte the walk reads is
-  // written below (16-byte stores for P, Ts^T; the mma fragments of W).
+  // Every byte of the record the walk reads is written below: P, Ts^T and W
+  // through shared-memory staging and bulk stores (P and Ts^T directly at
+  // K = 64), the scalars directly.
   unsigned char *rec = ws + (static_cast<size_t>(gc) * HV + hv) * R::BYTES;
   float *rsc = reinterpret_cast<float *>(rec + R::SC);
   uint32_t *misc = reinterpret_cast<uint32_t *>(sm + Ly::OFF_MISC);
@@ -349,11 +358,24 @@ __global__ void __launch_bounds__(NTH, 4) chunk_prep_kernel(
         vl = make_uint4(pl[0], pl[1], pl[2], pl[3]);
       }
       const int chunk = half * 4 + q8;
-      *reinterpret_cast<uint4 *>(rec + R::PH + sw128(i, chunk)) = vh;
-      *reinterpret_cast<uint4 *>(rec + R::PL + sw128(i, chunk)) = vl;
+      if constexpr (K >= 128) {
+        *reinterpret_cast<uint4 *>(sm + Ly::OFF_PH + sw128(i, chunk)) = vh;
+        *reinterpret_cast<uint4 *>(sm + Ly::OFF_PL + sw128(i, chunk)) = vl;
+      } else {
+        *reinterpret_cast<uint4 *>(rec + R::PH + sw128(i, chunk)) = vh;
+        *reinterpret_cast<uint4 *>(rec + R::PL + sw128(i, chunk)) = vl;
+      }
     }
   }
+  if constexpr (K >= 128) fence_proxy_async_smem();  // P, for the bulk copies
   __syncthreads();
+  if constexpr (K >= 128) {
+    if (tid == 0) {
+      bulk_store(rec + R::PH, sb + Ly::OFF_PH, 8192);
+      bulk_store(rec + R::PL, sb + Ly::OFF_PL, 8192);
+      bulk_commit();
+    }
+  }
 
   // T = (I + A)^{-1}, in place.  Diagonal 16x16 blocks: warps 0-3, lanes 0-15,
   // one column each (right-looking substitution).  Warps 4-7 zero the K rows
@@ -377,6 +399,9 @@ __global__ void __launch_bounds__(NTH, 4) chunk_prep_kernel(
       const int zr = L + e / (8 * KA), kc = e % (8 * KA);
       *reinterpret_cast<uint4 *>(sm + Ly::OFF_KQ + (kc >> 3) * 16384 + sw128(zr, kc & 7)) = make_uint4(0, 0, 0, 0);
     }
+  }
+  if constexpr (K >= 128) {
+    if (tid == 0) bulk_wait_read();  // the solve's scratch and Tp reuse P's staging
   }
   __syncthreads();
   {
@@ -465,19 +490,25 @@ __global__ void __launch_bounds__(NTH, 4) chunk_prep_kernel(
       }
       w[q2] = pack_bf16(v2[0], v2[1]);
     }
-    *reinterpret_cast<uint4 *>(rec + R::TS + sw128(j, ich)) = make_uint4(w[0], w[1], w[2], w[3]);
+    if constexpr (K >= 128)
+      *reinterpret_cast<uint4 *>(sm + Ly::OFF_TSS + sw128(j, ich)) = make_uint4(w[0], w[1], w[2], w[3]);
+    else
+      *reinterpret_cast<uint4 *>(rec + R::TS + sw128(j, ich)) = make_uint4(w[0], w[1], w[2], w[3]);
   }
-  __syncthreads();
 
   // W = Tp K (64 x K) on tcgen05: A = Tp (K-major, its rows 64-127 whatever
   // follows the tile: those accumulator lanes are not read), B = the K rows of
   // the [K;Q] tile as an MN-major operand (keys contiguous, 64-key atoms 16 KB
   // apart), fp32 accumulator in the TMEM columns of the first product.  The
   // warps of TMEM lanes 0-63 turn it into the record's bf16 W, one row and
-  // 64 keys per thread, with 16-byte stores.
-  fence_proxy_async_smem();  // Tp and the zeroed K rows, for the tensor core
+  // 64 keys per thread, staged in the K rows for two bulk stores.
+  fence_proxy_async_smem();  // Tp, the zeroed K rows and Ts^T, for the async proxy
   __syncthreads();
   if (tid == 0) {
+    if constexpr (K >= 128) {
+      bulk_store(rec + R::TS, sb + Ly::OFF_TSS, 8192);
+      bulk_commit();
+    }
     tc_fence_after();
     constexpr uint32_t idw = umma_idesc_bf16(128, K, 0, 1);
 #pragma unroll
@@ -495,7 +526,7 @@ __global__ void __launch_bounds__(NTH, 4) chunk_prep_kernel(
     tc_fence_after();
     const int i = 32 * (warp & 3) + lane, a = warp >> 2;
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + 64 * a;
-    unsigned char *wrow = rec + R::W + a * 8192;
+    unsigned char *wrow = sm + Ly::OFF_KQ + a * 16384;  // the K rows of atom a: dead now
 #pragma unroll
     for (int q4 = 0; q4 < 4; ++q4) {
       uint32_t x[16];
@@ -510,12 +541,21 @@ __global__ void __launch_bounds__(NTH, 4) chunk_prep_kernel(
         *reinterpret_cast<uint4 *>(wrow + sw128(i, 2 * q4 + c2)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
+    fence_proxy_async_smem();  // W, for the bulk copies
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, 128);
+  }
+  if (tid == 0) {
+    if (!misc[1]) {
+#pragma unroll
+      for (int a = 0; a < KA; ++a) bulk_store(rec + R::W + a * 8192, sb + Ly::OFF_KQ + a * 16384, 8192);
+      bulk_commit();
+    }
+    bulk_wait_all();  // shared memory must outlive the copies
   }
 }
 
