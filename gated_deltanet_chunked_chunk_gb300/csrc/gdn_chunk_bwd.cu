@@ -269,16 +269,18 @@ __global__ void __launch_bounds__(BT, 1) chunk_dh_kernel(
     } else {
       cp_async_wait<0>();
     }
-    // dh' of this chunk: to the workspace and to shared memory.
+    // dh' of this chunk: to shared memory, then from there to the workspace
+    // with coalesced 16-byte stores (rows of DVC consecutive floats).
+    cvisit(dh, [&](int, int r, int cc, float x) { dhs[(dm0 + r) * Ly::BS + dc0 + cc] = x; });
+    __syncthreads();
     {
       float *dst = DH + (((cb + c) * HV + hv) * K) * (int64_t)V + vt0;
-      cvisit(dh, [&](int, int r, int cc, float x) {
-        const int row = dm0 + r, col = dc0 + cc;
-        dst[(int64_t)row * V + col] = x;
-        dhs[row * Ly::BS + col] = x;
-      });
+      for (int e = tid; e < K * (DVC / 4); e += BT) {
+        const int row = e / (DVC / 4), c4 = e % (DVC / 4);
+        *reinterpret_cast<float4 *>(dst + (int64_t)row * V + 4 * c4) =
+            *reinterpret_cast<const float4 *>(dhs + row * Ly::BS + 4 * c4);
+      }
     }
-    __syncthreads();
     const unsigned char *S = smem + st * Ly::STAGE;
     const float *sc = reinterpret_cast<const float *>(S + Ly::OFF_SC);
     const uint16_t *Ks = reinterpret_cast<const uint16_t *>(S + Ly::OFF_K);
