@@ -917,6 +917,388 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
   }
 }
 
+// -------------------------------------------- state-gradient walk, tcgen05
+// The same recurrence as chunk_dh_kernel for K = 128 and 64-column slices of
+// V, on tcgen05 with TMEM accumulators, built like the forward walk: one CTA
+// per (64-column slice, value head, sequence) walks the chunks last to first;
+// the fp32 dh' lives in registers of eight chain warps (thread = TMEM lane,
+// i.e. key, x 32 columns) and is written back as bf16 hi | lo as the B operand
+// of the next chunk's first product.  Per chunk (operands from the record and
+// raw bf16 tiles, 128-byte swizzled shared memory, fp32 accumulators):
+//   D1 = K [dh'_hi | dh'_lo]               M=128 (rows 64-127 not read) N=128, two partials (warps 0, 1)
+//   D2 = P_hi^T do + P_lo^T do             M=128 (rows 64-127 not read) N=64  (converter warp, early)
+//   dv_new = diag(sv) (D1 hi + lo) + scale D2     (rows 0-63), as bf16 hi | lo
+//   D34 = Q^T [s do_hi | s do_lo]          s = scale e^gamma / ||q||, rows >= L zero (converter, early)
+//   D34 -= W^T [dv_new hi | lo]            the A operand negated in the instruction (warp 0)
+//   dh = e^{gamma_L} dh' + D34 hi + lo
+// Rows >= L of a chunk: W, P rows are zero in the record and the scaled do
+// rows are zeroed here, so the K, Q and do rows that TMA brings in from the
+// next sequence never reach dh.
+struct DhtLay {
+  static constexpr int KT = 0;          // K tile [64 tokens][128 keys]: two 64-key atoms of 8 KB (TMA)
+  static constexpr int QT = 16384;      // Q tile, the same (TMA)
+  static constexpr int WR = 32768;      // record W | P hi | P lo (bulk, 32 KB)
+  static constexpr int PH = WR + 16384, PL = WR + 24576;
+  static constexpr int DO = 65536;      // do box [64 tokens][64 columns] (TMA)
+  static constexpr int SC = 73728;      // record scalars (1 KB)
+  static constexpr int STAGE = 74752;
+  static constexpr int OFF_H = 2 * STAGE;          // [dh'_hi | dh'_lo]: two N atoms [128 keys][64] of 16 KB
+  static constexpr int OFF_DV = OFF_H + 32768;     // [dv_new hi | lo]: two N atoms [64 tokens][64] of 8 KB
+  static constexpr int OFF_DS = OFF_DV + 16384;    // [s do hi | lo]: the same
+  static constexpr int OFF_BAR = OFF_DS + 16384;
+  static constexpr int NBAR = 16;
+  static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
+  static constexpr int BYTES = OFF_MISC + 16;
+  static constexpr uint32_t TX = 4 * 8192 + 32768 + 8192 + 1024;
+  static_assert(STAGE % 1024 == 0 && SC + 1024 <= STAGE && OFF_H % 1024 == 0, "stage layout");
+  static_assert(BYTES + 1024 <= 232448, "shared memory budget (227 KB per CTA)");
+};
+// TMEM columns.
+constexpr uint32_t DT_D1A = 0, DT_D1B = 128, DT_D2 = 256, DT_D34 = 384;
+constexpr int DT_THREADS = 10 * 32;
+enum { DB_FULL = 0, DB_EMPTY = 2, DB_D2R = 4, DB_CHD = 6, DB_M1 = 8, DB_M3 = 9, DB_D4R = 10, DB_DRAIN = 11 };
+
+__global__ void __launch_bounds__(DT_THREADS, 1) chunk_dh_tc_kernel(
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    const __grid_constant__ CUtensorMap tm_do, const unsigned char *__restrict__ ws, float *__restrict__ DH,
+    const float *__restrict__ dht, float *__restrict__ dh0, float scale, const int32_t *__restrict__ cu,
+    const int32_t *__restrict__ cs, int T, int H, int HV, int V, int32_t *dev_status) {
+  constexpr int K = 128;
+  using Ly = DhtLay;
+  using R = Rec<K>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                        ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(sm);
+  const int vt0 = blockIdx.x * DVC, hv = blockIdx.y, n = blockIdx.z;
+  const int h = hv / (HV / H);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int64_t tok0, len;
+  if (!seq_bounds(cu, n, T, tok0, len)) {
+    if (tid == 0) set_status(dev_status, GDN_DEV_BAD_CU_SEQLENS);
+    return;
+  }
+  const int NC = chunks_of(len);
+  const int64_t cb = chunk_base(cs, n, T);
+  const int64_t sbase = ((int64_t)n * HV + hv) * K;
+  uint32_t *misc = reinterpret_cast<uint32_t *>(sm + Ly::OFF_MISC);
+  volatile uint32_t *abort_flag = misc + 1;
+  auto bar = [&](int i) { return sb + Ly::OFF_BAR + 8 * i; };
+  if (tid == 0) {
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(DB_FULL + b), 1);
+      mbar_init(bar(DB_EMPTY + b), 1);
+      mbar_init(bar(DB_D2R + b), 1);
+      mbar_init(bar(DB_CHD + b), 1);
+    }
+    mbar_init(bar(DB_M1), 2);
+    mbar_init(bar(DB_M3), 1);
+    mbar_init(bar(DB_D4R), 1);
+    mbar_init(bar(DB_DRAIN), 4);  // warps 0, 1 and 9, and the producer's stand-in
+    misc[1] = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0) tmem_alloc(sb + Ly::OFF_MISC, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  bool dead = false;
+  auto waitl = [&](uint32_t b, uint32_t parity) -> bool {
+    uint32_t ok = 0;
+    if (lane == 0 && !dead) {
+      const long long t0 = clock64();
+      for (int it = 1;; ++it) {
+        if (mbar_try_wait(b, parity)) { ok = 1; break; }
+        if ((it & 63) == 0) {
+          if (*abort_flag) break;
+          if (clock64() - t0 > kWaitLimit) { *abort_flag = 1; break; }
+        }
+      }
+    }
+    __syncwarp();
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    dead = dead || !ok;
+    return ok != 0;
+  };
+  auto wait2 = [&](int slot, int it) { return waitl(bar(slot + (it & 1)), (it >> 1) & 1); };
+  auto stage = [&](int it) { return sb + (it & 1) * Ly::STAGE; };
+  auto chunk_of = [&](int it) { return NC - 1 - it; };
+  auto rows_of = [&](int c) {
+    const int64_t rem = len - (int64_t)c * C;
+    return rem < C ? (int)rem : C;
+  };
+  constexpr uint32_t ID1 = umma_idesc_bf16(128, 128, 0, 1);
+  constexpr uint32_t ID2 = umma_idesc_bf16(128, 64, 1, 1);
+  constexpr uint32_t ID4 = umma_idesc_bf16(128, 128, 1, 1);
+  constexpr uint32_t ID3N = umma_idesc_bf16(128, 128, 1, 1) | (1u << 13);  // A negated
+  int issued = 0;
+
+  if (warp < 8) {
+    // ------------------------------------------------------- chain warps
+    const int r = 32 * (warp & 3) + lane;  // TMEM lane: key (dh) or token (dv_new, r < 64)
+    const int hs = warp >> 2;              // columns 32 hs .. 32 hs + 31 of the slice
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    float dh[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) dh[j] = dht ? dht[(sbase + r) * V + vt0 + 32 * hs + j] : 0.f;
+    // Row r of a two-atom MN-major SW128 tile (atom = 64 columns): columns
+    // [32 hs, 32 hs + 32) of the hi and the lo atom.
+    auto write_split = [&](uint32_t off, int atom_bytes, const float *x) {
+      unsigned char *base = sm + off + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float x0 = x[8 * m + 2 * e], x1 = x[8 * m + 2 * e + 1];
+          hi[e] = pack_bf16(x0, x1);
+          lo[e] = pack_bf16(x0 - bf16lo_f(hi[e]), x1 - bf16hi_f(hi[e]));
+        }
+        const int chk = (4 * hs + m) ^ (r & 7);
+        *reinterpret_cast<uint4 *>(base + (chk << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4 *>(base + atom_bytes + (chk << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+    };
+    bool go = true;
+    for (int it = 0; it < NC; ++it) {
+      const int c = chunk_of(it);
+      // dh' of chunk c: to the workspace and, split, to the H tile (its last
+      // reader, the first product of the chunk before, has completed).
+      {
+        float *dst = DH + (((cb + c) * HV + hv) * K + r) * (int64_t)V + vt0 + 32 * hs;
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4 *>(dst + j) = make_float4(dh[j], dh[j + 1], dh[j + 2], dh[j + 3]);
+        write_split(Ly::OFF_H, 16384, dh);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 256);
+      go = wait2(DB_FULL, it) && go;
+      const unsigned char *scp = sm + (it & 1) * Ly::STAGE + Ly::SC;
+      const float dL = go ? reinterpret_cast<const float *>(scp)[RS_DL] : 0.f;
+      const float svr = (go && r < 64) ? reinterpret_cast<const float *>(scp)[RS_SV + r] : 0.f;
+      if (warp < 2 && lane == 0 && go) {
+        tc_fence_after();
+        const uint32_t st = stage(it);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int kk = 4 * warp + m;  // keys 16 kk .. 16 kk + 15
+          const uint64_t a = umma_desc_sw128(st + Ly::KT + (kk >> 2) * 8192 + (kk & 3) * 32);
+          const uint64_t b = umma_desc_sw128_mn(sb + Ly::OFF_H + kk * 2048, 16384);
+          umma_bf16(tmem + (warp ? DT_D1B : DT_D1A), a, b, ID1, m > 0 ? 1u : 0u);
+        }
+        umma_commit(bar(DB_M1));
+      }
+      __syncwarp();
+      go = waitl(bar(DB_M1), it & 1) && go;
+      go = wait2(DB_D2R, it) && go;
+      if (go && r < 64) {
+        // dv_new rows 0-63 (warps 0, 1, 4, 5), 16 columns at a time.
+        tc_fence_after();
+        float dv[32];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const uint32_t col = 32 * hs + 16 * q;
+          uint32_t a0[16], a1[16], b0[16], b1[16], p[16];
+          tmem_ld16_issue(tl + DT_D1A + col, a0);
+          tmem_ld16_issue(tl + DT_D1A + 64 + col, a1);
+          tmem_ld16_issue(tl + DT_D1B + col, b0);
+          tmem_ld16_issue(tl + DT_D1B + 64 + col, b1);
+          tmem_ld16_issue(tl + DT_D2 + 64 * (it & 1) + col, p);
+          tmem_ld_wait16(a0);
+          tmem_ld_wait16(a1);
+          tmem_ld_wait16(b0);
+          tmem_ld_wait16(b1);
+          tmem_ld_wait16(p);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float kd = (__uint_as_float(a0[j]) + __uint_as_float(a1[j])) + (__uint_as_float(b0[j]) + __uint_as_float(b1[j]));
+            dv[16 * q + j] = fmaf(svr, kd, scale * __uint_as_float(p[j]));
+          }
+        }
+        write_split(Ly::OFF_DV, 8192, dv);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_bar_sync(1, 256);
+      if (warp == 0) {
+        go = waitl(bar(DB_D4R), it & 1) && go;  // Q^T (s do) is in D34: accumulate onto it
+        if (lane == 0 && go) {
+          tc_fence_after();
+          const uint32_t st = stage(it);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t a = umma_desc_sw128_mn(st + Ly::WR + kk * 2048, 8192);
+            const uint64_t b = umma_desc_sw128_mn(sb + Ly::OFF_DV + kk * 2048, 8192);
+            umma_bf16(tmem + DT_D34, a, b, ID3N, 1u);
+          }
+          umma_commit(bar(DB_M3));
+          umma_commit(bar(DB_EMPTY + (it & 1)));  // every product that reads the stage is done then
+        }
+        __syncwarp();
+      }
+      go = waitl(bar(DB_M3), it & 1) && go;
+      if (go) {
+        tc_fence_after();
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const uint32_t col = 32 * hs + 16 * q;
+          uint32_t x0[16], x1[16];
+          tmem_ld16_issue(tl + DT_D34 + col, x0);
+          tmem_ld16_issue(tl + DT_D34 + 64 + col, x1);
+          tmem_ld_wait16(x0);
+          tmem_ld_wait16(x1);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            dh[16 * q + j] = fmaf(dL, dh[16 * q + j], __uint_as_float(x0[j]) + __uint_as_float(x1[j]));
+        }
+      }
+      tc_fence_before();
+      named_bar_sync(1, 256);
+      if (tid == 0) mbar_arrive(bar(DB_CHD + (it & 1)));
+    }
+    if (dh0 && !*abort_flag) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 4)
+        *reinterpret_cast<float4 *>(dh0 + (sbase + r) * V + vt0 + 32 * hs + j) =
+            make_float4(dh[j], dh[j + 1], dh[j + 2], dh[j + 3]);
+    }
+  } else if (warp == 8) {
+    // ----------------------------------------------------------- producer
+    for (int it = 0; it < NC; ++it) {
+      if (it >= 2 && !wait2(DB_EMPTY, it - 2)) break;
+      if (lane == 0) {
+        const int c = chunk_of(it);
+        const uint32_t st = stage(it), fb = bar(DB_FULL + (it & 1));
+        const int trow = static_cast<int>(tok0) + c * C;
+        const unsigned char *rec = ws + (static_cast<size_t>(cb + c) * HV + hv) * R::BYTES;
+        mbar_arrive_expect_tx(fb, Ly::TX);
+#pragma unroll
+        for (int a = 0; a < 2; ++a) {
+          tma_load_3d(st + Ly::KT + a * 8192, &tm_k, fb, 64 * a, h, trow);
+          tma_load_3d(st + Ly::QT + a * 8192, &tm_q, fb, 64 * a, h, trow);
+        }
+#pragma unroll
+        for (int p = 0; p < 4; ++p) bulk_load(st + Ly::WR + p * 8192, rec + R::W + p * 8192, 8192, fb);
+        tma_load_3d(st + Ly::DO, &tm_do, fb, vt0, hv, trow);
+        bulk_load(st + Ly::SC, rec + R::SC, 1024, fb);
+      }
+      issued = it + 1;
+      __syncwarp();
+    }
+  } else {
+    // ------------------- converter: P^T do into D2, Q^T (s do) into D34
+    for (int it = 0; it < NC; ++it) {
+      const int c = chunk_of(it);
+      const uint32_t st = stage(it);
+      bool ok = wait2(DB_FULL, it);
+      if (it >= 2) ok = ok && wait2(DB_CHD, it - 2);  // the chain has read D2 of chunk it - 2
+      if (!ok) break;
+      if (lane == 0) {
+        tc_fence_after();
+        const uint32_t d2 = tmem + DT_D2 + 64 * (it & 1);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16(d2, umma_desc_sw128_mn(st + Ly::PH + kk * 2048, 8192), umma_desc_sw128_mn(st + Ly::DO + kk * 2048, 8192),
+                    ID2, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16(d2, umma_desc_sw128_mn(st + Ly::PL + kk * 2048, 8192), umma_desc_sw128_mn(st + Ly::DO + kk * 2048, 8192),
+                    ID2, 1u);
+        umma_commit(bar(DB_D2R + (it & 1)));
+      }
+      __syncwarp();
+      // The scaled do tile and D34 of chunk it - 1 are free once the chain has
+      // finished that chunk.
+      if (it >= 1 && !wait2(DB_CHD, it - 1)) break;
+      {
+        const int L = rows_of(c);
+        const float *scf = reinterpret_cast<const float *>(sm + (it & 1) * Ly::STAGE + Ly::SC);
+        const unsigned char *dop = sm + (it & 1) * Ly::STAGE + Ly::DO;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int i = lane + 32 * half;
+          const float s = i < L ? scale * scf[RS_OG + i] : 0.f;
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            const uint4 x = *reinterpret_cast<const uint4 *>(dop + sw128(i, ch));
+            const uint32_t xv[4] = {x.x, x.y, x.z, x.w};
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float y0 = s * bf16lo_f(xv[e]), y1 = s * bf16hi_f(xv[e]);
+              hi[e] = pack_bf16(y0, y1);
+              lo[e] = pack_bf16(y0 - bf16lo_f(hi[e]), y1 - bf16hi_f(hi[e]));
+            }
+            *reinterpret_cast<uint4 *>(sm + Ly::OFF_DS + sw128(i, ch)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4 *>(sm + Ly::OFF_DS + 8192 + sw128(i, ch)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16(tmem + DT_D34, umma_desc_sw128_mn(st + Ly::QT + kk * 2048, 8192),
+                    umma_desc_sw128_mn(sb + Ly::OFF_DS + kk * 2048, 8192), ID4, kk > 0 ? 1u : 0u);
+        umma_commit(bar(DB_D4R));
+      }
+      __syncwarp();
+    }
+  }
+  // After an abort: the producer waits for its last loads; the issuing threads
+  // commit once more to DRAIN (warps 0, 1, 9, plus thread 0 for the producer's
+  // share), completing when their products have.
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    if (warp == 8 && lane == 0)
+      for (int k2 = (issued > 2 ? issued - 2 : 0); k2 < issued; ++k2)
+        if (!mbar_wait_bounded(bar(DB_FULL + (k2 & 1)), (k2 >> 1) & 1, kWaitLimit))
+          set_status(dev_status, GDN_DEV_DRAIN_TIMEOUT);
+    if (lane == 0 && (warp < 2 || warp == 9)) {
+      tc_fence_after();
+      umma_commit(bar(DB_DRAIN));
+    }
+    if (tid == 0) {
+      mbar_arrive(bar(DB_DRAIN));
+      if (!mbar_wait_bounded(bar(DB_DRAIN), 0, kWaitLimit)) set_status(dev_status, GDN_DEV_DRAIN_TIMEOUT);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  if (tid == 0 && *abort_flag) set_status(dev_status, GDN_DEV_WAIT_TIMEOUT);
+}
+
+typedef CUresult (*DhEncodeFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                               const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                               CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+// 3-D map over a [rows][heads][dim] bf16 tensor, box {64, 1 head, 64 rows}, 128-byte swizzle.
+bool dh_map(CUtensorMap *m, const void *ptr, int dim, int heads, int64_t rows) {
+  static DhEncodeFn fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) != cudaSuccess ||
+        qr != cudaDriverEntryPointSuccess)
+      return false;
+    fn = reinterpret_cast<DhEncodeFn>(p);
+  }
+  cuuint64_t gdim[3] = {static_cast<cuuint64_t>(dim), static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(rows)};
+  cuuint64_t gstr[2] = {static_cast<cuuint64_t>(dim) * 2, static_cast<cuuint64_t>(dim) * heads * 2};
+  cuuint32_t box[3] = {64, 1, 64};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), gdim, gstr, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int K>
 cudaError_t launch_bwd_k(const gdn_host::ChunkBwdArgs &a, cudaStream_t s) {
   const int64_t slots = total_chunk_slots(a.B, a.T, a.N, a.cu != nullptr);
@@ -943,8 +1325,23 @@ cudaError_t launch_bwd_k(const gdn_host::ChunkBwdArgs &a, cudaStream_t s) {
   f.o = nullptr; f.ht = nullptr; f.hsave = Hs; f.ws = a.ws; f.ws_bytes = rec_bytes; f.dev_status = a.dev_status;
   e = gdn_host::launch_chunk(f, s);
   if (e != cudaSuccess) return e;
-  // 2. state gradients, last chunk first
-  {
+  // 2. state gradients, last chunk first (tcgen05 walk at K = 128 and 64-column slices)
+  if (K == 128 && a.V % DVC == 0 && rows > 0) {
+    CUtensorMap mq, mk, md;
+    memset(&mq, 0, sizeof(mq));
+    memset(&mk, 0, sizeof(mk));
+    memset(&md, 0, sizeof(md));
+    if (!dh_map(&mq, a.q, K, a.H, rows) || !dh_map(&mk, a.k, K, a.H, rows) || !dh_map(&md, a.dout, a.V, a.HV, rows))
+      return cudaErrorInvalidValue;
+    const int smem = DhtLay::BYTES + 1024;
+    e = cudaFuncSetAttribute(chunk_dh_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    chunk_dh_tc_kernel<<<dim3(a.V / DVC, a.HV, a.N), DT_THREADS, smem, s>>>(
+        mq, mk, md, static_cast<const unsigned char *>(a.ws), DH, a.dht, a.dh0, a.scale, a.cu, cs, a.T, a.H, a.HV,
+        a.V, a.dev_status);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  } else {
     const int smem = DhLay<K>::BYTES;
     e = cudaFuncSetAttribute(chunk_dh_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
