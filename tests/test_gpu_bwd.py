@@ -112,3 +112,14 @@ def test_bwd_varlen_many_sequences():
     case = W.prefill_case("bwd_many", 46, 1, sum(lens), 1, 2, 64, 64, init="all",
                           cu_seqlens=W.cu_from_lengths(lens))
     _run(case, seed=6)
+
+
+def test_bwd_k128_varlen_short_sequences():
+    # K = 128 takes the tcgen05 state-gradient walk: 40 packed sequences of
+    # 0..150 tokens, so most chunks are partial and the rows past a sequence's
+    # end that the walk's tile loads bring in belong to the next sequence.
+    rng = np.random.default_rng(47)
+    lens = [int(x) if rng.random() > 0.15 else 0 for x in rng.integers(1, 151, 40)]
+    case = W.prefill_case("bwd_k128_var", 47, 1, sum(lens), 2, 4, 128, 128, init="even",
+                          cu_seqlens=W.cu_from_lengths(lens))
+    _run(case, seed=7)
