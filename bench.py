@@ -342,6 +342,7 @@ def run_ours(args, rank, world, local_rank):
         line["conv1d"] = bench_conv(dev, stream, hbm, args)
         line["decode_variants"] = bench_decode_variants(dev, stream, hbm, args)
         line["backward"] = bench_backward(dev, stream, args, hbm, bf16_burst)
+        line["chunk_configs"] = bench_chunk_configs(dev, stream, args, hbm, bf16_sust)
         line["fused_gating"] = bench_fused_gating(dev, stream, args,
                                                   (q, k, v, A_log, a, b, dt_bias, h0, o, ht, ws, B, T, HV))
         line["e2e"] = bench_e2e(case, dev, stream, args, world)
@@ -510,6 +511,36 @@ def bench_conv(dev, stream, hbm, args):
             "decode": {"workload": f"conv1d update R={R} (valid {valid}) x {dimd} channels, pool "
                                    f"{tuple(sd.shape)} bf16", "us": ms_d * 1e3,
                        "achieved_GBps": bytes_d / (ms_d / 1e3) / 1e9}}
+
+
+def bench_chunk_configs(dev, stream, args, hbm, bf16):
+    """gdn_chunk_fwd on the other two prefill workloads, each against its own
+    roofline: the dense B=2 x T=4096 batch (initial and final states) and the
+    varlen pack of 8 sequences (19,103 tokens, states for every other one)."""
+    import torch
+    import gated_deltanet_chunked_chunk_gb300 as gdn
+    from gated_deltanet_chunked_chunk_gb300 import workloads as W
+    out = {}
+    d = lambda t: None if t is None else t.to(dev).contiguous()
+    for name, case in (("dense_B2_T4096", W.config1()), ("varlen_8seq", W.config2())):
+        g, beta = gdn.gdn_gating(d(case.A_log), d(case.a), d(case.b), d(case.dt_bias))
+        g, beta = g.view(case.B, case.T, case.HV), beta.view(case.B, case.T, case.HV)
+        q, k, v, h0, cu = d(case.q), d(case.k), d(case.v), d(case.initial_state), d(case.cu_seqlens)
+        o = torch.empty(case.B, case.T, case.HV, case.V, dtype=torch.bfloat16, device=dev)
+        ht = torch.empty(case.N, case.HV, case.K, case.V, device=dev)
+        ws = torch.empty(max(gdn.chunk_fwd_workspace_size(case.B, case.T, case.H, case.HV, case.K, case.V, case.N,
+                                                          cu is not None), 1), dtype=torch.uint8, device=dev)
+        ms = _timed_flush(dev, stream, lambda: gdn.gdn_chunk_fwd(
+            q, k, v, g, beta, initial_state=h0, cu_seqlens=cu, num_seqs=case.N, o=o, final_state=ht,
+            workspace=ws), max(args.steps, 10))
+        tokens = case.B * case.T
+        ab = prefill_bytes(case.B, case.T, case.H, case.HV, case.K, case.V, case.N)
+        af = prefill_flops(tokens, case.H, case.HV, case.K, case.V)
+        roof_ms = max(ab / (hbm * 1e9), af / (bf16 * 1e12)) * 1e3
+        out[name] = {"workload": f"B={case.B} T={case.T} N={case.N} H={case.H} HV={case.HV} K={case.K} V={case.V}",
+                     "ms": ms, "tokens_per_s": tokens / (ms / 1e3), "alg_bytes": ab, "roofline_ms": roof_ms,
+                     "frac": roof_ms / ms, "l2_flush": FLUSH_NOTE}
+    return out
 
 
 def bench_backward(dev, stream, args, hbm=None, bf16=None):
