@@ -21,8 +21,9 @@
 //
 // The forward is re-run first (prep + walk kernels of gdn_chunk.cu) with the
 // walk saving the state entering every chunk; the dh walk saves dh' of every
-// chunk.  Both backward kernels run their products on the tensor cores
-// (warp-level mma.sync, computed operands split hi + lo; see the helpers).
+// chunk.  The dh walk runs on tcgen05 at K = 128 (chunk_dh_tc_kernel, TMEM
+// accumulators) and on warp-level mma.sync otherwise; the per-chunk gradients
+// run on mma.sync (computed operands split hi + lo; see the helpers).
 #include <math.h>
 #include <string.h>
 
