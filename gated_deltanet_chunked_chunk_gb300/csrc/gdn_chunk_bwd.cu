@@ -956,8 +956,9 @@ struct DhtLay {
 };
 // TMEM columns.
 constexpr uint32_t DT_D1A = 0, DT_D1B = 128, DT_D2 = 256, DT_D34 = 384;
-constexpr int DT_THREADS = 10 * 32;
-enum { DB_FULL = 0, DB_EMPTY = 2, DB_D2R = 4, DB_CHD = 6, DB_M1 = 8, DB_M3 = 9, DB_D4R = 10, DB_DRAIN = 11 };
+constexpr int DT_THREADS = 11 * 32;
+enum { DB_FULL = 0, DB_EMPTY = 2, DB_D2R = 4, DB_CHD = 6, DB_M1 = 8, DB_M3 = 9, DB_D4R = 10, DB_DRAIN = 11,
+       DB_CONV = 12 };
 
 __global__ void __launch_bounds__(DT_THREADS, 1) chunk_dh_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -995,6 +996,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1) chunk_dh_tc_kernel(
     mbar_init(bar(DB_M1), 2);
     mbar_init(bar(DB_M3), 1);
     mbar_init(bar(DB_D4R), 1);
+    mbar_init(bar(DB_CONV), 2);
     mbar_init(bar(DB_DRAIN), 4);  // warps 0, 1 and 9, and the producer's stand-in
     misc[1] = 0;
     mbar_fence_init();
@@ -1187,15 +1189,17 @@ __global__ void __launch_bounds__(DT_THREADS, 1) chunk_dh_tc_kernel(
       issued = it + 1;
       __syncwarp();
     }
-  } else {
-    // ------------------- converter: P^T do into D2, Q^T (s do) into D34
+  } else if (warp == 9 || warp == 10) {
+    // ------------- converters: P^T do into D2 (warp 9), the scaled do tile
+    // (rows 0-31 warp 9, rows 32-63 warp 10), Q^T (s do) into D34 (warp 9)
+    const int cw = warp - 9;
     for (int it = 0; it < NC; ++it) {
       const int c = chunk_of(it);
       const uint32_t st = stage(it);
       bool ok = wait2(DB_FULL, it);
-      if (it >= 2) ok = ok && wait2(DB_CHD, it - 2);  // the chain has read D2 of chunk it - 2
+      if (cw == 0 && it >= 2) ok = ok && wait2(DB_CHD, it - 2);  // the chain has read D2 of chunk it - 2
       if (!ok) break;
-      if (lane == 0) {
+      if (cw == 0 && lane == 0) {
         tc_fence_after();
         const uint32_t d2 = tmem + DT_D2 + 64 * (it & 1);
 #pragma unroll
@@ -1216,9 +1220,8 @@ __global__ void __launch_bounds__(DT_THREADS, 1) chunk_dh_tc_kernel(
         const int L = rows_of(c);
         const float *scf = reinterpret_cast<const float *>(sm + (it & 1) * Ly::STAGE + Ly::SC);
         const unsigned char *dop = sm + (it & 1) * Ly::STAGE + Ly::DO;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const int i = lane + 32 * half;
+        {
+          const int i = lane + 32 * cw;
           const float s = i < L ? scale * scf[RS_OG + i] : 0.f;
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch) {
@@ -1238,6 +1241,9 @@ __global__ void __launch_bounds__(DT_THREADS, 1) chunk_dh_tc_kernel(
       }
       fence_proxy_async_smem();
       __syncwarp();
+      if (lane == 0) mbar_arrive(bar(DB_CONV));
+      if (cw == 1) continue;
+      if (!waitl(bar(DB_CONV), it & 1)) break;  // both halves of the scaled do tile are written
       if (lane == 0) {
         tc_fence_after();
 #pragma unroll
