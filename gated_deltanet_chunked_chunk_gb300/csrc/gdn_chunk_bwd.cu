@@ -469,17 +469,15 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
   };
   prefetch_slice(0);
   // ---- raw q, k rows (zero past L), gates and their cumsum
+  // (asynchronous 16-byte copies, zero-filled past L: every copy in flight at once)
   for (int e = tid; e < 64 * (K / 8); e += BT) {
     const int i = e / (K / 8), ch = e % (K / 8);
-    uint4 a = make_uint4(0, 0, 0, 0), b = a;
-    if (i < L) {
-      const int64_t off = ((trow0 + i) * H + h) * K + ch * 8;
-      a = *reinterpret_cast<const uint4 *>(q + off);
-      b = *reinterpret_cast<const uint4 *>(k + off);
-    }
-    *reinterpret_cast<uint4 *>(Qb + i * BR + ch * 8) = a;
-    *reinterpret_cast<uint4 *>(Kb + i * BR + ch * 8) = b;
+    const bool ok = i < L;
+    const int64_t off = ok ? ((trow0 + i) * H + h) * K + ch * 8 : 0;
+    cp_async16(Qb + i * BR + ch * 8, q + off, ok);
+    cp_async16(Kb + i * BR + ch * 8, k + off, ok);
   }
+  cp_async_commit();
   if (warp == 0) {
     float x[2];
 #pragma unroll
@@ -498,6 +496,7 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
     gam[2 * lane + 1] = sum;
   }
   for (int e = tid; e < 64 * (GV_MISC - GV_DB + 1); e += BT) vec[GV_DB * 64 + e] = 0.f;
+  cp_async_wait<0>();
   __syncthreads();
   {  // norms: four threads per row
     const int i = tid >> 2, p = tid & 3;
