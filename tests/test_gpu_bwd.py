@@ -123,3 +123,13 @@ def test_bwd_k128_varlen_short_sequences():
     case = W.prefill_case("bwd_k128_var", 47, 1, sum(lens), 2, 4, 128, 128, init="even",
                           cu_seqlens=W.cu_from_lengths(lens))
     _run(case, seed=7)
+
+
+def test_bwd_k128_without_l2norm_or_state_gradients():
+    # The tcgen05 state-gradient walk with raw keys and queries (no norm, no
+    # initial state, no final-state gradient); dimension 128 keys scaled by
+    # 1/16 (exact in bf16) keep |k| near 0.7.
+    case = W.prefill_case("bwd_nol2_k128", 48, 1, 200, 2, 4, 128, 128, init="none")
+    case.q = case.q * 0.0625
+    case.k = case.k * 0.0625
+    _run(case, l2=False, with_dht=False, seed=8)
