@@ -178,12 +178,7 @@ __global__ void __launch_bounds__(NTH, 4) chunk_prep_kernel(
     mbar_init(b_mma, 1);
     misc[1] = 0;
     mbar_fence_init();
-  }
-  if (warp == 0) tmem_alloc(sb + Ly::OFF_MISC, 128);
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = misc[0];
-  if (tid == 0) {
+    // The loads go out first: they overlap the TMEM allocation and the gates.
     mbar_arrive_expect_tx(b_tma, KQ<K>::BYTES);
 #pragma unroll
     for (int a = 0; a < KA; ++a) {
@@ -191,6 +186,10 @@ __global__ void __launch_bounds__(NTH, 4) chunk_prep_kernel(
       tma_load_3d(kq + a * 16384 + 8192, &tm_q, b_tma, 64 * a, h, static_cast<int>(trow0));
     }
   }
+  if (warp == 0) tmem_alloc(sb + Ly::OFF_MISC, 128);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
   // Gates (rows >= L read as 0) and their chunk-local cumsum in base 2 (warp 4).
   // Fused gating follows FastDeploy PR "support fla triton kernel for qwen3.5",
   // Usage section 5: g = -e^{A_log} softplus(a + dt_bias), beta = sigmoid(b).
@@ -473,6 +472,25 @@ __global__ void __launch_bounds__(NTH, 4) chunk_prep_kernel(
     }
     *reinterpret_cast<uint4 *>(sm + Ly::OFF_TP + sw128(i, ch)) = tpv;
   }
+  // W = Tp K (64 x K) on tcgen05: A = Tp (K-major, its rows 64-127 whatever
+  // follows the tile: those accumulator lanes are not read), B = the K rows of
+  // the [K;Q] tile as an MN-major operand (keys contiguous, 64-key atoms 16 KB
+  // apart), fp32 accumulator in the TMEM columns of the first product.  It runs
+  // while the threads build Ts^T, whose staging block (the Q rows of the second
+  // atom) neither operand reads.  The warps of TMEM lanes 0-63 then turn it
+  // into the record's bf16 W, one row and 64 keys per thread, staged in the K
+  // rows for two bulk stores.
+  fence_proxy_async_smem();  // Tp and the zeroed K rows, for the async proxy
+  __syncthreads();
+  if (tid == 0) {
+    tc_fence_after();
+    constexpr uint32_t idw = umma_idesc_bf16(128, K, 0, 1);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      umma_bf16(tmem, umma_desc_sw128(sb + Ly::OFF_TP + kk * 32), umma_desc_sw128_mn(kq + kk * 2048, 16384), idw,
+                kk > 0 ? 1u : 0u);
+    umma_commit(b_mma);
+  }
   // Ts = (T - I) diag(beta) (j < i), written transposed (row j holds column j
   // of Ts): the MN-major A operand of the walk's u = Ts V product.  A warp
   // takes 32 consecutive columns j, so its reads of T hit distinct banks.
@@ -496,26 +514,13 @@ __global__ void __launch_bounds__(NTH, 4) chunk_prep_kernel(
       *reinterpret_cast<uint4 *>(rec + R::TS + sw128(j, ich)) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 
-  // W = Tp K (64 x K) on tcgen05: A = Tp (K-major, its rows 64-127 whatever
-  // follows the tile: those accumulator lanes are not read), B = the K rows of
-  // the [K;Q] tile as an MN-major operand (keys contiguous, 64-key atoms 16 KB
-  // apart), fp32 accumulator in the TMEM columns of the first product.  The
-  // warps of TMEM lanes 0-63 turn it into the record's bf16 W, one row and
-  // 64 keys per thread, staged in the K rows for two bulk stores.
-  fence_proxy_async_smem();  // Tp, the zeroed K rows and Ts^T, for the async proxy
+  if constexpr (K >= 128) fence_proxy_async_smem();  // Ts^T, for the bulk copy
   __syncthreads();
   if (tid == 0) {
     if constexpr (K >= 128) {
       bulk_store(rec + R::TS, sb + Ly::OFF_TSS, 8192);
       bulk_commit();
     }
-    tc_fence_after();
-    constexpr uint32_t idw = umma_idesc_bf16(128, K, 0, 1);
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-      umma_bf16(tmem, umma_desc_sw128(sb + Ly::OFF_TP + kk * 32), umma_desc_sw128_mn(kq + kk * 2048, 16384), idw,
-                kk > 0 ? 1u : 0u);
-    umma_commit(b_mma);
     if (!mbar_wait_bounded(b_mma, 1, kWaitLimit)) {
       misc[1] = 1;
       set_status(dev_status, GDN_DEV_WAIT_TIMEOUT);
@@ -527,18 +532,22 @@ __global__ void __launch_bounds__(NTH, 4) chunk_prep_kernel(
     const int i = 32 * (warp & 3) + lane, a = warp >> 2;
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + 64 * a;
     unsigned char *wrow = sm + Ly::OFF_KQ + a * 16384;  // the K rows of atom a: dead now
+    // Two 16-column loads in flight per round trip.
 #pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
-      uint32_t x[16];
-      tmem_ld16_issue(tl + 16 * q4, x);
-      tmem_ld_wait16(x);
+    for (int q8 = 0; q8 < 2; ++q8) {
+      uint32_t x[2][16];
+      tmem_ld16_issue(tl + 32 * q8, x[0]);
+      tmem_ld16_issue(tl + 32 * q8 + 16, x[1]);
+      tmem_ld_wait16(x[0]);
+      tmem_ld_wait16(x[1]);
 #pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
+      for (int c4 = 0; c4 < 4; ++c4) {
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          w[e] = pack_bf16(__uint_as_float(x[8 * c2 + 2 * e]), __uint_as_float(x[8 * c2 + 2 * e + 1]));
-        *reinterpret_cast<uint4 *>(wrow + sw128(i, 2 * q4 + c2)) = make_uint4(w[0], w[1], w[2], w[3]);
+          w[e] = pack_bf16(__uint_as_float(x[c4 >> 1][8 * (c4 & 1) + 2 * e]),
+                           __uint_as_float(x[c4 >> 1][8 * (c4 & 1) + 2 * e + 1]));
+        *reinterpret_cast<uint4 *>(wrow + sw128(i, 4 * q8 + c4)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
     fence_proxy_async_smem();  // W, for the bulk copies
@@ -555,7 +564,10 @@ __global__ void __launch_bounds__(NTH, 4) chunk_prep_kernel(
       for (int a = 0; a < KA; ++a) bulk_store(rec + R::W + a * 8192, sb + Ly::OFF_KQ + a * 16384, 8192);
       bulk_commit();
     }
-    bulk_wait_all();  // shared memory must outlive the copies
+    // Shared memory must outlive the copies' reads of it; their global writes
+    // are performed before the grid completes, which orders them before the
+    // walk on the stream.
+    bulk_wait_read();
   }
 }
 
