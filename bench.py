@@ -40,7 +40,8 @@ def parse():
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--e2e-steps", type=int, default=3)
+    p.add_argument("--e2e-steps", type=int, default=24,
+                   help="pipelined steps timed for e2e (the first input copy and the last output copy are not overlapped)")
     p.add_argument("--cpu-tokens", type=int, default=65536,
                    help="tokens of the workload (all heads) in the CPU oracle sample")
     p.add_argument("--cpu-runs", type=int, default=3, help="runs of that sample for cpu_baseline")
@@ -603,7 +604,9 @@ def bench_e2e(case, dev, stream, args, world):
     streaming job runs them: the copies of step i + 1 and of step i - 1 overlap
     the compute of step i (two input streams, one output stream, double-buffered
     device and host buffers, ordered by events); the timed region spans every
-    copy of every step."""
+    copy of every step.  Only the first step's input copy and the last step's
+    output copy have nothing to overlap, so the steady-state rate of a stream of
+    steps needs a couple of dozen of them (the default: 24 steps, ~0.15 s)."""
     import torch
     import gated_deltanet_chunked_chunk_gb300 as gdn
     B, T, H, HV, K, V, N = case.B, case.T, case.H, case.HV, case.K, case.V, case.N
