@@ -10,6 +10,8 @@ Cases:
   decode_bf16 : the same against a bf16 pool
   gating      : 524288 x 32 gates
   bwd_dense   : gdn_chunk_bwd on the chunk_dense workload (initial state, final-state gradient)
+  conv        : causal conv1d prefill, 8192 channels x 16384 tokens with an initial state
+  mtp         : multi-token decode, 64 requests x 4 tokens against a [256, 32, 128, 128] fp32 pool
 """
 from __future__ import annotations
 
@@ -25,7 +27,8 @@ from gated_deltanet_chunked_chunk_gb300 import workloads as W
 def main():
     p = argparse.ArgumentParser()
     p.add_argument("--case", default="chunk_dense",
-                   choices=["chunk_dense", "chunk_long", "decode", "decode_bf16", "gating", "bwd_dense"])
+                   choices=["chunk_dense", "chunk_long", "decode", "decode_bf16", "gating", "bwd_dense",
+                            "conv", "mtp"])
     p.add_argument("--reps", type=int, default=3)
     args = p.parse_args()
     gbuild.build()
@@ -61,6 +64,33 @@ def main():
         for _ in range(args.reps):
             fn(d(dc.q), d(dc.k), d(dc.v), pool, d(dc.ssm_indices),
                A_log=d(dc.A_log), a=d(dc.a), b=d(dc.b), dt_bias=d(dc.dt_bias))
+    elif args.case == "conv":
+        # dim 8192 (packed q | k | v of the long prefill) x 16384 tokens: 0.5 GB in + out
+        pc = W.conv_prefill_case("conv_profile_T16384_dim8192", 13, 8192, [16384], init_every=1, P=4)
+        x, w, bias, st = d(pc.x), d(pc.weight), d(pc.bias), d(pc.conv_states)
+        qsl, ci, hi = d(pc.query_start_loc), d(pc.cache_indices), d(pc.has_initial_state)
+        out = torch.empty_like(x)
+        for _ in range(args.reps):
+            gdn.gdn_causal_conv1d_fwd(x, w, bias, st, qsl, ci, hi, out=out)
+    elif args.case == "mtp":
+        # 64 requests x 4 tokens against a [256, 32, 128, 128] fp32 pool (0.5 GB)
+        N, ld, H, HV, K, V = 64, 4, 16, 32, 128, 128
+        gen = torch.Generator().manual_seed(24)
+        Tt = N * ld
+        qm = d(torch.randn(Tt, H, K, generator=gen).to(torch.bfloat16))
+        km = d(torch.randn(Tt, H, K, generator=gen).to(torch.bfloat16))
+        vm = d(torch.randn(Tt, HV, V, generator=gen).to(torch.bfloat16))
+        am = d(torch.randn(Tt, HV, generator=gen).to(torch.bfloat16))
+        bm = d(torch.randn(Tt, HV, generator=gen).to(torch.bfloat16))
+        A_log = d(torch.zeros(HV))
+        dt = d(torch.zeros(HV))
+        pool = torch.randn(N * ld, HV, K, V, generator=gen).mul_(0.1).to(dev)
+        slots = d(torch.arange(N, dtype=torch.int32)[:, None] * ld + torch.arange(ld, dtype=torch.int32)[None, :])
+        cu = d(torch.arange(0, Tt + 1, ld, dtype=torch.int32))
+        acc = d(torch.full((N,), 2, dtype=torch.int32))
+        for _ in range(args.reps):
+            gdn.gdn_recurrent_decode_mtp(qm, km, vm, pool, cu, slots, slots, acc, A_log=A_log, a=am, b=bm,
+                                         dt_bias=dt)
     else:
         n, HV = 65536 * 8, 32
         gen = torch.Generator().manual_seed(5)
