@@ -15,7 +15,7 @@
 //
 // All three ops are memory-bound (a few multiply-adds per element).
 //  * conv_prefill_kernel: x is channel-first [dim, total]; a CTA takes one
-//    channel and 32768 tokens, a thread 8 consecutive tokens per step with
+//    channel and 32768 tokens, a thread 16 consecutive tokens per step with
 //    16-byte loads and stores (the general per-token path, with a binary
 //    search in query_start_loc, serves sequence starts and unaligned rows).
 //  * conv_state_kernel (same stream, after the prefill kernel, so every read
@@ -34,6 +34,15 @@ namespace {
 constexpr int kConvMaxW = 8;
 constexpr int kConvMaxS = 64;
 constexpr int kPrefillTile = 32768;
+constexpr int kGroup = 16;  // tokens a thread takes per step on the vector path
+
+// Two floats to a bf16 pair (round to nearest even, as __float2bfloat16_rn),
+// lo in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 
 // SiLU with the hardware exponential and a fast divide: a few ulp of fp32,
 // far below the bf16 rounding of the output (for x < -87 the divisor is huge
@@ -85,11 +94,11 @@ __device__ __forceinline__ float conv_prefill_one(const uint16_t *__restrict__ x
 }
 
 // One CTA per (channel, 32768-token tile).  Vector path (rows 16-byte aligned):
-// a thread takes 8 consecutive tokens, loads them and the 8 before them with
-// two 16-byte loads (the second mostly an L1 hit) and stores 16 bytes; tokens
-// within W - 1 of a sequence start, or sharing the 8 with a boundary, take the
+// a thread takes 16 consecutive tokens, loads them and the 8 before them with
+// three 16-byte loads (the last mostly an L1 hit) and stores 32 bytes; tokens
+// within W - 1 of a sequence start, or sharing the 16 with a boundary, take the
 // general path.  Without aligned rows every token takes the general path.
-// WT > 0 fixes the width at compile time (so the 16-value window stays in
+// WT > 0 fixes the width at compile time (so the 24-value window stays in
 // registers); WT = 0 takes it from W at run time.
 template <int WT>
 __global__ void __launch_bounds__(256) conv_prefill_kernel(
@@ -117,12 +126,12 @@ __global__ void __launch_bounds__(256) conv_prefill_kernel(
     return;
   }
   // The sequence [s_lo, s_hi) holding the last group looked up: the thread's
-  // groups are 8 blockDim tokens apart, so the binary search runs only when a
-  // group leaves it.
+  // groups are kGroup blockDim tokens apart, so the binary search runs only
+  // when a group leaves it.
   int64_t s_lo = 1, s_hi = 0;
-  for (int64_t t0 = tile0 + 8 * threadIdx.x; t0 < t_end; t0 += 8 * blockDim.x) {
-  // Fast path: all 8 tokens in one sequence, at least W - 1 tokens past its start.
-  bool fast = t0 + 8 <= t_end;
+  for (int64_t t0 = tile0 + kGroup * threadIdx.x; t0 < t_end; t0 += kGroup * blockDim.x) {
+  // Fast path: all kGroup tokens in one sequence, at least W - 1 tokens past its start.
+  bool fast = t0 + kGroup <= t_end;
   if (fast) {
     if (t0 < s_lo || t0 >= s_hi) {
       const int n = seq_of(qsl, N, t0);
@@ -134,22 +143,24 @@ __global__ void __launch_bounds__(256) conv_prefill_kernel(
         s_hi = 0;
       }
     }
-    fast = t0 >= s_lo && t0 - s_lo >= W - 1 && s_hi >= t0 + 8;
+    fast = t0 >= s_lo && t0 - s_lo >= W - 1 && s_hi >= t0 + kGroup;
   }
   if (fast) {
-    const uint4 cur = *reinterpret_cast<const uint4 *>(xr + t0);
+    // The group's tokens and the 8 before it (W - 1 <= 7 of them are taps).
+    const uint4 c0 = *reinterpret_cast<const uint4 *>(xr + t0);
+    const uint4 c1 = *reinterpret_cast<const uint4 *>(xr + t0 + 8);
     uint4 prv = make_uint4(0, 0, 0, 0);
     if (t0 >= 8) prv = *reinterpret_cast<const uint4 *>(xr + t0 - 8);
-    const uint32_t wv[8] = {prv.x, prv.y, prv.z, prv.w, cur.x, cur.y, cur.z, cur.w};
-    float v[16];
+    const uint32_t wv[12] = {prv.x, prv.y, prv.z, prv.w, c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    float v[24];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < 12; ++i) {
       v[2 * i] = gdn::bf2f(static_cast<uint16_t>(wv[i] & 0xFFFFu));
       v[2 * i + 1] = gdn::bf2f(static_cast<uint16_t>(wv[i] >> 16));
     }
-    uint32_t o[4];
+    uint32_t o[8];
 #pragma unroll
-    for (int e = 0; e < 8; e += 2) {
+    for (int e = 0; e < kGroup; e += 2) {
       float a0 = b0, a1 = b0;
 #pragma unroll
       for (int j = 0; j < kConvMaxW; ++j) {
@@ -158,13 +169,13 @@ __global__ void __launch_bounds__(256) conv_prefill_kernel(
           a1 = fmaf(wf[j], v[9 + e - (W - 1) + j], a1);
         }
       }
-      o[e / 2] = static_cast<uint32_t>(gdn::f2bf(conv_act(a0, act))) |
-                 (static_cast<uint32_t>(gdn::f2bf(conv_act(a1, act))) << 16);
+      o[e / 2] = pack_bf16x2(conv_act(a0, act), conv_act(a1, act));
     }
     *reinterpret_cast<uint4 *>(orow + t0) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4 *>(orow + t0 + 8) = make_uint4(o[4], o[5], o[6], o[7]);
     continue;
   }
-  for (int64_t t = t0; t < t0 + 8 && t < t_end; ++t) {
+  for (int64_t t = t0; t < t0 + kGroup && t < t_end; ++t) {
     bool ok;
     const float acc = conv_prefill_one(xr, wf, b0, states, P, S, qsl, cache, has_init, N, dim, d, t, W,
                                        dev_status, ok);
