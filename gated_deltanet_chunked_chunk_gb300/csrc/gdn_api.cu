@@ -15,6 +15,15 @@ std::atomic<int> g_force_wait_expiry{0};
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ECUDA; }
 
+// The chunk entry points encode TMA tensor maps with a driver call, which needs
+// a context current on the calling thread.  A thread whose first CUDA work this
+// is (a framework's worker thread, say) may have none: setting the thread's
+// device again makes that device's primary context current.
+bool bind_context() {
+  int dev = 0;
+  return cudaGetDevice(&dev) == cudaSuccess && cudaSetDevice(dev) == cudaSuccess;
+}
+
 }  // namespace
 
 extern "C" {
@@ -80,6 +89,7 @@ int chunk_fwd_common(gdn_host::ChunkArgs &a, const uint16_t *q, const uint16_t *
   a.o = o; a.ht = final_state; a.ws = workspace; a.ws_bytes = workspace_bytes;
   a.dev_status = dev_status;
   a.force_expiry = g_force_wait_expiry.load();
+  if (!bind_context()) return GDN_ECUDA;
   return cuda_status(gdn_host::launch_chunk(a, static_cast<cudaStream_t>(stream)));
 }
 }  // namespace
@@ -140,6 +150,7 @@ int gdn_chunk_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const
   a.N = N; a.B = B; a.T = T; a.H = H; a.HV = HV; a.K = K; a.V = V; a.l2 = use_qk_l2norm ? 1 : 0;
   a.dout = dout; a.dht = dht; a.dq = dq; a.dk = dk; a.dv = dv; a.dg = dg; a.dbeta = dbeta; a.dh0 = dh0;
   a.ws = workspace; a.ws_bytes = workspace_bytes; a.dev_status = dev_status;
+  if (!bind_context()) return GDN_ECUDA;
   return cuda_status(gdn_host::launch_chunk_bwd(a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
     const float *__restrict__ g, const float *__restrict__ beta, const uint16_t *__restrict__ dout,
     const float *__restrict__ Hs, const float *__restrict__ DH, float scale, const int32_t *__restrict__ cu,
     const int32_t *__restrict__ cs, int N, int T, int H, int HV, int V, int l2, float *__restrict__ dq,
-    float *__restrict__ dk,
+    float *__restrict__ dk, float *__restrict__ dqk_part, int64_t part_stride,
     float *__restrict__ dv, float *__restrict__ dg, float *__restrict__ dbeta, int32_t *dev_status) {
   using Ly = GradLay<K>;
   constexpr int BR = Ly::BROW;
@@ -725,7 +725,7 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
         hh = fmaf(bf2f(DHhi[o16]) + bf2f(DHlo[o16]), bf2f(Hhi[o16]) + bf2f(Hlo[o16]), hh);
       }
       hh = warp_sum(hh);
-      if (lane == 0) atomicAdd(&misc[0], hh);
+      if (lane == 0) misc[warp - 4] += hh;  // one slot per warp, summed in a fixed order below
     }
     __syncthreads();
     {
@@ -841,6 +841,8 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
     };
     wgemm_bf<NH, false, true>(accK, 0, 128, fa, fb);
     // d gamma's output term: sum_c (q^_i . h_c) do_ic = q^_i . (do h^T)_i
+    // (each element of SQ, PQ, PK below gets exactly two adds, one per warp of
+    // a row block, so their order cannot change the sum)
     {
       float sq[2] = {0.f, 0.f};
       cvisit(accQ, [&](int rh, int r, int n, float x) { sq[rh] = fmaf(qv(r0 + r, x0 + n), x, sq[rh]); });
@@ -856,7 +858,10 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
     auto fb2 = [&](int m, int n) { return make_float2(kv(m, x0 + n), kv(m + 1, x0 + n)); };
     wgemm_bf<NH, false, true>(accQ, 0, r0 + 16, fa2, fb2);
   }
-  // ---- through the L2 norms (dx = r (dx^ - x^ (x^ . dx^))), summed over the group's value heads
+  // ---- through the L2 norms (dx = r (dx^ - x^ (x^ . dx^))).  The group's first
+  // value head writes its share into dq, dk, the j-th later one into slot j - 1
+  // of dqk_part (dq shares, then dk shares, part_stride floats apart); a
+  // second pass adds the slots in head order, so two runs agree bit for bit.
   {
     float pq[2] = {0.f, 0.f}, pk[2] = {0.f, 0.f};
     cvisit(accQ, [&](int rh, int r, int n, float x) { pq[rh] = fmaf(qv(r0 + r, x0 + n), x, pq[rh]); });
@@ -874,18 +879,21 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
     }
   }
   __syncthreads();
+  const int gj = hv % (HV / H);  // this value head's place in its group
+  float *dq_dst = gj == 0 ? dq : dqk_part + (int64_t)(gj - 1) * 2 * part_stride;
+  float *dk_dst = gj == 0 ? dk : dqk_part + ((int64_t)(gj - 1) * 2 + 1) * part_stride;
   cvisit(accQ, [&](int, int r, int n, float x) {
     const int i = r0 + r, xx = x0 + n;
     if (i < L) {
       const float gq = l2 ? rq[i] * (x - rq[i] * rq[i] * qv(i, xx) * PQ[i]) : x;
-      atomicAdd(dq + ((trow0 + i) * H + h) * K + xx, gq);
+      dq_dst[((trow0 + i) * H + h) * K + xx] = gq;
     }
   });
   cvisit(accK, [&](int, int r, int n, float x) {
     const int i = r0 + r, xx = x0 + n;
     if (i < L) {
       const float gk = l2 ? rk[i] * (x - rk[i] * rk[i] * kv(i, xx) * PK[i]) : x;
-      atomicAdd(dk + ((trow0 + i) * H + h) * K + xx, gk);
+      dk_dst[((trow0 + i) * H + h) * K + xx] = gk;
     }
   });
   // ---- d gamma, then dg = reverse cumsum over the chunk; d beta
@@ -897,7 +905,7 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
       d[u] = DG[i] - bet[i] * og[i] * SG[i] + scale * og[i] * SQ[i] - sv[i] * SLv[i];
       dl = fmaf(sv[i], SLv[i], dl);
     }
-    dl = warp_sum(dl) + og[63] * misc[0];  // d gamma_L
+    dl = warp_sum(dl) + og[63] * (((misc[0] + misc[1]) + misc[2]) + misc[3]);  // d gamma_L
     if (lane == 31) d[1] += dl;
     float s = d[0] + d[1];
 #pragma unroll
@@ -1305,6 +1313,24 @@ bool dh_map(CUtensorMap *m, const void *ptr, int dim, int heads, int64_t rows) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// dq, dk += the shares of a group's later value heads, added in head order
+// (part holds nparts pairs of [rows, H, K] shares: dq's, then dk's).
+__global__ void __launch_bounds__(256) dqk_sum_kernel(float *__restrict__ dq, float *__restrict__ dk,
+                                                      const float *__restrict__ part, int64_t n4,
+                                                      int64_t part_stride, int nparts) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
+    float4 a = reinterpret_cast<const float4 *>(dq)[i], b = reinterpret_cast<const float4 *>(dk)[i];
+    for (int j = 0; j < nparts; ++j) {
+      const float4 pa = reinterpret_cast<const float4 *>(part + 2 * j * part_stride)[i];
+      const float4 pb = reinterpret_cast<const float4 *>(part + (2 * j + 1) * part_stride)[i];
+      a = make_float4(a.x + pa.x, a.y + pa.y, a.z + pa.z, a.w + pa.w);
+      b = make_float4(b.x + pb.x, b.y + pb.y, b.z + pb.z, b.w + pb.w);
+    }
+    reinterpret_cast<float4 *>(dq)[i] = a;
+    reinterpret_cast<float4 *>(dk)[i] = b;
+  }
+}
+
 template <int K>
 cudaError_t launch_bwd_k(const gdn_host::ChunkBwdArgs &a, cudaStream_t s) {
   const int64_t slots = total_chunk_slots(a.B, a.T, a.N, a.cu != nullptr);
@@ -1317,12 +1343,22 @@ cudaError_t launch_bwd_k(const gdn_host::ChunkBwdArgs &a, cudaStream_t s) {
   const int32_t *cs =
       a.cu ? reinterpret_cast<const int32_t *>(wsb + (size_t)slots * a.HV * Rec<K>::BYTES) : nullptr;
   const int64_t rows = (int64_t)a.B * a.T;
+  // dq, dk shares of the later value heads of each group, after the states.
+  const int nparts = a.HV / a.H - 1;
+  const int64_t part_stride = rows * a.H * K;
+  float *part = reinterpret_cast<float *>(wsb + rec_bytes + 2 * hbytes);
   cudaError_t e;
-  if (rows > 0) {
-    e = cudaMemsetAsync(a.dq, 0, (size_t)rows * a.H * K * sizeof(float), s);
+  if (rows > 0 && a.cu) {
+    // Every token of every sequence gets its dq, dk (and shares) written;
+    // tokens that cu_seqlens leaves outside all sequences stay zero.
+    e = cudaMemsetAsync(a.dq, 0, (size_t)part_stride * sizeof(float), s);
     if (e != cudaSuccess) return e;
-    e = cudaMemsetAsync(a.dk, 0, (size_t)rows * a.H * K * sizeof(float), s);
+    e = cudaMemsetAsync(a.dk, 0, (size_t)part_stride * sizeof(float), s);
     if (e != cudaSuccess) return e;
+    if (nparts > 0) {
+      e = cudaMemsetAsync(part, 0, (size_t)nparts * 2 * part_stride * sizeof(float), s);
+      if (e != cudaSuccess) return e;
+    }
   }
   // 1. forward again, saving the state entering every chunk (no output needed)
   gdn_host::ChunkArgs f{};
@@ -1364,9 +1400,20 @@ cudaError_t launch_bwd_k(const gdn_host::ChunkBwdArgs &a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     chunk_grad_kernel<K><<<dim3((unsigned)(slots * a.HV)), BT, smem, s>>>(
         a.q, a.k, a.v, a.g, a.beta, a.dout, Hs, DH, a.scale, a.cu, cs, a.N, a.T, a.H, a.HV, a.V, a.l2, a.dq,
-        a.dk, a.dv, a.dg, a.dbeta, a.dev_status);
+        a.dk, part, part_stride, a.dv, a.dg, a.dbeta, a.dev_status);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (nparts > 0) {
+      int dev = 0, sms = 148;
+      cudaGetDevice(&dev);
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      const int64_t n4 = part_stride / 4;
+      const int64_t want = (n4 + 255) / 256;
+      const int blocks = (int)(want < (int64_t)sms * 8 ? want : (int64_t)sms * 8);
+      dqk_sum_kernel<<<blocks, 256, 0, s>>>(a.dq, a.dk, part, n4, part_stride, nparts);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
   }
   return cudaSuccess;
 }
@@ -1378,7 +1425,9 @@ namespace gdn_host {
 size_t chunk_bwd_workspace_bytes(int B, int T, int H, int HV, int K, int V, int N, int varlen) {
   const size_t rec = chunk_workspace_bytes(B, T, H, HV, K, V, N, varlen);
   const size_t st = (size_t)total_chunk_slots(B, T, N, varlen != 0) * HV * K * V * sizeof(float);
-  return rec + 2 * st;
+  // the dq, dk shares of each group's later value heads
+  const size_t parts = H > 0 ? (size_t)(HV / H - 1) * 2 * B * T * H * K * sizeof(float) : 0;
+  return rec + 2 * st + parts;
 }
 
 cudaError_t launch_chunk_bwd(const ChunkBwdArgs &a, cudaStream_t s) {

@@ -214,7 +214,9 @@ int gdn_recurrent_decode(const uint16_t *q, const uint16_t *k,
 /*
  * gdn_chunk_bwd_workspace_size -- bytes of device workspace gdn_chunk_bwd
  * needs (the forward's workspace -- records, and the chunk-start table for
- * cu_seqlens input -- plus two fp32 states per chunk and value head).
+ * cu_seqlens input -- plus two fp32 states per chunk and value head, plus the
+ * fp32 dq and dk shares [B*T, H, K] of every value head of a group but its
+ * first).
  */
 size_t gdn_chunk_bwd_workspace_size(int B, int T, int H, int HV, int K, int V,
                                     int N, int varlen);
@@ -233,12 +235,13 @@ size_t gdn_chunk_bwd_workspace_size(int B, int T, int H, int HV, int K, int V,
  * use_qk_l2norm); do: bf16 [B, T, HV, V]; dht: fp32 [N, HV, K, V] or NULL
  * (zero).  The forward is recomputed inside (the call saves the state
  * entering every chunk in the workspace), then the state gradients run last
- * chunk first, then the per-chunk gradients in parallel: four launches (five
- * with cu_seqlens) plus two memsets of dq, dk on `stream`.  Products run on the
- * tensor cores with computed operands split into bf16 hi + lo parts (relative
- * error near 2^-17 per product, fp32 accumulation); dq, dk (over the value
- * heads of a group) and parts of dg are summed with atomic adds, so two runs
- * agree to rounding, not bit for bit.  Errors as gdn_chunk_fwd; the workspace
+ * chunk first, then the per-chunk gradients in parallel, then (HV > H) a pass
+ * adding the later value heads' dq, dk shares in head order: up to five
+ * launches (six with cu_seqlens, which also adds memsets of dq, dk and the
+ * shares on `stream`).  Products run on the tensor cores with computed
+ * operands split into bf16 hi + lo parts (relative error near 2^-17 per
+ * product, fp32 accumulation).  Every sum has a fixed order, so two runs on
+ * the same inputs agree bit for bit.  Errors as gdn_chunk_fwd; the workspace
  * must hold gdn_chunk_bwd_workspace_size() bytes.
  */
 int gdn_chunk_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,

@@ -151,3 +151,37 @@ def test_bad_cu_seqlens_sets_device_status():
     gdn.gdn_chunk_fwd(x, x, v, gz, gz, cu_seqlens=cu, dev_status=st)
     torch.cuda.synchronize()
     assert int(st.item()) & gdn.DEV_BAD_CU_SEQLENS
+
+
+def test_chunk_entry_points_from_a_fresh_thread():
+    # The first CUDA work of a new host thread is the library call (outputs and
+    # workspace allocated beforehand on the main thread): the entry points make
+    # the device's context current before their tensor-map encode, and give the
+    # same bits as on the main thread.
+    import threading
+    import gated_deltanet_chunked_chunk_gb300 as gdn
+    case = W.prefill_case("thread", 71, 1, 150, 2, 4, 64, 128, init="all")
+    g, beta = P.oracle_gates(case)
+    d = lambda t: t.to("cuda").contiguous()
+    args = (d(case.q), d(case.k), d(case.v), d(g), d(beta))
+    h0 = d(case.initial_state)
+    ws = torch.empty(gdn.chunk_fwd_workspace_size(1, 150, 2, 4, 64, 128, 1, False), dtype=torch.uint8,
+                     device="cuda")
+    o_main, ht_main = gdn.gdn_chunk_fwd(*args, initial_state=h0, workspace=ws)
+    o = torch.empty_like(o_main)
+    ht = torch.empty_like(ht_main)
+    torch.cuda.synchronize()
+    errors = []
+
+    def work():
+        try:
+            gdn.gdn_chunk_fwd(*args, initial_state=h0, o=o, final_state=ht, workspace=ws)
+        except Exception as ex:  # reported on the main thread below
+            errors.append(ex)
+
+    t = threading.Thread(target=work)
+    t.start()
+    t.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_main) and torch.equal(ht, ht_main)
