@@ -882,20 +882,27 @@ __global__ void __launch_bounds__(BT, 1) chunk_grad_kernel(
   const int gj = hv % (HV / H);  // this value head's place in its group
   float *dq_dst = gj == 0 ? dq : dqk_part + (int64_t)(gj - 1) * 2 * part_stride;
   float *dk_dst = gj == 0 ? dk : dqk_part + ((int64_t)(gj - 1) * 2 + 1) * part_stride;
-  cvisit(accQ, [&](int, int r, int n, float x) {
-    const int i = r0 + r, xx = x0 + n;
-    if (i < L) {
-      const float gq = l2 ? rq[i] * (x - rq[i] * rq[i] * qv(i, xx) * PQ[i]) : x;
-      dq_dst[((trow0 + i) * H + h) * K + xx] = gq;
+  // A thread's accumulator holds two adjacent columns of a row per 8-column
+  // tile and row half: one 8-byte store each.
+#pragma unroll
+  for (int nt = 0; nt < NH; ++nt) {
+#pragma unroll
+    for (int rh = 0; rh < 2; ++rh) {
+      const int i = r0 + g8 + 8 * rh, xx = x0 + 8 * nt + 2 * t4;
+      if (i < L) {
+        float gq[2], gk[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float xq = accQ[nt][2 * rh + e], xk = accK[nt][2 * rh + e];
+          gq[e] = l2 ? rq[i] * (xq - rq[i] * rq[i] * qv(i, xx + e) * PQ[i]) : xq;
+          gk[e] = l2 ? rk[i] * (xk - rk[i] * rk[i] * kv(i, xx + e) * PK[i]) : xk;
+        }
+        const int64_t off = ((trow0 + i) * H + h) * K + xx;
+        *reinterpret_cast<float2 *>(dq_dst + off) = make_float2(gq[0], gq[1]);
+        *reinterpret_cast<float2 *>(dk_dst + off) = make_float2(gk[0], gk[1]);
+      }
     }
-  });
-  cvisit(accK, [&](int, int r, int n, float x) {
-    const int i = r0 + r, xx = x0 + n;
-    if (i < L) {
-      const float gk = l2 ? rk[i] * (x - rk[i] * rk[i] * kv(i, xx) * PK[i]) : x;
-      dk_dst[((trow0 + i) * H + h) * K + xx] = gk;
-    }
-  });
+  }
   // ---- d gamma, then dg = reverse cumsum over the chunk; d beta
   if (warp == 0) {
     float d[2], dl = 0.f;
