@@ -1,8 +1,10 @@
 // gdn_api.cu -- the C ABI of libgdn: argument checks, then stream-ordered
 // launches.  No entry point allocates device memory or synchronises.
+#include <cuda.h>
 #include <math.h>
 
 #include <atomic>
+#include <initializer_list>
 
 #include "gdn_common.cuh"
 
@@ -15,11 +17,32 @@ std::atomic<int> g_force_wait_expiry{0};
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ECUDA; }
 
+// Buffers that the chunk kernels move with TMA, bulk copies or 16-byte
+// accesses must start on a 16-byte boundary; a view at an odd offset is refused
+// on the host instead of faulting on the device.  Null pointers pass.
+bool aligned16(std::initializer_list<const void *> ptrs) {
+  for (const void *p : ptrs)
+    if (reinterpret_cast<uintptr_t>(p) & 15u) return false;
+  return true;
+}
+
 // The chunk entry points encode TMA tensor maps with a driver call, which needs
 // a context current on the calling thread.  A thread whose first CUDA work this
-// is (a framework's worker thread, say) may have none: setting the thread's
-// device again makes that device's primary context current.
+// is (a framework's worker thread, say) may have none: then setting the
+// thread's device makes that device's primary context current.  A context the
+// caller made current is left in place.
 bool bind_context() {
+  using GetCurrentFn = CUresult (*)(CUcontext *);
+  static const GetCurrentFn get_current = [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    const bool ok = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+                        cudaSuccess &&
+                    q == cudaDriverEntryPointSuccess;
+    return ok ? reinterpret_cast<GetCurrentFn>(p) : nullptr;
+  }();
+  CUcontext ctx = nullptr;
+  if (get_current && get_current(&ctx) == CUDA_SUCCESS && ctx) return true;
   int dev = 0;
   return cudaGetDevice(&dev) == cudaSuccess && cudaSetDevice(dev) == cudaSuccess;
 }
@@ -78,6 +101,7 @@ int chunk_fwd_common(gdn_host::ChunkArgs &a, const uint16_t *q, const uint16_t *
   const bool has_tokens = (int64_t)B * T > 0;
   const bool gates = a.A_log ? (a.ga && a.gb && a.dt_bias) : (a.g && a.beta);
   if (has_tokens && (!q || !k || !v || !gates || !o)) return GDN_EINVAL;
+  if (!aligned16({q, k, v, o, initial_state, final_state, workspace})) return GDN_EINVAL;
   if (N == 0) return GDN_OK;
   const size_t need = gdn_host::chunk_workspace_bytes(B, T, H, HV, K, V, N, cu_seqlens != nullptr);
   if (need > 0 && (!workspace || workspace_bytes < need)) return GDN_EWORKSPACE;
@@ -141,6 +165,7 @@ int gdn_chunk_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const
   const bool has_tokens = (int64_t)B * T > 0;
   if (has_tokens && (!q || !k || !v || !g || !beta || !dout || !dq || !dk || !dv || !dg || !dbeta))
     return GDN_EINVAL;
+  if (!aligned16({q, k, v, dout, dht, initial_state, dq, dk, dh0, workspace})) return GDN_EINVAL;
   if (N == 0) return GDN_OK;
   const size_t need = gdn_host::chunk_bwd_workspace_bytes(B, T, H, HV, K, V, N, cu_seqlens != nullptr);
   if (!workspace || workspace_bytes < need) return GDN_EWORKSPACE;

@@ -139,7 +139,11 @@ size_t gdn_chunk_fwd_workspace_size(int B, int T, int H, int HV, int K, int V,
  *                   (NULL when that size is 0)
  * Chunks restart at every sequence start; the last chunk of a sequence may be
  * partial.  A sequence of length 0 writes final_state = initial_state (or 0).
- * N > 65535 returns GDN_EUNSUPPORTED.
+ * N > 65535 returns GDN_EUNSUPPORTED.  q, k, v, o, initial_state, final_state
+ * and the workspace move by TMA, bulk copies and 16-byte accesses: each must
+ * start on a 16-byte boundary (a view at an odd offset returns GDN_EINVAL
+ * before any launch).  The call may be the first CUDA work of its thread: if
+ * no context is current, it makes the current device's primary context current.
  */
 int gdn_chunk_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                   const float *g, const float *beta, float scale,
@@ -241,8 +245,10 @@ size_t gdn_chunk_bwd_workspace_size(int B, int T, int H, int HV, int K, int V,
  * shares on `stream`).  Products run on the tensor cores with computed
  * operands split into bf16 hi + lo parts (relative error near 2^-17 per
  * product, fp32 accumulation).  Every sum has a fixed order, so two runs on
- * the same inputs agree bit for bit.  Errors as gdn_chunk_fwd; the workspace
- * must hold gdn_chunk_bwd_workspace_size() bytes.
+ * the same inputs agree bit for bit.  Errors as gdn_chunk_fwd; q, k, v, do,
+ * dht, initial_state, dq, dk, dh0 and the workspace must start on a 16-byte
+ * boundary (else GDN_EINVAL); the workspace must hold
+ * gdn_chunk_bwd_workspace_size() bytes.
  */
 int gdn_chunk_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                   const float *g, const float *beta, float scale,

@@ -66,6 +66,30 @@ def test_chunk_fwd_host_validation(lib):
     assert _chunk(lib, N=0, B=0, T=0) == gdn.GDN_OK           # nothing to do, nothing launched
 
 
+def test_chunk_misaligned_buffers_refused_before_launch(lib):
+    """The prefill and backward move q, k, v, o, the states and their gradients
+    with TMA, bulk copies and 16-byte accesses: a buffer that is only 8-byte
+    aligned is refused on the host (the fake pointers are never dereferenced)."""
+    ok = ctypes.c_void_p(64)
+    odd = ctypes.c_void_p(64 + 8)
+    base = dict(q=ok, k=ok, v=ok, g=ok, beta=ok, o=ok, ws=ok, wsb=1 << 40)
+    for name in ("q", "k", "v", "o", "h0", "ht", "ws"):
+        kw = dict(base)
+        kw[name] = odd
+        assert _chunk(lib, **kw) == gdn.GDN_EINVAL, name
+    F = ctypes.c_float
+
+    def bwd(**kw):
+        a = dict(q=ok, k=ok, v=ok, g=ok, beta=ok, h0=NULL, cu=NULL, do=ok, dht=NULL, dq=ok, dk=ok, dv=ok, dg=ok,
+                 dbeta=ok, dh0=NULL, ws=ok)
+        a.update(kw)
+        return lib.gdn_chunk_bwd(a["q"], a["k"], a["v"], a["g"], a["beta"], F(-1.0), a["h0"], a["cu"], 1, 1, 8, 2,
+                                 4, 128, 128, 1, a["do"], a["dht"], a["dq"], a["dk"], a["dv"], a["dg"], a["dbeta"],
+                                 a["dh0"], a["ws"], ctypes.c_size_t(1 << 40), NULL, NULL)
+    for name in ("q", "k", "v", "do", "dht", "h0", "dq", "dk", "dh0", "ws"):
+        assert bwd(**{name: odd}) == gdn.GDN_EINVAL, name
+
+
 def test_chunk_fwd_gated_host_validation(lib):
     fake = ctypes.c_void_p(16)
 
