@@ -100,23 +100,40 @@ def gating_bytes(n_elem):
 # ------------------------------------------------------------------- clocks
 
 class Clocks:
+    """nvidia-smi sampling every 10 ms with a timestamp per sample.  It starts
+    before the warm-up (the tool takes a while to come up) and only the samples
+    stamped inside the timed region count; `window()` marks that region."""
+
     def __init__(self, index):
         self.index = index
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
 
     def start(self):
         try:
             fd, self.path = tempfile.mkstemp(prefix="gdn_clocks_", suffix=".csv")
             os.close(fd)
-            q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+            q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "10"],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            deadline = time.time() + 5.0
+            while time.time() < deadline and os.path.getsize(self.path) == 0:
+                time.sleep(0.01)
         except Exception:
             self.proc = None
+
+    def window(self, t0, t1):
+        self.t0, self.t1 = t0, t1
+
+    @staticmethod
+    def _stamp(text):
+        # "YYYY/MM/DD HH:MM:SS.mmm", local time
+        day, frac = text.rsplit(".", 1) if "." in text else (text, "0")
+        return time.mktime(time.strptime(day, "%Y/%m/%d %H:%M:%S")) + float("0." + frac)
 
     def stop(self):
         if self.proc is None:
@@ -126,25 +143,26 @@ class Clocks:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-        sm, mx, reasons = [], 0.0, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for line in open(self.path):
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx = max(mx, float(f[2]))
+                rows.append((self._stamp(f[0]), float(f[2]), float(f[3]), f[6:10]))
             except ValueError:
                 continue
-            for n, val in zip(names, f[5:9]):
-                if val.lower().startswith("active"):
-                    reasons.add(n)
         os.unlink(self.path)
-        if not sm:
+        if not rows:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        inside = [r for r in rows if self.t0 is not None and self.t0 <= r[0] <= self.t1]
+        use = inside or [min(rows, key=lambda r: abs(r[0] - (self.t0 or r[0])))]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in use for n, val in zip(names, r[3]) if val.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(inside),
+                "note": "nvidia-smi every 10 ms; samples stamped inside the timed region"
+                        + ("" if inside else " (none: the nearest one is reported)")}
 
 
 # ---------------------------------------------------------------- reference
@@ -282,6 +300,8 @@ def run_ours(args, rank, world, local_rank):
         if world > 1:
             dist.barrier()
 
+    clocks = Clocks(local_rank)
+    clocks.start()
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize(dev)
@@ -289,16 +309,17 @@ def run_ours(args, rank, world, local_rank):
            for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    clocks = Clocks(local_rank)
     barrier()
     torch.cuda.synchronize(dev)
-    clocks.start()
+    wall0 = time.time()
     t_start.record(stream)
     for i in range(args.steps):
         step(evs[i])
     t_end.record(stream)
     torch.cuda.synchronize(dev)
+    wall1 = time.time()
     barrier()
+    clocks.window(wall0, wall1)
     clk = clocks.stop()
     ms = t_start.elapsed_time(t_end)
     chunk_ms = [a_.elapsed_time(b_) for a_, b_ in evs]
