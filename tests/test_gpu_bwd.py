@@ -135,15 +135,19 @@ def test_bwd_k128_without_l2norm_or_state_gradients():
     _run(case, l2=False, with_dht=False, seed=8)
 
 
-@pytest.mark.parametrize("K", [64, 128])
-def test_bwd_four_value_heads_per_key_head_and_repeatable(K):
-    # One gradient CTA walks the four value heads of its key head and adds
-    # their dq, dk shares in head order: parity with the oracle, and a second
-    # call on the same inputs returns the same bits in every output.
+@pytest.mark.parametrize("K,varlen", [(64, True), (128, True), (128, False)])
+def test_bwd_four_value_heads_per_key_head_and_repeatable(K, varlen):
+    # Each value head's dq, dk share is stored on its own and the three later
+    # ones are added in head order: parity with the oracle, and a second call
+    # on the same inputs returns the same bits in every output.  Dense input
+    # takes no memsets: every row of dq, dk and of the shares is written.
     import gated_deltanet_chunked_chunk_gb300 as gdn
     lengths = [70, 1, 130, 64]
-    case = W.prefill_case("bwd_g4", 49, 1, sum(lengths), 1, 4, K, 128, init="all",
-                          cu_seqlens=W.cu_from_lengths(lengths))
+    if varlen:
+        case = W.prefill_case("bwd_g4", 49, 1, sum(lengths), 1, 4, K, 128, init="all",
+                              cu_seqlens=W.cu_from_lengths(lengths))
+    else:
+        case = W.prefill_case("bwd_g4_dense", 50, 2, 133, 1, 4, K, 128, init="all")
     _run(case, seed=9)
     g, beta = P.oracle_gates(case)
     gen = torch.Generator().manual_seed(1009)
@@ -151,7 +155,8 @@ def test_bwd_four_value_heads_per_key_head_and_repeatable(K):
     dht = torch.randn(case.N, case.HV, case.K, case.V, generator=gen).to(DEV)
     d = lambda t: t.to(DEV).contiguous()
     args = (d(case.q), d(case.k), d(case.v), d(g), d(beta), do)
-    kw = dict(initial_state=d(case.initial_state), cu_seqlens=d(case.cu_seqlens), dht=dht)
+    kw = dict(initial_state=d(case.initial_state), dht=dht,
+              cu_seqlens=None if case.cu_seqlens is None else d(case.cu_seqlens))
     first = gdn.gdn_chunk_bwd(*args, **kw)
     second = gdn.gdn_chunk_bwd(*args, **kw)
     for a, b in zip(first, second):
