@@ -572,25 +572,35 @@ __global__ void __launch_bounds__(NTH, 4) chunk_prep_kernel(
 }
 
 // ============================================================== walk kernel
-// Nine warps.  Every product runs on tcgen05 with fp32 accumulators in TMEM.
+// Eleven warps.  Every product runs on tcgen05 with fp32 accumulators in TMEM.
 // A thread needs about 100 cycles to issue one tcgen05.mma while issues from
 // different warps overlap, and every wait on an mbarrier costs several hundred
-// cycles while the tensor core and TMA keep shared memory busy; so the compute
-// warps issue all products themselves (the serial ones split over several
-// warps into partial accumulators that the epilogues add up), and completions
-// that are always needed together share one barrier.
-//  * Compute warps 0-7: thread (lane group w & 3, column half w >> 2) owns TMEM
-//    lane r = 32 (w & 3) + lane and 16 of the slice's 32 columns, and holds the
-//    fp32 state h[r][16 columns] in registers.  Per chunk c:
-//      [W; Q] [h_hi | h_lo] -> ACC1 (4 partials, warps 0-3) and
-//      u(c) = Ts V -> ACC4 (warp 6);
-//      meanwhile the output of chunk c - 1 from ACC3 and Q h;
-//      lanes 0-63: v_new = beta v + u - W h -> s v_new, v_new (bf16 hi | lo);
-//      lanes 64-127: e^gamma rq (Q h), kept in registers for the output;
-//      then K^T [s v_new hi | lo] -> ACC2 (2 partials, warps 0-1),
-//      [P_hi; P_lo] [v_new hi | lo] -> ACC3 (warp 2);
-//      h <- e^{gamma_L} h + ACC2, written back as [h_hi | h_lo].
+// cycles while the tensor core and TMA keep shared memory busy; so the serial
+// products are split over several issuing warps into partial accumulators
+// that the epilogues add up, the products off the serial chain are issued by
+// warps of their own, and completions that are always needed together share
+// one barrier.
+//
+// Products whose rows are the chunk's 64 tokens use M = 64.  Row i of such an
+// accumulator sits in TMEM lane 32 (i / 16) + i % 16, so each of the four lane
+// quarters holds 16 rows and the token-row epilogues run on all four SM
+// sub-partitions (an M = 128 accumulator would put them in lanes 0-63, which
+// only two of them reach).
+//  * Compute warps 0-7.  Token-row work: thread t of warp w takes row
+//    16 (w & 3) + t % 16 and the 8 columns 16 (w >> 2) + 8 (t / 16) .. + 7 of
+//    the slice's 32.  State work: the thread owns TMEM lane r = 32 (w & 3) + t
+//    (key r) and the 16 columns 16 (w >> 2) .. + 15, and holds the fp32 state
+//    h[r][16 columns] in registers.  Per chunk c:
+//      W [h_hi | h_lo] -> ACC1 (4 partials, warps 0-3) and u(c) = Ts V -> ACC4
+//      (warp 6); meanwhile the output of chunk c - 1;
+//      v_new = beta v + u - W h -> s v_new, v_new (bf16 hi | lo);
+//      K^T [s v_new hi | lo] -> ACC2 (2 partials, warps 0-1);
+//      h <- e^{gamma_L} h + ACC2, written back as [h_hi | h_lo], and
+//      e^gamma rq (Q h) of chunk c from ACCQ into registers for its output.
 //  * Warp 8: TMA / bulk loads of chunk c + 2 into the stage chunk c released.
+//  * Warps 9 and 10, off the serial chain: Q [h_hi | h_lo] -> ACCQ (warp 9,
+//    once W h is done), then P_hi [v_new hi | lo] -> ACC3 (warp 9) and
+//    P_lo [v_new hi | lo] -> ACC3L (warp 10) once the state product is done.
 template <int K>
 struct WalkLay {
   static constexpr int KA = K / 64;
@@ -604,23 +614,23 @@ struct WalkLay {
   static constexpr int OFF_H = NS * STAGE;               // [K][64] bf16 (h hi | h lo), MN-major SW128
   static constexpr int OFF_VS = OFF_H + K * 128;         // [64][64] bf16 (s v_new hi | lo), MN-major SW128
   static constexpr int OFF_VN = OFF_VS + 8192;           // [64][64] bf16 (v_new hi | lo), MN-major SW128
-  static constexpr int OFF_Z = OFF_VN + 8192;            // 8 KB of zeros: missing rows 64-127 of an M = 128 operand
-  static constexpr int XROW = 36;
-  static constexpr int OFF_X = OFF_Z + 8192;             // fp32 [64][XROW]: P_hi v_new of the output
-  static constexpr int OFF_BAR = OFF_X + 64 * XROW * 4;
+  static constexpr int OFF_Z = OFF_VN + 8192;            // 8 KB of zeros: keys 64-127 of the state product for K = 64
+  static constexpr int OFF_BAR = OFF_Z + 8192;
   static constexpr int NBAR = 12;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr uint32_t TX = STAGE;                  // every byte of a stage is loaded per chunk
-  // TMEM columns: ACC1 four partials of 64, ACC2 two, ACC3 and ACC4 one each.
-  static constexpr uint32_t ACC1 = 0, ACC2 = 256, ACC3 = 384, ACC4 = 448;
+  // TMEM columns: ACC1 four M = 64 partials of 64 columns; ACC2 (M = 128, two
+  // partials) reuses ACC1's first two, which the v_new epilogue has read before
+  // the state product is issued; ACC3, ACC3L, ACC4 and ACCQ one M = 64 block each.
+  static constexpr uint32_t ACC1 = 0, ACC2 = 0, ACC3 = 256, ACC3L = 320, ACC4 = 384, ACCQ = 448;
   static constexpr uint32_t TMEM_COLS = 512;
   static_assert(STAGE % 1024 == 0 && OFF_H % 1024 == 0 && OFF_VS % 1024 == 0 && OFF_Z % 1024 == 0,
                 "swizzled tile alignment");
   static_assert(BYTES + 1024 <= 232448, "shared memory budget (227 KB per CTA)");
 };
 constexpr int WALK_COMPUTE = 256;
-constexpr int WALK_THREADS = WALK_COMPUTE + 32;
+constexpr int WALK_THREADS = WALK_COMPUTE + 96;
 
 template <int K>
 __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
@@ -633,7 +643,6 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
   using R = Rec<K>;
   constexpr int KA = K / 64;
   constexpr int NS = Ly::NS;
-  constexpr int XROW = Ly::XROW;
   constexpr int TSO = Ly::RR + (R::TS - R::PH);          // Ts^T within a stage
   constexpr int SCO = Ly::RR + (R::SC - R::PH);          // scalars within a stage
   extern __shared__ unsigned char smem_raw[];
@@ -654,30 +663,35 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
   uint32_t *misc = reinterpret_cast<uint32_t *>(sm + Ly::OFF_MISC);
   volatile uint32_t *abort_flag = misc + 1;
   // Two-slot barriers, slot c & 1 serving chunk c:
-  //   FULL(c):  the loads of chunk c landed and the output product of chunk
-  //             c - 1 is done (producer arrive with the byte count, plus the
-  //             output product's commit; thread 0 stands in for the missing
-  //             chunk -1, and for chunk NC after the loop);
-  //   CDONE(c): the compute warps and the first two products of chunk c no
-  //             longer read the stage.
-  // Single-slot: M1 (phase c: u(c) and the four parts of [W; Q] h of chunk c
-  // are done) and M2 (phase c: K^T (s v_new) of chunk c is done).
+  //   FULL(c):  the loads of chunk c landed (the producer's arrive with the
+  //             byte count; nothing else, so that a drain after an abort
+  //             waits for the copies alone);
+  //   OUT(c):   the two output products of chunk c are done (the commits of
+  //             warps 9 and 10);
+  //   CDONE(c): no warp and no product but the output products (which OUT(c)
+  //             covers) reads chunk c's stage any more.
+  // Single-slot: M1 (phase c: u(c) and the four parts of W h of chunk c are
+  // done), M2 (phase c: K^T (s v_new) of chunk c is done) and QD (phase c:
+  // Q h of chunk c is done).
   enum { FULL = 0, CDONE = 1 };
   auto bar = [&](int kind, int b) { return sb + Ly::OFF_BAR + 8 * (2 * kind + b); };
   const uint32_t b_m1 = sb + Ly::OFF_BAR + 32, b_m2 = sb + Ly::OFF_BAR + 40, b_drain = sb + Ly::OFF_BAR + 48;
   const uint32_t b_never = sb + Ly::OFF_BAR + 56;  // nothing arrives: the testing hook's wait
+  const uint32_t b_qd = sb + Ly::OFF_BAR + 64;
+  auto b_out = [&](int c) { return sb + Ly::OFF_BAR + 72 + 8 * (c & 1); };
   if (tid == 0) {
     for (int b = 0; b < 2; ++b) {
-      mbar_init(bar(FULL, b), 2);
+      mbar_init(bar(FULL, b), 1);
       mbar_init(bar(CDONE, b), 1);
+      mbar_init(sb + Ly::OFF_BAR + 72 + 8 * b, 2);
     }
     mbar_init(b_m1, 5);
     mbar_init(b_m2, 2);
-    mbar_init(b_drain, 5);
+    mbar_init(b_drain, 7);
     mbar_init(b_never, 1);
+    mbar_init(b_qd, 1);
     misc[1] = 0;
     mbar_fence_init();
-    mbar_arrive(bar(FULL, 0));  // no output product precedes chunk 0
   }
   for (int e = tid; e < 8192 / 16; e += WALK_THREADS)
     reinterpret_cast<uint4 *>(sm + Ly::OFF_Z)[e] = make_uint4(0, 0, 0, 0);
@@ -714,25 +728,27 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
   };
   auto waitb = [&](uint32_t b, uint32_t parity) { return waitl(b, parity, kWaitLimit); };
   auto waitc = [&](int kind, int c) { return waitb(bar(kind, c & 1), (c >> 1) & 1); };
+  auto wait_out = [&](int c) { return waitb(b_out(c), (c >> 1) & 1); };
   auto chunk_rows = [&](int c) {
     const int64_t rem = len - static_cast<int64_t>(c) * C;
     return static_cast<int>(rem < C ? rem : C);
   };
   const int64_t sbase = (static_cast<int64_t>(n) * HV + hv) * K;
-  float *X = reinterpret_cast<float *>(sm + Ly::OFF_X);
 
   if (warp < 8) {
     // ------------------------------------------------------- compute warps
-    const int r = 32 * (warp & 3) + lane;                // TMEM lane
-    const int hs = warp >> 2;                            // column half: columns 16 hs .. 16 hs + 15
-    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    const int q4 = warp & 3;                             // TMEM lane quarter
+    const int hs = warp >> 2;                            // column half of the state work
+    const int r = 32 * q4 + lane;                        // state work: TMEM lane, key r
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
     const bool krow = r < K;
-    float hr[16], qh[16];
+    const int ti = 16 * q4 + (lane & 15);                // token-row work: row ti, columns tc .. tc + 7
+    const int tc = 16 * hs + 8 * (lane >> 4);
+    float hr[16], qh[8];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      hr[j] = (h0 && krow) ? h0[(sbase + r) * V + vt0 + 16 * hs + j] : 0.f;
-      qh[j] = 0.f;
-    }
+    for (int j = 0; j < 16; ++j) hr[j] = (h0 && krow) ? h0[(sbase + r) * V + vt0 + 16 * hs + j] : 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) qh[j] = 0.f;
     // Row r of h -> columns [16 hs, 16 hs + 16) of the hi and lo halves of the
     // MN-major SW128 H tile.
     auto write_h = [&]() {
@@ -752,80 +768,45 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
         *reinterpret_cast<uint4 *>(row + (((4 + chh) ^ (r & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
     };
-    // Sum of the hi and lo column blocks of NP partial accumulators at `base`.
-    auto sum_partials = [&](uint32_t base, int np, float *acc) {
-#pragma unroll
-      for (int j = 0; j < 16; ++j) acc[j] = 0.f;
-      for (int p = 0; p < np; p += 2) {
-        uint32_t x0[16], y0[16], x1[16], y1[16];
-        tmem_ld16_issue(tl + base + 64 * p + 16 * hs, x0);
-        tmem_ld16_issue(tl + base + 64 * p + 32 + 16 * hs, y0);
-        tmem_ld16_issue(tl + base + 64 * (p + 1) + 16 * hs, x1);
-        tmem_ld16_issue(tl + base + 64 * (p + 1) + 32 + 16 * hs, y1);
-        tmem_ld_wait16(x0);
-        tmem_ld_wait16(y0);
-        tmem_ld_wait16(x1);
-        tmem_ld_wait16(y1);
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          acc[j] += (__uint_as_float(x0[j]) + __uint_as_float(y0[j])) + (__uint_as_float(x1[j]) + __uint_as_float(y1[j]));
-      }
-    };
-    // Output of chunk c, from ACC3 (P_hi rows in lanes 0-63, P_lo rows in
-    // lanes 64-127) and the e^gamma rq Q h that lanes 64-127 hold; the caller
-    // has seen the output product complete.
+    // Output of chunk c for row ti, columns tc .. tc + 7: ACC3 holds
+    // P_hi [v_new hi | lo], ACC3L P_lo [v_new hi | lo] (of which the v_new hi
+    // block is used), qh the e^gamma rq Q h of chunk c; the caller has seen
+    // both output products complete.
     auto output = [&](int c, bool go) {
-      if (go && r < 64) {
+      if (go) {
         tc_fence_after();
-        uint32_t a[16], b[16];
-        tmem_ld16_issue(tl + Ly::ACC3 + 16 * hs, a);
-        tmem_ld16_issue(tl + Ly::ACC3 + 32 + 16 * hs, b);
-        tmem_ld_wait16(a);
-        tmem_ld_wait16(b);
-        float *x = X + r * XROW + 16 * hs;
+        uint32_t a[8], b[8], l[8];
+        tmem_ld8x2_issue(tl + Ly::ACC3 + 16 * hs, a);
+        tmem_ld8x2_issue(tl + Ly::ACC3 + 32 + 16 * hs, b);
+        tmem_ld8x2_issue(tl + Ly::ACC3L + 16 * hs, l);
+        tmem_ld_wait8(a);
+        tmem_ld_wait8(b);
+        tmem_ld_wait8(l);
+        if (o && ti < chunk_rows(c)) {
+          const int64_t trow = tok0 + static_cast<int64_t>(c) * C + ti;
+          uint32_t w[4];
 #pragma unroll
-        for (int j = 0; j < 16; j += 4)
-          *reinterpret_cast<float4 *>(x + j) =
-              make_float4(__uint_as_float(a[j]) + __uint_as_float(b[j]), __uint_as_float(a[j + 1]) + __uint_as_float(b[j + 1]),
-                          __uint_as_float(a[j + 2]) + __uint_as_float(b[j + 2]), __uint_as_float(a[j + 3]) + __uint_as_float(b[j + 3]));
-      }
-      named_bar_sync(1, WALK_COMPUTE);
-      if (go && r >= 64) {
-        tc_fence_after();
-        const int i = r - 64;
-        uint32_t a[16];
-        tmem_ld16_issue(tl + Ly::ACC3 + 16 * hs, a);
-        tmem_ld_wait16(a);
-        if (o && i < chunk_rows(c)) {
-          const float *x = X + i * XROW + 16 * hs;
-          const int64_t trow = tok0 + static_cast<int64_t>(c) * C + i;
-          uint4 *dst = reinterpret_cast<uint4 *>(o + (trow * HV + hv) * V + vt0 + 16 * hs);
-#pragma unroll
-          for (int m = 0; m < 2; ++m) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int j = 8 * m + 2 * e;
-              w[e] = pack_bf16(scale * (qh[j] + x[j] + __uint_as_float(a[j])),
-                               scale * (qh[j + 1] + x[j + 1] + __uint_as_float(a[j + 1])));
-            }
-            dst[m] = make_uint4(w[0], w[1], w[2], w[3]);
+          for (int e = 0; e < 4; ++e) {
+            const int j = 2 * e;
+            w[e] = pack_bf16(scale * (qh[j] + (__uint_as_float(a[j]) + __uint_as_float(b[j])) + __uint_as_float(l[j])),
+                             scale * (qh[j + 1] + (__uint_as_float(a[j + 1]) + __uint_as_float(b[j + 1])) +
+                                      __uint_as_float(l[j + 1])));
           }
+          *reinterpret_cast<uint4 *>(o + (trow * HV + hv) * V + vt0 + tc) = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
       return go;
     };
-    // u(c) = Ts V into ACC4, completing on phase c of M1; Ts^T is the
-    // MN-major A operand whose rows 64-127 come from the zero block.
+    // u(c) = Ts V into ACC4 (M = 64), completing on phase c of M1; Ts^T is
+    // the MN-major A operand.
     auto issue_u = [&](int c) {
       const int s = c % NS;
       const uint32_t st = sb + s * Ly::STAGE;
       tc_fence_after();
-      constexpr uint32_t id4 = umma_idesc_bf16(128, 64, 1, 1);
-      const uint32_t lbo = static_cast<uint32_t>(Ly::OFF_Z - s * Ly::STAGE - TSO);
+      constexpr uint32_t id4 = umma_idesc_bf16(64, 64, 1, 1);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t a = umma_desc_sw128_mn(st + TSO + kk * 2048, lbo);
+        const uint64_t a = umma_desc_sw128_mn(st + TSO + kk * 2048, 8192);
         const uint64_t b = umma_desc_sw128_mn(st + Ly::VB + kk * 2048, 8192);
         umma_bf16(tmem + Ly::ACC4, a, b, id4, kk > 0 ? 1u : 0u);
       }
@@ -846,13 +827,13 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
 #pragma unroll
         for (int j = 0; j < 16; j += 4) *reinterpret_cast<float4 *>(dst + j) = make_float4(hr[j], hr[j + 1], hr[j + 2], hr[j + 3]);
       }
-      // also: the output product of chunk c - 1 is done.  The testing hook
-      // replaces the first wait by one on a barrier nothing completes.
+      // The loads of chunk c.  The testing hook replaces the first wait by one
+      // on a barrier nothing completes.
       go = ((force_expiry && c == 0) ? waitl(b_never, 0, kTestWaitLimit) : waitc(FULL, c)) && go;
-      // [W; Q] [h_hi | h_lo]: warp p < 4 takes k-steps [p KA, p KA + KA).
+      // W [h_hi | h_lo] (M = 64): warp p < 4 takes k-steps [p KA, p KA + KA).
       if (warp < 4 && lane == 0 && go) {
         tc_fence_after();
-        constexpr uint32_t id1 = umma_idesc_bf16(128, 64, 0, 1);
+        constexpr uint32_t id1 = umma_idesc_bf16(64, 64, 0, 1);
 #pragma unroll
         for (int m = 0; m < KA; ++m) {
           const int kk = warp * KA + m;
@@ -862,57 +843,60 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
         }
         umma_commit(b_m1);
       } else if (warp == 6 && lane == 0 && go) {
-        issue_u(c);  // ACC4 was last read for chunk c - 1, before its barrier F
+        issue_u(c);  // ACC4 was last read for chunk c - 1, before its v_new barrier
       }
       __syncwarp();
       // Output of the previous chunk while these products run.
-      if (c >= 1) go = output(c - 1, go);
-      go = waitb(b_m1, c & 1) && go;  // [W; Q] h and u of this chunk
+      if (c >= 1) {
+        go = wait_out(c - 1) && go;
+        go = output(c - 1, go);
+      }
+      go = waitb(b_m1, c & 1) && go;  // W h and u of this chunk
       const float dL = go ? rsc[RS_DL] : 0.f;
+      float og = 0.f;
       if (go) {
+        // v_new = beta v + u - W (h_hi + h_lo) for row ti; s v_new and v_new
+        // as bf16 hi | lo.
         tc_fence_after();
-        float wh[16];
-        sum_partials(Ly::ACC1, 4, wh);
-        if (r < 64) {
-          // v_new = beta v + u - W (h_hi + h_lo); s v_new and v_new as bf16 hi | lo.
-          const int i = r;
-          uint32_t u[16];
-          tmem_ld16_issue(tl + Ly::ACC4 + vhalf + 16 * hs, u);
-          const float bt = rsc[RS_BET + i], sv = rsc[RS_SV + i];
-          const int vc = (vhalf + 16 * hs) >> 3;
-          uint4 vv[2];
+        const int i = ti;
+        uint32_t pw[8][8], u[8];
 #pragma unroll
-          for (int m = 0; m < 2; ++m)
-            vv[m] = *reinterpret_cast<const uint4 *>(stp + Ly::VB + i * 128 + (((vc + m) ^ (i & 7)) << 4));
-          tmem_ld_wait16(u);
-          unsigned char *vsr = sm + Ly::OFF_VS + (i >> 3) * 1024 + (i & 7) * 128;
-          unsigned char *vnr = sm + Ly::OFF_VN + (i >> 3) * 1024 + (i & 7) * 128;
-#pragma unroll
-          for (int m = 0; m < 2; ++m) {
-            const uint32_t vw[4] = {vv[m].x, vv[m].y, vv[m].z, vv[m].w};
-            uint32_t yh[4], yl[4], xh[4], xl[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int j = 8 * m + 2 * e;
-              const float x0 = fmaf(bt, bf16lo_f(vw[e]), __uint_as_float(u[j])) - wh[j];
-              const float x1 = fmaf(bt, bf16hi_f(vw[e]), __uint_as_float(u[j + 1])) - wh[j + 1];
-              xh[e] = pack_bf16(x0, x1);
-              xl[e] = pack_bf16(x0 - bf16lo_f(xh[e]), x1 - bf16hi_f(xh[e]));
-              const float y0 = sv * x0, y1 = sv * x1;
-              yh[e] = pack_bf16(y0, y1);
-              yl[e] = pack_bf16(y0 - bf16lo_f(yh[e]), y1 - bf16hi_f(yh[e]));
-            }
-            const int chh = 2 * hs + m;
-            *reinterpret_cast<uint4 *>(vsr + ((chh ^ (i & 7)) << 4)) = make_uint4(yh[0], yh[1], yh[2], yh[3]);
-            *reinterpret_cast<uint4 *>(vsr + (((4 + chh) ^ (i & 7)) << 4)) = make_uint4(yl[0], yl[1], yl[2], yl[3]);
-            *reinterpret_cast<uint4 *>(vnr + ((chh ^ (i & 7)) << 4)) = make_uint4(xh[0], xh[1], xh[2], xh[3]);
-            *reinterpret_cast<uint4 *>(vnr + (((4 + chh) ^ (i & 7)) << 4)) = make_uint4(xl[0], xl[1], xl[2], xl[3]);
-          }
-        } else {
-          const float og = rsc[RS_OG + r - 64];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) qh[j] = og * wh[j];
+        for (int p = 0; p < 4; ++p) {
+          tmem_ld8x2_issue(tl + Ly::ACC1 + 64 * p + 16 * hs, pw[2 * p]);
+          tmem_ld8x2_issue(tl + Ly::ACC1 + 64 * p + 32 + 16 * hs, pw[2 * p + 1]);
         }
+        tmem_ld8x2_issue(tl + Ly::ACC4 + vhalf + 16 * hs, u);
+        const float bt = rsc[RS_BET + i], sv = rsc[RS_SV + i];
+        og = rsc[RS_OG + i];
+        const uint4 vv = *reinterpret_cast<const uint4 *>(stp + Ly::VB + i * 128 + ((((vhalf + tc) >> 3) ^ (i & 7)) << 4));
+#pragma unroll
+        for (int p = 0; p < 8; ++p) tmem_ld_wait8(pw[p]);
+        tmem_ld_wait8(u);
+        float wh[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          wh[j] = ((__uint_as_float(pw[0][j]) + __uint_as_float(pw[1][j])) + (__uint_as_float(pw[2][j]) + __uint_as_float(pw[3][j]))) +
+                  ((__uint_as_float(pw[4][j]) + __uint_as_float(pw[5][j])) + (__uint_as_float(pw[6][j]) + __uint_as_float(pw[7][j])));
+        const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
+        uint32_t yh[4], yl[4], xh[4], xl[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j = 2 * e;
+          const float x0 = fmaf(bt, bf16lo_f(vw[e]), __uint_as_float(u[j])) - wh[j];
+          const float x1 = fmaf(bt, bf16hi_f(vw[e]), __uint_as_float(u[j + 1])) - wh[j + 1];
+          xh[e] = pack_bf16(x0, x1);
+          xl[e] = pack_bf16(x0 - bf16lo_f(xh[e]), x1 - bf16hi_f(xh[e]));
+          const float y0 = sv * x0, y1 = sv * x1;
+          yh[e] = pack_bf16(y0, y1);
+          yl[e] = pack_bf16(y0 - bf16lo_f(yh[e]), y1 - bf16hi_f(yh[e]));
+        }
+        const int chh = tc >> 3;
+        unsigned char *vsr = sm + Ly::OFF_VS + (i >> 3) * 1024 + (i & 7) * 128;
+        unsigned char *vnr = sm + Ly::OFF_VN + (i >> 3) * 1024 + (i & 7) * 128;
+        *reinterpret_cast<uint4 *>(vsr + ((chh ^ (i & 7)) << 4)) = make_uint4(yh[0], yh[1], yh[2], yh[3]);
+        *reinterpret_cast<uint4 *>(vsr + (((4 + chh) ^ (i & 7)) << 4)) = make_uint4(yl[0], yl[1], yl[2], yl[3]);
+        *reinterpret_cast<uint4 *>(vnr + ((chh ^ (i & 7)) << 4)) = make_uint4(xh[0], xh[1], xh[2], xh[3]);
+        *reinterpret_cast<uint4 *>(vnr + (((4 + chh) ^ (i & 7)) << 4)) = make_uint4(xl[0], xl[1], xl[2], xl[3]);
       }
       tc_fence_before();
       fence_proxy_async_smem();
@@ -931,27 +915,31 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
           umma_bf16(tmem + Ly::ACC2 + 64 * warp, a, b, id2, m > 0 ? 1u : 0u);
         }
         umma_commit(b_m2);
-      } else if (warp == 2 && lane == 0 && go) {
-        // [P_hi; P_lo] [v_new hi | lo], completing on FULL(c + 1).
-        tc_fence_after();
-        constexpr uint32_t id3 = umma_idesc_bf16(128, 64, 0, 1);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t a = umma_desc_sw128(st + Ly::RR + kk * 32);
-          const uint64_t b = umma_desc_sw128_mn(sb + Ly::OFF_VN + kk * 2048, 8192);
-          umma_bf16(tmem + Ly::ACC3, a, b, id3, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(bar(FULL, (c + 1) & 1));
       }
       __syncwarp();
       go = waitb(b_m2, c & 1) && go;
-      if (tid == 0 && go) mbar_arrive(bar(CDONE, c & 1));  // nothing of this stage is read any more
+      go = waitb(b_qd, c & 1) && go;  // Q h: it read the stage's Q tile and the H tile
+      if (tid == 0 && go) mbar_arrive(bar(CDONE, c & 1));
       if (go) {
         tc_fence_after();
-        float dh[16];
-        sum_partials(Ly::ACC2, 2, dh);
+        uint32_t x0[16], y0[16], x1[16], y1[16], qa[8], qb[8];
+        tmem_ld16_issue(tl + Ly::ACC2 + 16 * hs, x0);
+        tmem_ld16_issue(tl + Ly::ACC2 + 32 + 16 * hs, y0);
+        tmem_ld16_issue(tl + Ly::ACC2 + 64 + 16 * hs, x1);
+        tmem_ld16_issue(tl + Ly::ACC2 + 96 + 16 * hs, y1);
+        tmem_ld8x2_issue(tl + Ly::ACCQ + 16 * hs, qa);
+        tmem_ld8x2_issue(tl + Ly::ACCQ + 32 + 16 * hs, qb);
+        tmem_ld_wait16(x0);
+        tmem_ld_wait16(y0);
+        tmem_ld_wait16(x1);
+        tmem_ld_wait16(y1);
+        tmem_ld_wait8(qa);
+        tmem_ld_wait8(qb);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) hr[j] = fmaf(dL, hr[j], dh[j]);
+        for (int j = 0; j < 16; ++j)
+          hr[j] = fmaf(dL, hr[j], (__uint_as_float(x0[j]) + __uint_as_float(y0[j])) + (__uint_as_float(x1[j]) + __uint_as_float(y1[j])));
+#pragma unroll
+        for (int j = 0; j < 8; ++j) qh[j] = og * (__uint_as_float(qa[j]) + __uint_as_float(qb[j]));
         write_h();
       }
       tc_fence_before();
@@ -959,10 +947,7 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
       named_bar_sync(1, WALK_COMPUTE);
     }
     if (NC > 0) {
-      // The output product of the last chunk completes on FULL(NC), which no
-      // load feeds: thread 0 stands in for the producer.
-      if (tid == 0) mbar_arrive(bar(FULL, NC & 1));
-      go = waitc(FULL, NC) && go;
+      go = wait_out(NC - 1) && go;
       go = output(NC - 1, go);
     }
     if (lane == 0 && *abort_flag) {
@@ -979,6 +964,54 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
       for (int j = 0; j < 16; j += 4)
         *reinterpret_cast<float4 *>(ht + (sbase + r) * V + vt0 + 16 * hs + j) =
             make_float4(hr[j], hr[j + 1], hr[j + 2], hr[j + 3]);
+    }
+  } else if (warp >= 9) {
+    // ------------------------------------------------- off-chain products
+    bool go = true;
+    for (int c = 0; c < NC; ++c) {
+      const int s = c % NS;
+      const uint32_t st = sb + s * Ly::STAGE;
+      if (warp == 9) {
+        // Q [h_hi | h_lo] (M = 64) once W h is done: h_c and Q are in shared
+        // memory, and ACCQ of chunk c - 1 was read before W h was issued.
+        go = waitc(FULL, c) && go;
+        go = waitb(b_m1, c & 1) && go;
+        if (lane == 0 && go) {
+          tc_fence_after();
+          constexpr uint32_t idq = umma_idesc_bf16(64, 64, 0, 1);
+#pragma unroll
+          for (int kk = 0; kk < 4 * KA; ++kk) {
+            const uint64_t a = umma_desc_sw128(st + Ly::WQ + (kk >> 2) * 16384 + 8192 + (kk & 3) * 32);
+            const uint64_t b = umma_desc_sw128_mn(sb + Ly::OFF_H + kk * 2048, 8192);
+            umma_bf16(tmem + Ly::ACCQ, a, b, idq, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(b_qd);
+        }
+        __syncwarp();
+      }
+      // [P_hi | P_lo] [v_new hi | lo] once the state product is done: v_new of
+      // chunk c is in shared memory and ACC3 / ACC3L of chunk c - 1 were read
+      // before it was issued.  Both complete on OUT(c).
+      go = waitb(b_m2, c & 1) && go;
+      if (lane == 0 && go) {
+        tc_fence_after();
+        constexpr uint32_t id3 = umma_idesc_bf16(64, 64, 0, 1);
+        const uint32_t pa = st + Ly::RR + (warp - 9) * 8192;
+        const uint32_t acc = tmem + (warp == 9 ? Ly::ACC3 : Ly::ACC3L);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t a = umma_desc_sw128(pa + kk * 32);
+          const uint64_t b = umma_desc_sw128_mn(sb + Ly::OFF_VN + kk * 2048, 8192);
+          umma_bf16(acc, a, b, id3, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(b_out(c));
+      }
+      __syncwarp();
+    }
+    if (lane == 0 && *abort_flag) {
+      tc_fence_after();
+      umma_commit(b_drain);
+      if (!mbar_wait_bounded(b_drain, 0, kWaitLimit)) set_status(dev_status, GDN_DEV_DRAIN_TIMEOUT);
     }
   } else {
     // ------------------------------------------------------------- producer
@@ -1004,7 +1037,7 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
     __syncwarp();
     for (int c = 0; c + NS < NC; ++c) {
       bool can = waitc(CDONE, c);
-      can = waitc(FULL, c + 1) && can;  // includes: the output product of chunk c read P hi / lo
+      can = wait_out(c) && can;  // the output products of chunk c read P hi / lo
       if (can && lane == 0) issue(c + NS);
       __syncwarp();
     }

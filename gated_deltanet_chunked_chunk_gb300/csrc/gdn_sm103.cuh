@@ -197,6 +197,22 @@ __device__ __forceinline__ void tmem_ld_wait16(uint32_t *r) {
                : "memory");
 }
 
+// 16 lanes x 8 consecutive columns per half warp, issue only: thread t gets
+// lane (base lane + t % 16), columns [col + 8 (t / 16), col + 8 (t / 16) + 8).
+// This is how the rows of an M = 64 accumulator (16 per lane quarter) are read
+// with every thread of the warp busy.
+__device__ __forceinline__ void tmem_ld8x2_issue(uint32_t taddr, uint32_t *r) {
+  asm volatile("tcgen05.ld.sync.aligned.16x32bx2.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], 8;"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait8(uint32_t *r) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])
+               :
+               : "memory");
+}
+
 // ------------------------------------------------------------ ldmatrix / mma
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t *r) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
