@@ -294,7 +294,9 @@ def run_ours(args, rank, world, local_rank):
         if ev is not None:
             ev[1].record(stream)
 
-    launches_per_step = 3  # gating kernel + the chunk forward's prep and walk kernels
+    # The gating kernel plus the chunk forward's prep and walk kernels (two of
+    # each when the sequence is walked in two chunk ranges).
+    launches_per_step = 1 + gdn.chunk_fwd_kernel_launches(B, T, H, HV, K, V, N, False)
 
     def barrier():
         if world > 1:
@@ -603,8 +605,8 @@ def bench_backward(dev, stream, args, hbm=None, bf16=None):
 
 def bench_fused_gating(dev, stream, args, bufs):
     """The same long-context prefill with the gating fused into the prefill's
-    first kernel (gdn_chunk_fwd_gated: two launches, no g / beta arrays),
-    timed beside the headline's gdn_gating + gdn_chunk_fwd."""
+    first kernel (gdn_chunk_fwd_gated: the launches of gdn_chunk_fwd, no g /
+    beta arrays), timed beside the headline's gdn_gating + gdn_chunk_fwd."""
     import torch
     import gated_deltanet_chunked_chunk_gb300 as gdn
     q, k, v, A_log, a, b, dt_bias, h0, o, ht, ws, B, T, HV = bufs
@@ -615,7 +617,8 @@ def bench_fused_gating(dev, stream, args, bufs):
                                 workspace=ws)
     ms = _timed_flush(dev, stream, call, max(args.steps, 5))
     return {"workload": f"long-context prefill B={B} T={T}, gating fused (gdn_chunk_fwd_gated)",
-            "ms": ms, "tokens_per_s": B * T / (ms / 1e3), "launches": 2}
+            "ms": ms, "tokens_per_s": B * T / (ms / 1e3),
+            "launches": gdn.chunk_fwd_kernel_launches(B, T, q.shape[2], HV, q.shape[3], v.shape[3], B, False)}
 
 
 def bench_e2e(case, dev, stream, args, world):

@@ -21,7 +21,7 @@ from typing import Optional, Tuple
 
 import torch
 
-__all__ = ["gdn_gating", "gdn_chunk_fwd", "gdn_recurrent_decode", "chunk_fwd_workspace_size",
+__all__ = ["gdn_gating", "gdn_chunk_fwd", "gdn_recurrent_decode", "chunk_fwd_workspace_size", "chunk_fwd_kernel_launches",
            "gdn_chunk_fwd_noalloc", "NOALLOC_SCRATCH_BYTES", "gdn_causal_conv1d_fwd",
            "gdn_causal_conv1d_update", "gdn_causal_conv1d_update_spec", "gdn_conv_decode_pack",
            "gdn_recurrent_decode_bf16",
@@ -40,6 +40,7 @@ DEV_BAD_CU_SEQLENS, DEV_BAD_SLOT, DEV_WAIT_TIMEOUT, DEV_DRAIN_TIMEOUT = 1, 2, 4,
 
 #: Every symbol include/gdn.h declares (checked by the tests).
 EXPORTED_SYMBOLS = ("gdn_status_string", "gdn_version", "gdn_gating", "gdn_chunk_fwd_workspace_size",
+                    "gdn_chunk_fwd_kernel_launches",
                     "gdn_chunk_fwd", "gdn_recurrent_decode", "gdn_chunk_fwd_noalloc",
                     "gdn_causal_conv1d_fwd", "gdn_causal_conv1d_update", "gdn_conv_decode_pack",
                     "gdn_recurrent_decode_bf16", "gdn_recurrent_decode_mtp", "gdn_chunk_bwd_workspace_size",
@@ -81,6 +82,8 @@ def load_library():
         lib.gdn_gating.restype = I
         lib.gdn_chunk_fwd_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
         lib.gdn_chunk_fwd_workspace_size.restype = SZ
+        lib.gdn_chunk_fwd_kernel_launches.argtypes = [I, I, I, I, I, I, I, I]
+        lib.gdn_chunk_fwd_kernel_launches.restype = I
         lib.gdn_chunk_fwd.argtypes = [P, P, P, P, P, F, P, P, I, I, I, I, I, I, I, I, P, P, P, SZ, P, P]
         lib.gdn_chunk_fwd.restype = I
         lib.gdn_chunk_fwd_gated.argtypes = [P, P, P, P, P, P, P, F, P, P, I, I, I, I, I, I, I, I, P, P, P, P,
@@ -185,6 +188,11 @@ def gdn_gating(A_log: torch.Tensor, a: torch.Tensor, b: torch.Tensor, dt_bias: t
 
 def chunk_fwd_workspace_size(B, T, H, HV, K, V, N, varlen) -> int:
     return int(load_library().gdn_chunk_fwd_workspace_size(B, T, H, HV, K, V, N, int(bool(varlen))))
+
+
+def chunk_fwd_kernel_launches(B, T, H, HV, K, V, N, varlen) -> int:
+    """Kernels gdn_chunk_fwd launches for these sizes on the current device."""
+    return int(load_library().gdn_chunk_fwd_kernel_launches(B, T, H, HV, K, V, N, int(bool(varlen))))
 
 
 def _prefill_args(fn, q, k, v, initial_state, output_final_state, cu_seqlens, num_seqs, dev_status, o,

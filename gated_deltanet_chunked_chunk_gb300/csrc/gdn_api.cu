@@ -82,6 +82,11 @@ size_t gdn_chunk_fwd_workspace_size(int B, int T, int H, int HV, int K, int V,
   return gdn_host::chunk_workspace_bytes(B, T, H, HV, K, V, N, varlen);
 }
 
+int gdn_chunk_fwd_kernel_launches(int B, int T, int H, int HV, int K, int V, int N, int varlen) {
+  if (B < 0 || T < 0 || N < 0 || HV <= 0 || (K != 64 && K != 128) || (V != 64 && V != 128)) return -1;
+  return gdn_host::chunk_fwd_launches(B, T, H, HV, K, V, N, varlen);
+}
+
 namespace {
 // Shared checks and launch of the two prefill entry points; `a` arrives with
 // its gate fields set.

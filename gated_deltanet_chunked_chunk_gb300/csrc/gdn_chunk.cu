@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(NTH, 4) chunk_prep_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k, const float *__restrict__ g,
     const float *__restrict__ beta, const PrepGates gt, const int32_t *__restrict__ cu,
     const int32_t *__restrict__ cs, int N, int T, int H, int HV, int l2, unsigned char *__restrict__ ws,
-    int32_t *dev_status) {
+    int32_t *dev_status, int slot0) {
   using Ly = PrepLay<K>;
   using R = Rec<K>;
   constexpr int KA = K / 64;
@@ -144,8 +144,9 @@ __global__ void __launch_bounds__(NTH, 4) chunk_prep_kernel(
   unsigned char *sm = align1024(smem_raw);
   const uint32_t sb = smem_u32(sm);
   // Value head fastest: the G value heads of a key head run side by side and
-  // share the K, Q tile through L2.
-  const int gc = static_cast<int>(blockIdx.x / HV), hv = static_cast<int>(blockIdx.x % HV);
+  // share the K, Q tile through L2.  The grid covers the chunk slots from slot0
+  // on.
+  const int gc = slot0 + static_cast<int>(blockIdx.x / HV), hv = static_cast<int>(blockIdx.x % HV);
   const int h = hv / (HV / H);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g4 = lane >> 2, t4 = lane & 3;
@@ -638,9 +639,13 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
     const __grid_constant__ CUtensorMap tm_v, float scale, const float *__restrict__ h0,
     const int32_t *__restrict__ cu, int T, int H, int HV, int V, const unsigned char *__restrict__ ws,
     uint16_t *__restrict__ o, float *__restrict__ ht, float *__restrict__ hsave, const int32_t *__restrict__ cs,
-    int32_t *dev_status, int force_expiry) {
+    int32_t *dev_status, int force_expiry, int c_begin, int c_end) {
   using Ly = WalkLay<K>;
   using R = Rec<K>;
+  // A kernel launched as this grid's programmatic dependent (the next range's
+  // prep) may start once every CTA of this grid is resident; it reads nothing
+  // this grid writes.  Without such a dependent this does nothing.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int KA = K / 64;
   constexpr int NS = Ly::NS;
   constexpr int TSO = Ly::RR + (R::TS - R::PH);          // Ts^T within a stage
@@ -658,8 +663,17 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
     if (tid == 0) set_status(dev_status, GDN_DEV_BAD_CU_SEQLENS);
     return;
   }
-  const int NC = chunks_of(len);
-  const int64_t cb = chunk_base(cs, n, T);
+  int64_t cb = chunk_base(cs, n, T);
+  {
+    // This launch walks chunks [c_begin, c_end) of the sequence, starting from
+    // the state h0 and leaving the state after its last chunk in ht: chunk c
+    // below is chunk c_begin + c of the sequence.
+    const int64_t skip = c_begin < chunks_of(len) ? c_begin : chunks_of(len);
+    tok0 += skip * C;
+    len -= skip * C;
+    cb += skip;
+  }
+  const int NC = chunks_of(len) < c_end - c_begin ? chunks_of(len) : c_end - c_begin;
   uint32_t *misc = reinterpret_cast<uint32_t *>(sm + Ly::OFF_MISC);
   volatile uint32_t *abort_flag = misc + 1;
   // Two-slot barriers, slot c & 1 serving chunk c:
@@ -1125,9 +1139,43 @@ template <int K>
 size_t records_bytes(int B, int T, int HV, int N, bool varlen) {
   return static_cast<size_t>(total_chunk_slots(B, T, N, varlen)) * HV * Rec<K>::BYTES;
 }
+// A long single sequence (dense input) is walked in two chunk ranges.  While
+// the walk of the first range runs, the prep of the second runs on the SMs
+// the walk leaves free (a walk CTA fills an SM): it is launched as a
+// programmatic dependent of that walk, whose CTAs release it once they are all
+// resident, so it can never take the walk's SMs first.  The walk of the
+// second range, launched normally after it, waits for both and starts from
+// the state the first one left in the workspace.
+constexpr int kSplitMinChunks = 64;
+constexpr int kSplitMinFreeSMs = 16;
+inline bool split_shape(int N, int T, bool varlen) {
+  return !varlen && N == 1 && (static_cast<int64_t>(T) + C - 1) / C >= kSplitMinChunks;
+}
+// Bytes of the state handed from the first range's walk to the second's.
+inline size_t handoff_bytes(int N, int T, int HV, int K, int V, bool varlen) {
+  return split_shape(N, T, varlen) ? static_cast<size_t>(N) * HV * K * V * 4 : 0;
+}
 template <int K>
-size_t ws_bytes(int B, int T, int HV, int N, bool varlen) {
-  return records_bytes<K>(B, T, HV, N, varlen) + chunk_starts_bytes(N, varlen);
+size_t ws_bytes(int B, int T, int HV, int V, int N, bool varlen) {
+  return records_bytes<K>(B, T, HV, N, varlen) + chunk_starts_bytes(N, varlen) + handoff_bytes(N, T, HV, K, V, varlen);
+}
+// Chunks of the first range when this call is walked in two ranges on the
+// current device, else 0 (or a CUDA error).  The first range's walk takes the
+// time the second range's prep needs on the free SMs: with the prep of a chunk
+// costing about a third of its walk on the whole GPU, the first range is
+// S / (S + 3 F) of the chunks for S SMs of which F are free.
+cudaError_t split_point(int N, int T, int HV, int V, bool varlen, bool hsave, int *c1) {
+  *c1 = 0;
+  if (T <= 0 || hsave || !split_shape(N, T, varlen)) return cudaSuccess;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const int free_sms = sms - (V / VT) * HV;
+  if (free_sms < kSplitMinFreeSMs) return cudaSuccess;
+  const int64_t nc = (static_cast<int64_t>(T) + C - 1) / C;
+  *c1 = static_cast<int>((nc * sms + (sms + 3 * free_sms) / 2) / (sms + 3 * free_sms));
+  return cudaSuccess;
 }
 
 template <int K>
@@ -1153,25 +1201,52 @@ cudaError_t launch_k(const gdn_host::ChunkArgs &a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     cs = csw;
   }
-  if (rows > 0 && slots > 0) {
-    const int psmem = PrepLay<K>::BYTES + 1024;
-    cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, psmem);
-    if (e != cudaSuccess) return e;
-    dim3 pgrid(static_cast<unsigned>(slots * a.HV));
-    const PrepGates gt{a.A_log, a.ga, a.gb, a.dt_bias, a.g_out, a.beta_out};
-    chunk_prep_kernel<K><<<pgrid, NTH, psmem, s>>>(mq, mk, a.g, a.beta, gt, a.cu, cs, a.N, a.T, a.H, a.HV, a.l2,
-                                                   static_cast<unsigned char *>(a.ws), a.dev_status);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
+  const int psmem = PrepLay<K>::BYTES + 1024;
   const int wsmem = WalkLay<K>::BYTES + 1024;
-  cudaError_t e = cudaFuncSetAttribute(chunk_walk_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, wsmem);
+  cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, psmem);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.V / VT, a.HV, a.N);
-  chunk_walk_kernel<K><<<grid, WALK_THREADS, wsmem, s>>>(mq, mk, mv, a.scale, a.h0, a.cu, a.T, a.H, a.HV, a.V,
-                                                static_cast<const unsigned char *>(a.ws), a.o, a.ht, a.hsave, cs,
-                                                a.dev_status, a.force_expiry);
-  return cudaGetLastError();
+  e = cudaFuncSetAttribute(chunk_walk_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, wsmem);
+  if (e != cudaSuccess) return e;
+  const PrepGates gt{a.A_log, a.ga, a.gb, a.dt_bias, a.g_out, a.beta_out};
+  // The prep of chunk slots [slot_begin, slot_begin + nslots).
+  auto prep = [&](int slot_begin, int64_t nslots, cudaStream_t st) {
+    if (rows <= 0 || nslots <= 0) return cudaSuccess;
+    dim3 pgrid(static_cast<unsigned>(nslots * a.HV));
+    chunk_prep_kernel<K><<<pgrid, NTH, psmem, st>>>(mq, mk, a.g, a.beta, gt, a.cu, cs, a.N, a.T, a.H, a.HV, a.l2,
+                                                    static_cast<unsigned char *>(a.ws), a.dev_status, slot_begin);
+    return cudaGetLastError();
+  };
+  // The walk of chunks [c_begin, c_end) of every sequence, from state hin to hout.
+  auto walk = [&](int c_begin, int c_end, const float *hin, float *hout, cudaStream_t st) {
+    dim3 grid(a.V / VT, a.HV, a.N);
+    chunk_walk_kernel<K><<<grid, WALK_THREADS, wsmem, st>>>(mq, mk, mv, a.scale, hin, a.cu, a.T, a.H, a.HV, a.V,
+                                                   static_cast<const unsigned char *>(a.ws), a.o, hout, a.hsave,
+                                                   cs, a.dev_status, a.force_expiry, c_begin, c_end);
+    return cudaGetLastError();
+  };
+  const int nc = static_cast<int>((static_cast<int64_t>(a.T) + C - 1) / C);
+  int c1 = 0;
+  if ((e = split_point(a.N, a.T, a.HV, a.V, a.cu != nullptr, a.hsave != nullptr, &c1)) != cudaSuccess) return e;
+  if (c1 <= 0 || c1 >= nc) {
+    if ((e = prep(0, slots, s)) != cudaSuccess) return e;
+    return walk(0, nc, a.h0, a.ht, s);
+  }
+  float *hmid = reinterpret_cast<float *>(static_cast<unsigned char *>(a.ws) + records_bytes<K>(a.B, a.T, a.HV, a.N, false));
+  if ((e = prep(0, c1, s)) != cudaSuccess || (e = walk(0, c1, a.h0, hmid, s)) != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(nc - c1) * a.HV));
+  cfg.blockDim = dim3(NTH);
+  cfg.dynamicSmemBytes = psmem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, chunk_prep_kernel<K>, mq, mk, a.g, a.beta, gt, a.cu, cs, a.N, a.T, a.H, a.HV, a.l2,
+                         static_cast<unsigned char *>(a.ws), a.dev_status, c1);
+  if (e != cudaSuccess) return e;
+  return walk(c1, nc, hmid, a.ht, s);
 }
 
 }  // namespace
@@ -1180,10 +1255,21 @@ namespace gdn_host {
 
 size_t chunk_workspace_bytes(int B, int T, int H, int HV, int K, int V, int N, int varlen) {
   (void)H;
-  (void)V;
-  if (K == 128) return ws_bytes<128>(B, T, HV, N, varlen != 0);
-  if (K == 64) return ws_bytes<64>(B, T, HV, N, varlen != 0);
+  if (K == 128) return ws_bytes<128>(B, T, HV, V, N, varlen != 0);
+  if (K == 64) return ws_bytes<64>(B, T, HV, V, N, varlen != 0);
   return 0;
+}
+
+int chunk_fwd_launches(int B, int T, int H, int HV, int K, int V, int N, int varlen) {
+  (void)H;
+  (void)K;
+  if (N <= 0) return 0;
+  int c1 = 0;
+  if (split_point(N, T, HV, V, varlen != 0, false, &c1) != cudaSuccess) return -1;
+  const int64_t nc = (static_cast<int64_t>(T) + C - 1) / C;
+  if (c1 > 0 && c1 < nc) return 4;
+  const bool prep = static_cast<int64_t>(B) * T > 0 && total_chunk_slots(B, T, N, varlen != 0) > 0;
+  return (varlen ? 1 : 0) + (prep ? 1 : 0) + 1;
 }
 
 cudaError_t launch_chunk(const ChunkArgs &a, cudaStream_t s) {

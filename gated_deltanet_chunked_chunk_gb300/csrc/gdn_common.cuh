@@ -123,6 +123,8 @@ struct ChunkArgs {
 size_t chunk_workspace_bytes(int B, int T, int H, int HV, int K, int V, int N,
                              int varlen);
 cudaError_t launch_chunk(const ChunkArgs &a, cudaStream_t s);
+// Kernel launches of launch_chunk for these sizes on the current device (-1: no device).
+int chunk_fwd_launches(int B, int T, int H, int HV, int K, int V, int N, int varlen);
 struct ChunkBwdArgs {
   const uint16_t *q, *k, *v;
   const float *g, *beta;

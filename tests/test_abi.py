@@ -66,6 +66,17 @@ def test_chunk_fwd_host_validation(lib):
     assert _chunk(lib, N=0, B=0, T=0) == gdn.GDN_OK           # nothing to do, nothing launched
 
 
+def test_chunk_fwd_launch_count_without_a_device(lib):
+    # Shapes that never take the two-range path are answered on the host.
+    assert gdn.chunk_fwd_kernel_launches(1, 8, 2, 4, 96, 128, 1, False) == -1   # K unsupported
+    assert gdn.chunk_fwd_kernel_launches(1, 8, 2, 4, 128, 32, 1, False) == -1   # V unsupported
+    assert gdn.chunk_fwd_kernel_launches(0, 0, 2, 4, 128, 128, 0, False) == 0
+    assert gdn.chunk_fwd_kernel_launches(2, 100, 2, 4, 128, 128, 2, False) == 2  # prep + walk
+    assert gdn.chunk_fwd_kernel_launches(1, 100, 2, 4, 128, 128, 3, True) == 3   # + the chunk-start table
+    assert gdn.chunk_fwd_kernel_launches(2, 0, 2, 4, 128, 128, 2, False) == 1    # states only: the walk
+    assert gdn.chunk_fwd_kernel_launches(1, 63 * 64, 2, 4, 128, 128, 1, False) == 2  # under 64 chunks
+
+
 def test_chunk_misaligned_buffers_refused_before_launch(lib):
     """The prefill and backward move q, k, v, o, the states and their gradients
     with TMA, bulk copies and 16-byte accesses: a buffer that is only 8-byte

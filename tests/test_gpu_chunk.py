@@ -119,6 +119,36 @@ def test_split_at_chunk_boundary_with_state_carry_is_bitwise():
     assert torch.equal(hb, h_full)
 
 
+def test_long_single_sequence_two_ranges_match_batched_call_bitwise():
+    # One dense sequence of 71 chunks (a ragged last one) is walked in two
+    # chunk ranges, the walk of the first overlapping the prep of the second,
+    # with the fp32 state handed over in the workspace.  The same sequence as
+    # one of a batch of two takes the single-range path: the same bits, and
+    # parity with the oracle.  The workspace starts as NaN bytes, so a second
+    # range that read the handed-over state before the first range wrote it
+    # would show.
+    import gated_deltanet_chunked_chunk_gb300 as gdn
+    T = 64 * 70 + 20
+    case = W.prefill_case("two_ranges", 11, 1, T, 2, 4, 128, 128, init="all")
+    _check_case(case)
+    g, beta = P.oracle_gates(case)
+    d = lambda t: t.cuda().contiguous()
+    two = lambda t: torch.cat([t, t.flip(1)], 0)
+    ws = torch.full((gdn.chunk_fwd_workspace_size(1, T, 2, 4, 128, 128, 1, False),), 255, dtype=torch.uint8,
+                    device="cuda")
+    o1, h1 = gdn.gdn_chunk_fwd(d(case.q), d(case.k), d(case.v), d(g), d(beta),
+                               initial_state=d(case.initial_state), workspace=ws)
+    o2, h2 = gdn.gdn_chunk_fwd(d(two(case.q)), d(two(case.k)), d(two(case.v)), d(two(g)), d(two(beta)),
+                               initial_state=d(torch.cat([case.initial_state, case.initial_state], 0)))
+    assert torch.equal(o2[:1], o1)
+    assert torch.equal(h2[:1], h1)
+    # 16 walk CTAs leave the SMs free: this shape takes four launches, the
+    # batch of two (and a 63-chunk sequence) two.
+    assert gdn.chunk_fwd_kernel_launches(1, T, 2, 4, 128, 128, 1, False) == 4
+    assert gdn.chunk_fwd_kernel_launches(2, T, 2, 4, 128, 128, 2, False) == 2
+    assert gdn.chunk_fwd_kernel_launches(1, 63 * 64, 2, 4, 128, 128, 1, False) == 2
+
+
 def test_deterministic_and_guard_bands():
     case = W.config1()
     g, beta = P.oracle_gates(case)

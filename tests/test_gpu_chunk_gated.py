@@ -78,6 +78,12 @@ def test_gated_ragged_gva_with_state():
     _check(W.prefill_case("gated_ragged", 51, 2, 200, 2, 4, 128, 128, init="all"))
 
 
+def test_gated_long_single_sequence_two_ranges():
+    # 71 chunks of one dense sequence: the two-range path, each range's prep
+    # computing the gates of its own chunks.
+    _check(W.prefill_case("gated_long", 54, 1, 64 * 70 + 20, 2, 4, 128, 128, init="all"))
+
+
 def test_gated_varlen_with_empty_sequence():
     lengths = [70, 0, 5, 129]
     _check(W.prefill_case("gated_var", 52, 1, sum(lengths), 2, 4, 64, 128, init="even",
