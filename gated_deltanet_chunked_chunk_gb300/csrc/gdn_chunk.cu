@@ -1139,15 +1139,19 @@ template <int K>
 size_t records_bytes(int B, int T, int HV, int N, bool varlen) {
   return static_cast<size_t>(total_chunk_slots(B, T, N, varlen)) * HV * Rec<K>::BYTES;
 }
-// A long single sequence (dense input) is walked in two chunk ranges.  While
-// the walk of the first range runs, the prep of the second runs on the SMs
-// the walk leaves free (a walk CTA fills an SM): it is launched as a
-// programmatic dependent of that walk, whose CTAs release it once they are all
-// resident, so it can never take the walk's SMs first.  The walk of the
-// second range, launched normally after it, waits for both and starts from
-// the state the first one left in the workspace.
+// A long single sequence (dense input) is walked in several chunk ranges.
+// While the walk of one range runs, the prep of the next runs on the SMs the
+// walk leaves free (a walk CTA fills an SM): it is launched as a programmatic
+// dependent of that walk, whose CTAs release it once they are all resident,
+// so it can never take the walk's SMs first.  The walk of the next range,
+// launched normally after it, waits for both and starts from the state the
+// previous walk left in the workspace (each CTA reads and later writes only
+// its own slice there, so one buffer serves every hand-over).  Only the first
+// range's prep is not hidden behind a walk.
 constexpr int kSplitMinChunks = 64;
 constexpr int kSplitMinFreeSMs = 16;
+constexpr int kMaxRanges = 4;
+constexpr int kMinRangeChunks = 32;
 inline bool split_shape(int N, int T, bool varlen) {
   return !varlen && N == 1 && (static_cast<int64_t>(T) + C - 1) / C >= kSplitMinChunks;
 }
@@ -1159,13 +1163,18 @@ template <int K>
 size_t ws_bytes(int B, int T, int HV, int V, int N, bool varlen) {
   return records_bytes<K>(B, T, HV, N, varlen) + chunk_starts_bytes(N, varlen) + handoff_bytes(N, T, HV, K, V, varlen);
 }
-// Chunks of the first range when this call is walked in two ranges on the
-// current device, else 0 (or a CUDA error).  The first range's walk takes the
-// time the second range's prep needs on the free SMs: with the prep of a chunk
-// costing about a third of its walk on the whole GPU, the first range is
-// S / (S + 3 F) of the chunks for S SMs of which F are free.
-cudaError_t split_point(int N, int T, int HV, int V, bool varlen, bool hsave, int *c1) {
-  *c1 = 0;
+// The chunk ranges of this call on the current device: bounds[0] = 0 <
+// bounds[1] < ... < bounds[R] = number of chunks; R = 1 when it is walked in
+// one range.  A range's walk should take as long as the next range's prep on
+// the F free SMs of S.  A chunk's prep costs about a third of its walk on the
+// whole GPU, so each range has q = 3 F / S times the chunks of the one before
+// it; the count is the largest (up to kMaxRanges) whose last range keeps
+// kMinRangeChunks chunks.
+cudaError_t chunk_ranges(int N, int T, int HV, int V, bool varlen, bool hsave, int *bounds, int *R) {
+  const int64_t nc = (static_cast<int64_t>(T) > 0 ? (static_cast<int64_t>(T) + C - 1) / C : 0);
+  *R = 1;
+  bounds[0] = 0;
+  bounds[1] = static_cast<int>(nc);
   if (T <= 0 || hsave || !split_shape(N, T, varlen)) return cudaSuccess;
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1173,8 +1182,25 @@ cudaError_t split_point(int N, int T, int HV, int V, bool varlen, bool hsave, in
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const int free_sms = sms - (V / VT) * HV;
   if (free_sms < kSplitMinFreeSMs) return cudaSuccess;
-  const int64_t nc = (static_cast<int64_t>(T) + C - 1) / C;
-  *c1 = static_cast<int>((nc * sms + (sms + 3 * free_sms) / 2) / (sms + 3 * free_sms));
+  const double q = free_sms * 3.0 < sms ? free_sms * 3.0 / sms : 0.9;
+  for (int r = kMaxRanges; r >= 2; --r) {
+    // Range k has about nc * q^k (1 - q) / (1 - q^r) chunks.
+    double w = 1.0, wsum = 0.0;
+    for (int k = 0; k < r; ++k, w *= q) wsum += w;
+    double acc = 0.0;
+    w = 1.0;
+    bool ok = true;
+    for (int k = 0; k < r; ++k, w *= q) {
+      acc += w;
+      bounds[k + 1] = k + 1 == r ? static_cast<int>(nc) : static_cast<int>(nc * acc / wsum + 0.5);
+      if (bounds[k + 1] - bounds[k] < kMinRangeChunks) ok = false;
+    }
+    if (ok) {
+      *R = r;
+      return cudaSuccess;
+    }
+  }
+  bounds[1] = static_cast<int>(nc);
   return cudaSuccess;
 }
 
@@ -1224,29 +1250,34 @@ cudaError_t launch_k(const gdn_host::ChunkArgs &a, cudaStream_t s) {
                                                    cs, a.dev_status, a.force_expiry, c_begin, c_end);
     return cudaGetLastError();
   };
-  const int nc = static_cast<int>((static_cast<int64_t>(a.T) + C - 1) / C);
-  int c1 = 0;
-  if ((e = split_point(a.N, a.T, a.HV, a.V, a.cu != nullptr, a.hsave != nullptr, &c1)) != cudaSuccess) return e;
-  if (c1 <= 0 || c1 >= nc) {
+  int bounds[kMaxRanges + 1], R = 1;
+  if ((e = chunk_ranges(a.N, a.T, a.HV, a.V, a.cu != nullptr, a.hsave != nullptr, bounds, &R)) != cudaSuccess)
+    return e;
+  if (R == 1) {
     if ((e = prep(0, slots, s)) != cudaSuccess) return e;
-    return walk(0, nc, a.h0, a.ht, s);
+    return walk(0, bounds[1], a.h0, a.ht, s);
   }
   float *hmid = reinterpret_cast<float *>(static_cast<unsigned char *>(a.ws) + records_bytes<K>(a.B, a.T, a.HV, a.N, false));
-  if ((e = prep(0, c1, s)) != cudaSuccess || (e = walk(0, c1, a.h0, hmid, s)) != cudaSuccess) return e;
+  if ((e = prep(0, bounds[1], s)) != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(nc - c1) * a.HV));
-  cfg.blockDim = dim3(NTH);
-  cfg.dynamicSmemBytes = psmem;
-  cfg.stream = s;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, chunk_prep_kernel<K>, mq, mk, a.g, a.beta, gt, a.cu, cs, a.N, a.T, a.H, a.HV, a.l2,
-                         static_cast<unsigned char *>(a.ws), a.dev_status, c1);
-  if (e != cudaSuccess) return e;
-  return walk(c1, nc, hmid, a.ht, s);
+  for (int r = 0; r < R; ++r) {
+    e = walk(bounds[r], bounds[r + 1], r == 0 ? a.h0 : hmid, r + 1 == R ? a.ht : hmid, s);
+    if (e != cudaSuccess || r + 1 == R) return e;
+    // The next range's prep, beside this walk.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(bounds[r + 2] - bounds[r + 1]) * a.HV));
+    cfg.blockDim = dim3(NTH);
+    cfg.dynamicSmemBytes = psmem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, chunk_prep_kernel<K>, mq, mk, a.g, a.beta, gt, a.cu, cs, a.N, a.T, a.H, a.HV, a.l2,
+                           static_cast<unsigned char *>(a.ws), a.dev_status, bounds[r + 1]);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -1264,10 +1295,9 @@ int chunk_fwd_launches(int B, int T, int H, int HV, int K, int V, int N, int var
   (void)H;
   (void)K;
   if (N <= 0) return 0;
-  int c1 = 0;
-  if (split_point(N, T, HV, V, varlen != 0, false, &c1) != cudaSuccess) return -1;
-  const int64_t nc = (static_cast<int64_t>(T) + C - 1) / C;
-  if (c1 > 0 && c1 < nc) return 4;
+  int bounds[kMaxRanges + 1], R = 1;
+  if (chunk_ranges(N, T, HV, V, varlen != 0, false, bounds, &R) != cudaSuccess) return -1;
+  if (R > 1) return 2 * R;
   const bool prep = static_cast<int64_t>(B) * T > 0 && total_chunk_slots(B, T, N, varlen != 0) > 0;
   return (varlen ? 1 : 0) + (prep ? 1 : 0) + 1;
 }

@@ -107,8 +107,8 @@ int gdn_gating(const float *A_log, const uint16_t *a, const uint16_t *b,
  * needs for these sizes (0 means none; pass workspace = NULL then): one
  * record per (chunk slot, value head); with cu_seqlens (varlen != 0) a table
  * of N + 1 chunk starts that the call fills first; for one dense sequence of
- * at least 64 chunks, room for the fp32 state [HV, K, V] that the first chunk
- * range hands to the second (see gdn_chunk_fwd).
+ * at least 64 chunks, room for the fp32 state [HV, K, V] that one chunk range
+ * hands to the next (see gdn_chunk_fwd).
  */
 size_t gdn_chunk_fwd_workspace_size(int B, int T, int H, int HV, int K, int V,
                                     int N, int varlen);
@@ -117,8 +117,8 @@ size_t gdn_chunk_fwd_workspace_size(int B, int T, int H, int HV, int K, int V,
  * gdn_chunk_fwd_kernel_launches -- number of kernels gdn_chunk_fwd (and
  * gdn_chunk_fwd_gated) launches for these sizes on the current device: the
  * prep and the walk kernel; before them, with cu_seqlens, the chunk-start
- * kernel; four in all when one long dense sequence is walked in two chunk
- * ranges (see gdn_chunk_fwd); 0 for N = 0.  Returns -1 for sizes the entry
+ * kernel; two per chunk range when one long dense sequence is walked in
+ * several (see gdn_chunk_fwd); 0 for N = 0.  Returns -1 for sizes the entry
  * point refuses (K or V not 64 or 128, negative sizes) or when the device
  * cannot be queried.
  */
@@ -163,11 +163,12 @@ int gdn_chunk_fwd_kernel_launches(int B, int T, int H, int HV, int K, int V,
  * value head), then the state walk (one CTA per 32-column slice of V, value
  * head and sequence, serial over the sequence's chunks).  One dense sequence
  * (N = 1, no cu_seqlens) of at least 64 chunks whose walk leaves at least 16
- * SMs free is done in two chunk ranges: prep and walk of the first range,
- * then the second range's prep (launched as a programmatic dependent of that
- * walk, so it runs on the SMs the walk leaves free while the walk runs), then
- * the second range's walk, starting from the fp32 state the first left in the
- * workspace.  The results are bit-identical to a single range.
+ * SMs free is done in up to four chunk ranges: prep and walk of the first
+ * range, then for each later range its prep (launched as a programmatic
+ * dependent of the previous walk, so it runs on the SMs that walk leaves
+ * free while it runs) and its walk, starting from the fp32 state the previous
+ * walk left in the workspace.  The results are bit-identical to a single
+ * range.
  * gdn_chunk_fwd_kernel_launches() gives the number of launches.
  */
 int gdn_chunk_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,

@@ -121,8 +121,9 @@ def test_split_at_chunk_boundary_with_state_carry_is_bitwise():
 
 def test_long_single_sequence_two_ranges_match_batched_call_bitwise():
     # One dense sequence of 71 chunks (a ragged last one) is walked in two
-    # chunk ranges, the walk of the first overlapping the prep of the second,
-    # with the fp32 state handed over in the workspace.  The same sequence as
+    # chunk ranges (16 walk CTAs leave most SMs free, so the ranges are about
+    # even), the walk of the first overlapping the prep of the second, with
+    # the fp32 state handed over in the workspace.  The same sequence as
     # one of a batch of two takes the single-range path: the same bits, and
     # parity with the oracle.  The workspace starts as NaN bytes, so a second
     # range that read the handed-over state before the first range wrote it
@@ -142,11 +143,32 @@ def test_long_single_sequence_two_ranges_match_batched_call_bitwise():
                                initial_state=d(torch.cat([case.initial_state, case.initial_state], 0)))
     assert torch.equal(o2[:1], o1)
     assert torch.equal(h2[:1], h1)
-    # 16 walk CTAs leave the SMs free: this shape takes four launches, the
-    # batch of two (and a 63-chunk sequence) two.
+    # Two ranges: four launches; the batch of two (and a 63-chunk sequence)
+    # takes two.
     assert gdn.chunk_fwd_kernel_launches(1, T, 2, 4, 128, 128, 1, False) == 4
     assert gdn.chunk_fwd_kernel_launches(2, T, 2, 4, 128, 128, 2, False) == 2
     assert gdn.chunk_fwd_kernel_launches(1, 63 * 64, 2, 4, 128, 128, 1, False) == 2
+
+
+def test_three_ranges_reuse_the_hand_over_buffer_bitwise():
+    # 300 chunks at HV = 32 (128 walk CTAs, 24 SMs free): three chunk ranges,
+    # the hand-over state rewritten in place twice.  NaN-filled workspace; the
+    # same sequence in a batch of two (one range) gives the same bits.
+    import gated_deltanet_chunked_chunk_gb300 as gdn
+    T = 64 * 300
+    case = W.prefill_case("three_ranges", 12, 1, T, 16, 32, 128, 128, init="all")
+    g, beta = P.oracle_gates(case)
+    d = lambda t: t.cuda().contiguous()
+    two = lambda t: torch.cat([t, t.flip(1)], 0)
+    assert gdn.chunk_fwd_kernel_launches(1, T, 16, 32, 128, 128, 1, False) == 6
+    ws = torch.full((gdn.chunk_fwd_workspace_size(1, T, 16, 32, 128, 128, 1, False),), 255, dtype=torch.uint8,
+                    device="cuda")
+    o1, h1 = gdn.gdn_chunk_fwd(d(case.q), d(case.k), d(case.v), d(g), d(beta),
+                               initial_state=d(case.initial_state), workspace=ws)
+    o2, h2 = gdn.gdn_chunk_fwd(d(two(case.q)), d(two(case.k)), d(two(case.v)), d(two(g)), d(two(beta)),
+                               initial_state=d(torch.cat([case.initial_state, case.initial_state], 0)))
+    assert torch.equal(o2[:1], o1)
+    assert torch.equal(h2[:1], h1)
 
 
 def test_deterministic_and_guard_bands():
