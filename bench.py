@@ -630,7 +630,9 @@ def bench_e2e(case, dev, stream, args, world):
     device and host buffers, ordered by events); the timed region spans every
     copy of every step.  Only the first step's input copy and the last step's
     output copy have nothing to overlap, so the steady-state rate of a stream of
-    steps needs a couple of dozen of them (the default: 24 steps, ~0.15 s)."""
+    steps needs a couple of dozen of them (the default: 24 steps, ~0.15 s).
+    The host link is shared with the rest of the machine, so the pipelined run
+    is timed three times and the median reported, with all three listed."""
     import torch
     import gated_deltanet_chunked_chunk_gb300 as gdn
     B, T, H, HV, K, V, N = case.B, case.T, case.H, case.HV, case.K, case.V, case.N
@@ -701,9 +703,11 @@ def bench_e2e(case, dev, stream, args, world):
         return e0.elapsed_time(e1) if timed else 0.0
 
     run(2, False)
-    ms = run(steps, True) / steps
+    runs = [run(steps, True) / steps for _ in range(3)]
+    ms = sorted(runs)[1]
     return {"value": B * T * world / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps,
+            "runs_ms_per_step": [round(r, 4) for r in runs], "of_runs": "median of 3",
             "pipelining": "copies of step i+1 (H2D, two streams) and i-1 (D2H) overlap the compute of step i"}
 
 
