@@ -171,6 +171,37 @@ def test_three_ranges_reuse_the_hand_over_buffer_bitwise():
     assert torch.equal(h2[:1], h1)
 
 
+def test_multi_range_call_captured_in_a_cuda_graph_matches_eager():
+    # A serving loop captures the prefill into a CUDA graph.  Three chunk
+    # ranges (six launches, the later preps programmatic dependents of the
+    # walks before them) captured and replayed give the eager call's bits.
+    import gated_deltanet_chunked_chunk_gb300 as gdn
+    T = 64 * 300
+    case = W.prefill_case("graph", 13, 1, T, 16, 32, 128, 128, init="all")
+    g, beta = P.oracle_gates(case)
+    d = lambda t: t.cuda().contiguous()
+    q, k, v, gg, bb, h0 = d(case.q), d(case.k), d(case.v), d(g), d(beta), d(case.initial_state)
+    ws = torch.empty(gdn.chunk_fwd_workspace_size(1, T, 16, 32, 128, 128, 1, False), dtype=torch.uint8,
+                     device="cuda")
+    o_e, h_e = gdn.gdn_chunk_fwd(q, k, v, gg, bb, initial_state=h0, workspace=ws)
+    o_g = torch.empty_like(o_e)
+    h_g = torch.empty_like(h_e)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        gdn.gdn_chunk_fwd(q, k, v, gg, bb, initial_state=h0, workspace=ws, o=o_g, final_state=h_g)
+    torch.cuda.current_stream().wait_stream(side)
+    o_g.zero_()
+    h_g.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        gdn.gdn_chunk_fwd(q, k, v, gg, bb, initial_state=h0, workspace=ws, o=o_g, final_state=h_g)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o_g, o_e)
+    assert torch.equal(h_g, h_e)
+
+
 def test_deterministic_and_guard_bands():
     case = W.config1()
     g, beta = P.oracle_gates(case)
