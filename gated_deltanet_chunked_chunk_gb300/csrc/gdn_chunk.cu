@@ -1166,10 +1166,11 @@ size_t ws_bytes(int B, int T, int HV, int V, int N, bool varlen) {
 // The chunk ranges of this call on the current device: bounds[0] = 0 <
 // bounds[1] < ... < bounds[R] = number of chunks; R = 1 when it is walked in
 // one range.  A range's walk should take as long as the next range's prep on
-// the F free SMs of S.  A chunk's prep costs about a third of its walk on the
-// whole GPU, so each range has q = 3 F / S times the chunks of the one before
-// it; the count is the largest (up to kMaxRanges) whose last range keeps
-// kMinRangeChunks chunks.
+// the F free SMs of S.  Measured at K = V = 128, a chunk's prep on the whole
+// GPU costs 1 / 3.1 of its walk, and a prep CTA beside a walk runs about 8 %
+// faster than in a full prep grid, so each range has q = 3.3 F / S times the
+// chunks of the one before it; the count is the largest (up to kMaxRanges)
+// whose last range keeps kMinRangeChunks chunks.
 cudaError_t chunk_ranges(int N, int T, int HV, int V, bool varlen, bool hsave, int *bounds, int *R) {
   const int64_t nc = (static_cast<int64_t>(T) > 0 ? (static_cast<int64_t>(T) + C - 1) / C : 0);
   *R = 1;
@@ -1182,7 +1183,7 @@ cudaError_t chunk_ranges(int N, int T, int HV, int V, bool varlen, bool hsave, i
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const int free_sms = sms - (V / VT) * HV;
   if (free_sms < kSplitMinFreeSMs) return cudaSuccess;
-  const double q = free_sms * 3.0 < sms ? free_sms * 3.0 / sms : 0.9;
+  const double q = free_sms * 3.3 < sms ? free_sms * 3.3 / sms : 0.9;
   for (int r = kMaxRanges; r >= 2; --r) {
     // Range k has about nc * q^k (1 - q) / (1 - q^r) chunks.
     double w = 1.0, wsum = 0.0;
