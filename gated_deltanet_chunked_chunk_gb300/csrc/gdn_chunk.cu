@@ -1139,7 +1139,7 @@ template <int K>
 size_t records_bytes(int B, int T, int HV, int N, bool varlen) {
   return static_cast<size_t>(total_chunk_slots(B, T, N, varlen)) * HV * Rec<K>::BYTES;
 }
-// A long single sequence (dense input) is walked in several chunk ranges.
+// A long single sequence (N = 1, dense or cu_seqlens) is walked in several chunk ranges.
 // While the walk of one range runs, the prep of the next runs on the SMs the
 // walk leaves free (a walk CTA fills an SM): it is launched as a programmatic
 // dependent of that walk, whose CTAs release it once they are all resident,
@@ -1153,7 +1153,8 @@ constexpr int kSplitMinFreeSMs = 16;
 constexpr int kMaxRanges = 4;
 constexpr int kMinRangeChunks = 32;
 inline bool split_shape(int N, int T, bool varlen) {
-  return !varlen && N == 1 && (static_cast<int64_t>(T) + C - 1) / C >= kSplitMinChunks;
+  (void)varlen;  // with cu_seqlens, N = 1 means the one sequence spans [0, T)
+  return N == 1 && (static_cast<int64_t>(T) + C - 1) / C >= kSplitMinChunks;
 }
 // Bytes of the state handed from the first range's walk to the second's.
 inline size_t handoff_bytes(int N, int T, int HV, int K, int V, bool varlen) {
@@ -1258,7 +1259,9 @@ cudaError_t launch_k(const gdn_host::ChunkArgs &a, cudaStream_t s) {
     if ((e = prep(0, slots, s)) != cudaSuccess) return e;
     return walk(0, bounds[1], a.h0, a.ht, s);
   }
-  float *hmid = reinterpret_cast<float *>(static_cast<unsigned char *>(a.ws) + records_bytes<K>(a.B, a.T, a.HV, a.N, false));
+  float *hmid = reinterpret_cast<float *>(static_cast<unsigned char *>(a.ws) +
+                                          records_bytes<K>(a.B, a.T, a.HV, a.N, a.cu != nullptr) +
+                                          chunk_starts_bytes(a.N, a.cu != nullptr));
   if ((e = prep(0, bounds[1], s)) != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1298,7 +1301,7 @@ int chunk_fwd_launches(int B, int T, int H, int HV, int K, int V, int N, int var
   if (N <= 0) return 0;
   int bounds[kMaxRanges + 1], R = 1;
   if (chunk_ranges(N, T, HV, V, varlen != 0, false, bounds, &R) != cudaSuccess) return -1;
-  if (R > 1) return 2 * R;
+  if (R > 1) return 2 * R + (varlen ? 1 : 0);
   const bool prep = static_cast<int64_t>(B) * T > 0 && total_chunk_slots(B, T, N, varlen != 0) > 0;
   return (varlen ? 1 : 0) + (prep ? 1 : 0) + 1;
 }

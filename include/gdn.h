@@ -106,9 +106,9 @@ int gdn_gating(const float *A_log, const uint16_t *a, const uint16_t *b,
  * gdn_chunk_fwd_workspace_size -- bytes of device workspace gdn_chunk_fwd
  * needs for these sizes (0 means none; pass workspace = NULL then): one
  * record per (chunk slot, value head); with cu_seqlens (varlen != 0) a table
- * of N + 1 chunk starts that the call fills first; for one dense sequence of
- * at least 64 chunks, room for the fp32 state [HV, K, V] that one chunk range
- * hands to the next (see gdn_chunk_fwd).
+ * of N + 1 chunk starts that the call fills first; for one sequence (N = 1)
+ * of at least 64 chunks, room for the fp32 state [HV, K, V] that one chunk
+ * range hands to the next (see gdn_chunk_fwd).
  */
 size_t gdn_chunk_fwd_workspace_size(int B, int T, int H, int HV, int K, int V,
                                     int N, int varlen);
@@ -117,8 +117,8 @@ size_t gdn_chunk_fwd_workspace_size(int B, int T, int H, int HV, int K, int V,
  * gdn_chunk_fwd_kernel_launches -- number of kernels gdn_chunk_fwd (and
  * gdn_chunk_fwd_gated) launches for these sizes on the current device: the
  * prep and the walk kernel; before them, with cu_seqlens, the chunk-start
- * kernel; two per chunk range when one long dense sequence is walked in
- * several (see gdn_chunk_fwd); 0 for N = 0.  Returns -1 for sizes the entry
+ * kernel; two per chunk range when one long sequence is walked in several
+ * (see gdn_chunk_fwd); 0 for N = 0.  Returns -1 for sizes the entry
  * point refuses (K or V not 64 or 128, negative sizes) or when the device
  * cannot be queried.
  */
@@ -161,8 +161,8 @@ int gdn_chunk_fwd_kernel_launches(int B, int T, int H, int HV, int K, int V,
  *
  * Launches, all on `stream`: a per-chunk prep kernel (one CTA per chunk and
  * value head), then the state walk (one CTA per 32-column slice of V, value
- * head and sequence, serial over the sequence's chunks).  One dense sequence
- * (N = 1, no cu_seqlens) of at least 64 chunks whose walk leaves at least 16
+ * head and sequence, serial over the sequence's chunks).  One sequence (N = 1,
+ * dense or with cu_seqlens) of at least 64 chunks whose walk leaves at least 16
  * SMs free is done in up to four chunk ranges: prep and walk of the first
  * range, then for each later range its prep (launched as a programmatic
  * dependent of the previous walk, so it runs on the SMs that walk leaves

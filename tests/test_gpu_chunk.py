@@ -143,9 +143,19 @@ def test_long_single_sequence_two_ranges_match_batched_call_bitwise():
                                initial_state=d(torch.cat([case.initial_state, case.initial_state], 0)))
     assert torch.equal(o2[:1], o1)
     assert torch.equal(h2[:1], h1)
-    # Two ranges: four launches; the batch of two (and a 63-chunk sequence)
-    # takes two.
+    # The same sequence given with cu_seqlens = [0, T] (one varlen sequence)
+    # takes the same ranges after the chunk-start table.
+    cu = torch.tensor([0, T], dtype=torch.int32, device="cuda")
+    ws3 = torch.full((gdn.chunk_fwd_workspace_size(1, T, 2, 4, 128, 128, 1, True),), 255, dtype=torch.uint8,
+                     device="cuda")
+    o3, h3 = gdn.gdn_chunk_fwd(d(case.q), d(case.k), d(case.v), d(g), d(beta), initial_state=d(case.initial_state),
+                               cu_seqlens=cu, workspace=ws3)
+    assert torch.equal(o3, o1)
+    assert torch.equal(h3, h1)
+    # Two ranges: four launches (five with the chunk-start table); the batch
+    # of two (and a 63-chunk sequence) takes two.
     assert gdn.chunk_fwd_kernel_launches(1, T, 2, 4, 128, 128, 1, False) == 4
+    assert gdn.chunk_fwd_kernel_launches(1, T, 2, 4, 128, 128, 1, True) == 5
     assert gdn.chunk_fwd_kernel_launches(2, T, 2, 4, 128, 128, 2, False) == 2
     assert gdn.chunk_fwd_kernel_launches(1, 63 * 64, 2, 4, 128, 128, 1, False) == 2
 
