@@ -593,7 +593,8 @@ __global__ void __launch_bounds__(NTH, 4) chunk_prep_kernel(
 //    (key r) and the 16 columns 16 (w >> 2) .. + 15, and holds the fp32 state
 //    h[r][16 columns] in registers.  Per chunk c:
 //      W [h_hi | h_lo] -> ACC1 (4 partials, warps 0-3) and u(c) = Ts V -> ACC4
-//      (warp 6); meanwhile the output of chunk c - 1;
+//      (warp 7, on the SM sub-partition no other issuing warp uses); meanwhile
+//      the output of chunk c - 1;
 //      v_new = beta v + u - W h -> s v_new, v_new (bf16 hi | lo);
 //      K^T [s v_new hi | lo] -> ACC2 (2 partials, warps 0-1);
 //      h <- e^{gamma_L} h + ACC2, written back as [h_hi | h_lo], and
@@ -856,7 +857,7 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
           umma_bf16(tmem + Ly::ACC1 + 64 * warp, a, b, id1, m > 0 ? 1u : 0u);
         }
         umma_commit(b_m1);
-      } else if (warp == 6 && lane == 0 && go) {
+      } else if (warp == 7 && lane == 0 && go) {
         issue_u(c);  // ACC4 was last read for chunk c - 1, before its v_new barrier
       }
       __syncwarp();
@@ -967,7 +968,7 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) chunk_walk_kernel(
     if (lane == 0 && *abort_flag) {
       // After an abort products may still be in flight: one more commit by
       // each issuing thread completes once all of that thread's products have.
-      if (warp < 4 || warp == 6) {
+      if (warp < 4 || warp == 7) {
         tc_fence_after();
         umma_commit(b_drain);
         if (!mbar_wait_bounded(b_drain, 0, kWaitLimit)) set_status(dev_status, GDN_DEV_DRAIN_TIMEOUT);

@@ -119,7 +119,8 @@ def test_split_at_chunk_boundary_with_state_carry_is_bitwise():
     assert torch.equal(hb, h_full)
 
 
-def test_long_single_sequence_two_ranges_match_batched_call_bitwise():
+@pytest.mark.parametrize("K", [128, 64])
+def test_long_single_sequence_two_ranges_match_batched_call_bitwise(K):
     # One dense sequence of 71 chunks (a ragged last one) is walked in two
     # chunk ranges (16 walk CTAs leave most SMs free, so the ranges are about
     # even), the walk of the first overlapping the prep of the second, with
@@ -130,12 +131,12 @@ def test_long_single_sequence_two_ranges_match_batched_call_bitwise():
     # would show.
     import gated_deltanet_chunked_chunk_gb300 as gdn
     T = 64 * 70 + 20
-    case = W.prefill_case("two_ranges", 11, 1, T, 2, 4, 128, 128, init="all")
+    case = W.prefill_case("two_ranges", 11, 1, T, 2, 4, K, 128, init="all")
     _check_case(case)
     g, beta = P.oracle_gates(case)
     d = lambda t: t.cuda().contiguous()
     two = lambda t: torch.cat([t, t.flip(1)], 0)
-    ws = torch.full((gdn.chunk_fwd_workspace_size(1, T, 2, 4, 128, 128, 1, False),), 255, dtype=torch.uint8,
+    ws = torch.full((gdn.chunk_fwd_workspace_size(1, T, 2, 4, K, 128, 1, False),), 255, dtype=torch.uint8,
                     device="cuda")
     o1, h1 = gdn.gdn_chunk_fwd(d(case.q), d(case.k), d(case.v), d(g), d(beta),
                                initial_state=d(case.initial_state), workspace=ws)
@@ -146,7 +147,7 @@ def test_long_single_sequence_two_ranges_match_batched_call_bitwise():
     # The same sequence given with cu_seqlens = [0, T] (one varlen sequence)
     # takes the same ranges after the chunk-start table.
     cu = torch.tensor([0, T], dtype=torch.int32, device="cuda")
-    ws3 = torch.full((gdn.chunk_fwd_workspace_size(1, T, 2, 4, 128, 128, 1, True),), 255, dtype=torch.uint8,
+    ws3 = torch.full((gdn.chunk_fwd_workspace_size(1, T, 2, 4, K, 128, 1, True),), 255, dtype=torch.uint8,
                      device="cuda")
     o3, h3 = gdn.gdn_chunk_fwd(d(case.q), d(case.k), d(case.v), d(g), d(beta), initial_state=d(case.initial_state),
                                cu_seqlens=cu, workspace=ws3)
@@ -154,10 +155,10 @@ def test_long_single_sequence_two_ranges_match_batched_call_bitwise():
     assert torch.equal(h3, h1)
     # Two ranges: four launches (five with the chunk-start table); the batch
     # of two (and a 63-chunk sequence) takes two.
-    assert gdn.chunk_fwd_kernel_launches(1, T, 2, 4, 128, 128, 1, False) == 4
-    assert gdn.chunk_fwd_kernel_launches(1, T, 2, 4, 128, 128, 1, True) == 5
-    assert gdn.chunk_fwd_kernel_launches(2, T, 2, 4, 128, 128, 2, False) == 2
-    assert gdn.chunk_fwd_kernel_launches(1, 63 * 64, 2, 4, 128, 128, 1, False) == 2
+    assert gdn.chunk_fwd_kernel_launches(1, T, 2, 4, K, 128, 1, False) == 4
+    assert gdn.chunk_fwd_kernel_launches(1, T, 2, 4, K, 128, 1, True) == 5
+    assert gdn.chunk_fwd_kernel_launches(2, T, 2, 4, K, 128, 2, False) == 2
+    assert gdn.chunk_fwd_kernel_launches(1, 63 * 64, 2, 4, K, 128, 1, False) == 2
 
 
 def test_three_ranges_reuse_the_hand_over_buffer_bitwise():
