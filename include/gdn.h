@@ -169,7 +169,11 @@ int gdn_chunk_fwd_kernel_launches(int B, int T, int H, int HV, int K, int V,
  * free while it runs) and its walk, starting from the fp32 state the previous
  * walk left in the workspace.  The results are bit-identical to a single
  * range.
- * gdn_chunk_fwd_kernel_launches() gives the number of launches.
+ * gdn_chunk_fwd_kernel_launches() gives the number of launches.  Every walk
+ * launch releases a programmatic dependent launch queued after it once its
+ * CTAs are resident: a caller's kernel launched that way right after this call
+ * must wait for its primary grid (griddepcontrol.wait) before it reads o or
+ * final_state, as any programmatic dependent must.
  */
 int gdn_chunk_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                   const float *g, const float *beta, float scale,
