@@ -26,22 +26,25 @@
 // 128B-swizzled smem operands, fp32 accumulator in TMEM), whose diagonal gives
 // the row norms; A and P are built from TMEM; T by 16x16 diagonal-block
 // substitution plus tf32 mma.sync for the off-diagonal blocks, in place; W by
-// mma.sync.  The CTA writes one record [W | P hi | P lo | Ts^T | scalars] per
-// (chunk, value head) to the workspace, laid out exactly as the walk kernel
-// wants it in shared memory.
+// one more tcgen05 product.  The CTA writes one record [W | P hi | P lo | Ts^T |
+// scalars] per (chunk, value head) to the workspace, laid out exactly as the
+// walk kernel wants it in shared memory.
 //
 // gdn_chunk_walk (one CTA per (32-column slice, value head, sequence)): keeps
 // the fp32 state slice in registers; a producer warp streams K, Q, a 64-column
-// V box and the record into a two-stage ring with TMA / bulk copies, and eight
-// compute warps run the four products of a chunk on tcgen05 (TMEM
-// accumulators, smem operands): [W; Q] h, K^T (s v_new), [P_hi; P_lo] v_new
-// and Ts V, with v_new, the state update and o in the epilogues.
+// V box and the record into a two-stage ring with TMA / bulk copies; eight
+// compute warps issue the serial chain's products on tcgen05 (TMEM
+// accumulators, smem operands), W h, Ts V and K^T (s v_new), and run v_new,
+// the state update and o in the epilogues; two more warps issue Q h and
+// P v_new off the chain.  One long sequence is walked in up to four chunk
+// ranges, each later range's prep running beside the previous range's walk.
 //
 // Precision: the main terms of o (P v_new and Q h) and the state update split
 // their computed factor into bf16 hi + lo parts (the raw bf16 q, k, v are
-// exact); W, Ts and the h in W h are plain bf16; accumulation is fp32, and h,
-// A, T stay fp32.  Every mbarrier wait is bounded; on expiry a CTA records
-// GDN_DEV_WAIT_TIMEOUT, drains its outstanding copies and leaves.
+// exact), and W h takes h as hi + lo too; W and Ts are plain bf16;
+// accumulation is fp32, and h, A, T stay fp32.  Every mbarrier wait is bounded;
+// on expiry a CTA records GDN_DEV_WAIT_TIMEOUT, drains its outstanding copies
+// and leaves.
 #include <cuda.h>
 #include <string.h>
 
