@@ -1181,7 +1181,8 @@ cudaError_t chunk_ranges(int N, int T, int HV, int V, bool varlen, bool hsave, i
   *R = 1;
   bounds[0] = 0;
   bounds[1] = static_cast<int>(nc);
-  if (T <= 0 || hsave || !split_shape(N, T, varlen)) return cudaSuccess;
+  (void)hsave;  // a walk that saves the chunk states splits the same way (each range saves its own)
+  if (T <= 0 || !split_shape(N, T, varlen)) return cudaSuccess;
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

@@ -272,7 +272,8 @@ size_t gdn_chunk_bwd_workspace_size(int B, int T, int H, int HV, int K, int V,
  * chunk first, then the per-chunk gradients in parallel, then (HV > H) a pass
  * adding the later value heads' dq, dk shares in head order: up to five
  * launches (six with cu_seqlens, which also adds memsets of dq, dk and the
- * shares on `stream`).  Products run on the tensor cores with computed
+ * shares on `stream`; the recomputed forward of one long sequence takes
+ * gdn_chunk_fwd's chunk ranges, two launches each).  Products run on the tensor cores with computed
  * operands split into bf16 hi + lo parts (relative error near 2^-17 per
  * product, fp32 accumulation).  Every sum has a fixed order, so two runs on
  * the same inputs agree bit for bit.  Errors as gdn_chunk_fwd; q, k, v, do,

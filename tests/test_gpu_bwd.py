@@ -161,3 +161,27 @@ def test_bwd_four_value_heads_per_key_head_and_repeatable(K, varlen):
     second = gdn.gdn_chunk_bwd(*args, **kw)
     for a, b in zip(first, second):
         assert torch.equal(a, b)
+
+
+def test_bwd_long_single_sequence_matches_batched_bitwise():
+    # One sequence of 71 chunks: the recomputed forward takes the chunk ranges
+    # (each range's walk saving its own chunks' states).  The same sequence as
+    # the first of a batch of two recomputes in one range: the same gradients,
+    # bit for bit (the one-range path is the one the oracle tests above pin).
+    import gated_deltanet_chunked_chunk_gb300 as gdn
+    T = 64 * 70 + 20
+    case = W.prefill_case("bwd_long", 51, 1, T, 2, 4, 128, 128, init="all")
+    g, beta = P.oracle_gates(case)
+    gen = torch.Generator().manual_seed(1051)
+    do = torch.randn(1, T, 4, 128, generator=gen).to(torch.bfloat16)
+    dht = torch.randn(1, 4, 128, 128, generator=gen)
+    d = lambda t: t.to(DEV).contiguous()
+    two = lambda t: torch.cat([t, t.flip(1)], 0)
+    one = gdn.gdn_chunk_bwd(d(case.q), d(case.k), d(case.v), d(g), d(beta), d(do),
+                            initial_state=d(case.initial_state), dht=d(dht))
+    both = gdn.gdn_chunk_bwd(d(two(case.q)), d(two(case.k)), d(two(case.v)), d(two(g)), d(two(beta)), d(two(do)),
+                             initial_state=d(torch.cat([case.initial_state] * 2, 0)), dht=d(torch.cat([dht] * 2, 0)))
+    torch.cuda.synchronize()
+    for name, a, b in zip(["dq", "dk", "dv", "dg", "dbeta", "dh0"], one, both):
+        assert torch.equal(a, b[:1]), name
+    assert gdn.chunk_fwd_kernel_launches(1, T, 2, 4, 128, 128, 1, False) == 4
