@@ -213,6 +213,29 @@ def test_multi_range_call_captured_in_a_cuda_graph_matches_eager():
     assert torch.equal(h_g, h_e)
 
 
+def test_varlen_maximum_sequence_count():
+    # 65535 packed sequences (the largest count the walk's grid takes; one
+    # more is refused on the host) of 0 to 3 tokens each, every one with its
+    # own initial state: sampled sequences against the oracle, and the empty
+    # ones carry their initial state through unchanged.
+    N = 65535
+    rng = np.random.default_rng(60)
+    lens = [int(x) for x in rng.integers(0, 4, N)]
+    cu = W.cu_from_lengths(lens)
+    case = W.prefill_case("max_n", 60, 1, cu[-1], 1, 1, 64, 64, cu_seqlens=cu, init="all")
+    g, beta = P.oracle_gates(case)
+    o_gpu, ht_gpu = P.run_chunk_gpu(case, g, beta)
+    assert np.isfinite(o_gpu).all() and np.isfinite(ht_gpu).all()
+    empty = [n for n in range(N) if lens[n] == 0]
+    assert len(empty) > 1000
+    np.testing.assert_array_equal(ht_gpu[empty[:2000]], case.initial_state[empty[:2000]].numpy())
+    for n in [0, 1, 2, 3, 77, 4096, 32767, 40000, N - 2, N - 1] + [int(x) for x in rng.integers(0, N, 20)]:
+        o_ref, h_ref, (b0, sl) = P.oracle_single_head(case, g, beta, n, 0)
+        if lens[n]:
+            P.assert_o_close(o_gpu[b0:b0 + 1, sl, 0:1], o_ref[None, :, None], f"o seq {n}")
+        P.assert_state_close(ht_gpu[n:n + 1, 0:1], h_ref[None, None], f"state seq {n}")
+
+
 def test_deterministic_and_guard_bands():
     case = W.config1()
     g, beta = P.oracle_gates(case)
