@@ -106,6 +106,13 @@ def test_decode_config4_fused_gating():
     _decode_check(W.config4(), fused=True)
 
 
+def test_decode_maximum_request_count():
+    """65535 requests (the largest count its grid takes; one more is refused on
+    the host) against a pool of 70000 slots, about 10 % PAD: sampled requests
+    against the oracle, PAD outputs zero, untouched slots bit-exact."""
+    _decode_check(W.decode_case("dec_max_r", 61, 65535, 70000, 1, 1, 64, 64, pad_prob=0.1), fused=True, sample=200)
+
+
 def test_decode_bad_slot_flagged_and_skipped():
     gdn = _gdn()
     case = W.decode_case("bad", 77, 4, 6, 2, 2, 64, 64, pad_prob=0.0)
