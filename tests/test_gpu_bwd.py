@@ -185,3 +185,41 @@ def test_bwd_long_single_sequence_matches_batched_bitwise():
     for name, a, b in zip(["dq", "dk", "dv", "dg", "dbeta", "dh0"], one, both):
         assert torch.equal(a, b[:1]), name
     assert gdn.chunk_fwd_kernel_launches(1, T, 2, 4, 128, 128, 1, False) == 4
+
+
+def test_bwd_maximum_sequence_count_sampled():
+    # 65535 packed sequences of 0 to 3 tokens (the largest count the grids
+    # take), each with its own initial state and final-state gradient: sampled
+    # sequences against the oracle run on that sequence alone.
+    import gated_deltanet_chunked_chunk_gb300 as gdn
+    N = 65535
+    rng = np.random.default_rng(62)
+    lens = [int(x) for x in rng.integers(0, 4, N)]
+    cu = W.cu_from_lengths(lens)
+    case = W.prefill_case("bwd_max_n", 62, 1, cu[-1], 1, 1, 64, 64, cu_seqlens=cu, init="all")
+    g, beta = P.oracle_gates(case)
+    gen = torch.Generator().manual_seed(1062)
+    do = torch.randn(1, case.T, 1, 64, generator=gen).to(torch.bfloat16)
+    dht = torch.randn(N, 1, 64, 64, generator=gen)
+    d = lambda t: t.to(DEV).contiguous()
+    out = gdn.gdn_chunk_bwd(d(case.q), d(case.k), d(case.v), d(g), d(beta), d(do),
+                            initial_state=d(case.initial_state), cu_seqlens=d(case.cu_seqlens), dht=d(dht))
+    torch.cuda.synchronize()
+    dq, dk, dv, dg, db, dh0 = [x.cpu().numpy().astype(np.float64) for x in out]
+    picks = [0, 1, 2, 3, 77, 32767, N - 2, N - 1] + [int(x) for x in rng.integers(0, N, 24)]
+    checked = 0
+    for n in picks:
+        t0, t1 = cu[n], cu[n + 1]
+        if t1 == t0:
+            continue
+        sl = slice(t0, t1)
+        ref = BO.backward(case.q[:, sl].float().numpy(), case.k[:, sl].float().numpy(), case.v[:, sl].float().numpy(),
+                          g[:, sl].numpy(), beta[:, sl].numpy(), do[:, sl].float().numpy(),
+                          initial_state=case.initial_state[n:n + 1].numpy(), dht=dht[n:n + 1].numpy(),
+                          use_qk_l2norm=True)
+        got = [dq[:, sl], dk[:, sl], dv[:, sl], dg[:, sl], db[:, sl], dh0[n:n + 1]]
+        for name, x, r in zip(["dq", "dk", "dv", "dg", "dbeta", "dh0"], got, ref):
+            err = P.rel_l2(x, r)
+            assert err <= BWD_REL_L2, f"seq {n} {name}: rel-L2 {err:.3e}"
+        checked += 1
+    assert checked >= 20
